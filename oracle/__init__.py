@@ -1,0 +1,29 @@
+"""fp64 CPU oracle for the Kalman Delta Network (KDN) mixer.
+
+TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may use this package; the product path (the
+CUDA library and its Python binding) never imports or calls it, and this
+package imports nothing from the product.
+
+Contents
+  recurrence  -- ctypes wrapper over ``kdn_oracle.c``: the token-by-token fp64
+                 recurrence of Diagonal and Isotropic KDN (KDN paper Sec. 4.1,
+                 Eq. 23-27 and 60-65; Sec. 4.2, Eq. 40 and App. C).
+  dense       -- numpy fp64 companions used only on tiny inputs: the dense
+                 exact Kalman filter (KDN paper Sec. 3.2, Eq. 12-17; Bayesian
+                 Layer Prop. 1), the Moebius 2x2 matrices of the uncertainty
+                 recurrence (KDN paper Eq. 32-37) and the weighted ridge
+                 regression closed form (Preconditioned DeltaNet Eq. 1-5;
+                 Gated KalmaNet test-time ridge regression).
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+against printed values, closed forms, special-case reductions and brute force.
+"""
+from .recurrence import build_oracle, forward, step, library_path  # noqa: F401
+from .dense import (  # noqa: F401
+    dense_kalman,
+    mobius_matrices,
+    mobius_apply,
+    mobius_product,
+    ridge_closed_form,
+)
