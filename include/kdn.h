@@ -1,0 +1,177 @@
+/*
+ * kdn.h -- C ABI of the GB300 (sm_103a) Kalman Delta Network mixer library.
+ *
+ * The library computes the forward mixer of a Kalman Delta Network (KDN):
+ * "Kalman Delta Networks: Uncertainty-aware Associative Memory" (Bui, Huang,
+ * Ying, arXiv:2609.07816v1).  Per head it keeps a memory S (d_k x d_v, row =
+ * key channel) and an uncertainty state (d_k variances for the Diagonal
+ * variant, one scalar for the Isotropic variant), and for every token t:
+ *
+ *   predict   S_hat = diag(a_t) S,   a_t = exp(log_alpha_t)         (Sec. 3.2 Eq. 12)
+ *             Diagonal:  p_hat = a_t^2 * p + omega_t                (Sec. 4.1 Eq. 23)
+ *             Isotropic: b_hat = mean_i(a_t,i^2) * b + omega_t      (Sec. 4.2 Eq. 40)
+ *   gain      Diagonal:  kappa = p_hat * k / (r_t + sum_i p_hat_i k_i^2)   (Eq. 24-27)
+ *             Isotropic: kappa = k * b_hat / (r_t + b_hat ||k||^2)
+ *   write     S = S_hat + kappa (v_t - S_hat^T k_t)^T               (Eq. 13-16, 38-39)
+ *   read      o_t = S^T q_t            (after the write)            (Eq. 17)
+ *   update    Diagonal:  p = p_hat / (1 + (mu / r_t) k^2 * p_hat)   (Eq. 60-65)
+ *             Isotropic: b = b_hat / (1 + mu ||k||^2 / (d_k r_t) * b_hat)   (App. C)
+ *
+ * The uncertainty recurrence is a Moebius map evaluated as a 2x2 associative
+ * scan (Eq. 32-37); the memory write is evaluated chunk by chunk in the
+ * compact-WY / UT form (App. D).  Results do not depend on the chunk length
+ * beyond floating-point rounding.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or retains them and keeps no global mutable state
+ *     (re-entrant; concurrent calls on different streams with disjoint buffers
+ *     are safe).
+ *   - Layouts are dense row-major with the feature dimension innermost:
+ *       q, k, log_alpha       [B, T, H, d_k]
+ *       v, o                  [B, T, H, d_v]
+ *       omega                 [B, T, H, d_k] (Diagonal) or [B, T, H] (Isotropic)
+ *       r                     [B, T, H]   observation-noise VARIANCE, > 0
+ *       S0, S_T, S            [B, H, d_k, d_v] fp32
+ *       p0, p_T, p            [B, H, d_k] (Diagonal) or [B, H] (Isotropic) fp32
+ *     q, k, v and o are stored as io_dtype (KDN_F32 or KDN_BF16); every other
+ *     tensor is fp32.  Arithmetic is fp32 (tensor-core operands bf16 on the
+ *     bf16 path, fp32 accumulation and fp32 state).
+ *   - Every pointer must be 16-byte aligned.
+ *   - Outputs must not overlap inputs, except S_T == S0 and p_T == p0 (resume
+ *     in place), which are allowed.
+ *   - mu < 0 selects mu = d_k (the paper's default information scale).
+ *   - Host-side validation runs before anything is enqueued and returns
+ *     synchronously.  Kernels are enqueued on `stream`; the call returns
+ *     without synchronising.  A launch failure returns KDN_ERR_CUDA.
+ *   - Conditions found on the device (a bounded wait that gave up, a chunk
+ *     whose cumulative log-decay is outside the safe range) are recorded in a
+ *     status word at the start of the workspace; kdn_read_device_status()
+ *     returns it.  No kernel traps, asserts, prints or spins without bound.
+ *   - Nothing throws across the ABI.
+ */
+#ifndef KDN_H
+#define KDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *kdn_stream_t;
+
+typedef enum {
+    KDN_OK = 0,
+    KDN_ERR_NULL = 1,         /* a required pointer is NULL                          */
+    KDN_ERR_SHAPE = 2,        /* a size is negative, or sizes are inconsistent       */
+    KDN_ERR_DTYPE = 3,        /* io_dtype is not KDN_F32 or KDN_BF16                 */
+    KDN_ERR_ALIGN = 4,        /* a pointer is not 16-byte aligned                    */
+    KDN_ERR_WORKSPACE = 5,    /* workspace NULL or smaller than kdn_workspace_size() */
+    KDN_ERR_UNSUPPORTED = 6,  /* d_k, d_v or chunk outside the supported set         */
+    KDN_ERR_CUDA = 7,         /* a CUDA runtime call or kernel launch failed         */
+    KDN_ERR_TIMEOUT = 8,      /* device: a bounded wait gave up (results invalid)    */
+    KDN_ERR_RANGE = 9,        /* device: a chunk's cumulative log-decay left the
+                                 range the factored decay supports (results invalid) */
+    KDN_ERR_ALIAS = 10        /* an output overlaps an input (other than S/p resume) */
+} kdn_status;
+
+typedef enum { KDN_F32 = 0, KDN_BF16 = 1 } kdn_dtype;
+typedef enum { KDN_DIAG = 0, KDN_ISO = 1 } kdn_variant;
+
+/* Flags for the forward calls. */
+#define KDN_FLAG_PORTABLE 0x1u   /* force the CUDA-core (FFMA) chunk path */
+
+/*
+ * Supported sizes: d_k, d_v in {16, 32, 64, 128}; chunk in {16, 32, 64}
+ * (0 selects 64, or T rounded up to 16 when T < 64); any T >= 0 (a ragged
+ * tail chunk is masked; T == 0 copies the initial state to the outputs);
+ * B, H >= 0.  The tensor-core path is used for bf16 io with d_k = d_v = 128
+ * and chunk 64; every other supported case runs on the CUDA-core path.
+ */
+
+/*
+ * Bytes of device workspace a forward (T > 0) or step (T == 1) call needs.
+ * variant: KDN_DIAG or KDN_ISO.  Returns 0 for unsupported arguments.  The
+ * workspace is scratch owned by the caller, at least 256-byte aligned; its
+ * first 256 bytes hold the device status word.  Calls that overlap in time
+ * must use different workspaces.
+ */
+size_t kdn_workspace_size(int variant, int B, int T, int H, int dk, int dv, int chunk,
+                          int io_dtype, uint32_t flags);
+
+/*
+ * Diagonal KDN forward over T tokens (KDN paper Sec. 4.1, Eq. 23-30 and
+ * 60-65; Moebius scan Eq. 32-37; chunkwise form App. D).
+ *
+ * Inputs : q, k [B,T,H,dk] io_dtype; v [B,T,H,dv] io_dtype;
+ *          log_alpha [B,T,H,dk] (log of the per-channel decay, <= 0 in use);
+ *          omega [B,T,H,dk] process-noise variance >= 0; r [B,T,H] > 0;
+ *          S0 [B,H,dk,dv] or NULL (zero memory); p0 [B,H,dk] or NULL (ones).
+ * Outputs: o [B,T,H,dv] io_dtype (read after each token's write);
+ *          S_T [B,H,dk,dv], p_T [B,H,dk]: the state after token T-1 (the
+ *          mu-scaled posterior variances), the resume point for kdn_step or
+ *          a later forward call.
+ * mu     : information scale (< 0 selects d_k); chunk: see above.
+ * Errors : KDN_ERR_* from validation, KDN_ERR_CUDA on a launch failure.
+ */
+kdn_status kdn_diag_forward(int B, int T, int H, int dk, int dv, int chunk, float mu,
+                            int io_dtype, uint32_t flags,
+                            const void *q, const void *k, const void *v,
+                            const float *log_alpha, const float *omega, const float *r,
+                            const float *S0, const float *p0,
+                            void *o, float *S_T, float *p_T,
+                            void *workspace, size_t workspace_bytes, kdn_stream_t stream);
+
+/*
+ * Isotropic KDN forward (KDN paper Sec. 4.2, Eq. 40; App. C): one
+ * uncertainty scalar per head, omega [B,T,H], p0 and p_T [B,H].  The mean
+ * path keeps the per-channel transition diag(a_t).  Everything else as
+ * kdn_diag_forward.
+ */
+kdn_status kdn_iso_forward(int B, int T, int H, int dk, int dv, int chunk, float mu,
+                           int io_dtype, uint32_t flags,
+                           const void *q, const void *k, const void *v,
+                           const float *log_alpha, const float *omega, const float *r,
+                           const float *S0, const float *p0,
+                           void *o, float *S_T, float *p_T,
+                           void *workspace, size_t workspace_bytes, kdn_stream_t stream);
+
+/*
+ * Single-token decode for B independent sequences (the recurrent form of
+ * the same recurrence; KDN paper Sec. 5.1 and App. C): one token per
+ * (sequence, head), state updated IN PLACE.
+ *
+ * variant: KDN_DIAG or KDN_ISO.
+ * Inputs : q, k [B,H,dk] io_dtype; v [B,H,dv] io_dtype; log_alpha [B,H,dk];
+ *          omega [B,H,dk] (Diagonal) or [B,H] (Isotropic); r [B,H].
+ * In/out : S [B,H,dk,dv], p [B,H,dk] or [B,H] (fp32).
+ * Output : o [B,H,dv] io_dtype.
+ * Workspace: kdn_workspace_size(variant, B, 1, H, dk, dv, 0, io_dtype, 0) bytes.
+ */
+kdn_status kdn_step(int variant, int B, int H, int dk, int dv, float mu, int io_dtype,
+                    const void *q, const void *k, const void *v,
+                    const float *log_alpha, const float *omega, const float *r,
+                    float *S, float *p, void *o,
+                    void *workspace, size_t workspace_bytes, kdn_stream_t stream);
+
+/*
+ * Synchronise `stream` and return the device status word the last call that
+ * used `workspace` left there: KDN_OK, KDN_ERR_TIMEOUT or KDN_ERR_RANGE (or
+ * KDN_ERR_CUDA if the copy itself fails, KDN_ERR_NULL for a NULL workspace).
+ */
+kdn_status kdn_read_device_status(const void *workspace, kdn_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char *kdn_status_string(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+int kdn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDN_H */

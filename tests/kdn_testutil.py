@@ -1,0 +1,54 @@
+"""Helpers shared by the GPU parity tests: error metrics and host/device moves.
+
+Error metrics (the tolerances the tests assert):
+  max_rel        max_i |x_i - y_i| / max(|y_i|, 1e-2 * rms(y)); the floor keeps
+                 entries near zero from dominating.  fp32 path bound: 1e-4.
+  norm_max_abs   max_i |x_i - y_i| / max_i |y_i|.  bf16-io path bound: 2e-2.
+"""
+import numpy as np
+import torch
+
+FP32_TOL = 1e-4
+BF16_TOL = 2e-2
+NAMES = ("q", "k", "v", "log_alpha", "omega", "r")
+
+
+def max_rel(x, y):
+    x = np.asarray(x, np.float64)
+    y = np.asarray(y, np.float64)
+    if y.size == 0:
+        return 0.0
+    floor = 1e-2 * np.sqrt(np.mean(y * y)) + 1e-300
+    return float(np.max(np.abs(x - y) / np.maximum(np.abs(y), floor)))
+
+
+def norm_max_abs(x, y):
+    x = np.asarray(x, np.float64)
+    y = np.asarray(y, np.float64)
+    if y.size == 0:
+        return 0.0
+    return float(np.max(np.abs(x - y)) / max(np.max(np.abs(y)), 1e-300))
+
+
+def err(x, y, io):
+    return max_rel(x, y) if io == "f32" else norm_max_abs(x, y)
+
+
+def tol(io):
+    return FP32_TOL if io == "f32" else BF16_TOL
+
+
+def to_device(x, dev="cuda:0"):
+    """numpy inputs (fp32 storage, bf16-valued for io == 'bf16') -> torch CUDA tensors."""
+    io = x["io"]
+    out = {}
+    for n in NAMES:
+        t = torch.from_numpy(np.ascontiguousarray(x[n]))
+        if n in ("q", "k", "v") and io == "bf16":
+            t = t.to(torch.bfloat16)   # exact: the values are bf16-representable
+        out[n] = t.to(dev)
+    return out
+
+
+def to_host(t):
+    return t.detach().float().cpu().numpy()

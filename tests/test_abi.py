@@ -1,0 +1,121 @@
+"""The C-ABI library loads and exports every entry point include/kdn.h declares.
+
+These tests run without a GPU: they only load the library, read constants
+and exercise host-side validation on arguments that are rejected before
+anything is enqueued (so no CUDA call is ever reached).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "kdn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(kdn_[a-z_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from uncertainty_aware_delta_gb300.build import build_library
+    import uncertainty_aware_delta_gb300 as kdn
+
+    build_library()
+    return kdn.library()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("kdn_diag_forward", "kdn_iso_forward", "kdn_step", "kdn_workspace_size",
+              "kdn_read_device_status", "kdn_status_string", "kdn_abi_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(lib._name)
+    for n in _declared_functions():
+        assert hasattr(raw, n), f"{n} declared in kdn.h but not exported"
+
+
+def test_status_strings_and_version(lib):
+    import uncertainty_aware_delta_gb300 as kdn
+
+    assert lib.kdn_abi_version() == 100
+    for code in range(0, 11):
+        s = kdn.status_string(code)
+        assert s and s != "unknown status"
+    assert kdn.status_string(99) == "unknown status"
+
+
+def test_workspace_size_rules(lib):
+    import uncertainty_aware_delta_gb300 as kdn
+
+    ws = kdn.workspace_size
+    # unsupported sizes are rejected with 0
+    assert ws(0, 1, 64, 2, 24, 16, 16, 0, 0) == 0
+    assert ws(0, 1, 64, 2, 16, 16, 48, 0, 0) == 0
+    assert ws(0, -1, 64, 2, 16, 16, 16, 0, 0) == 0
+    assert ws(2, 1, 64, 2, 16, 16, 16, 0, 0) == 0
+    assert ws(0, 1, 64, 2, 16, 16, 16, 5, 0) == 0
+    # the portable path stores gains [B,T,H,dk] fp32 plus the scan summaries
+    n = ws(0, 2, 100, 3, 32, 16, 16, 0, 1)
+    assert n >= 256 + 4 * 2 * 100 * 3 * 32
+    assert n % 256 == 0
+    # decode needs only the status word
+    assert ws(0, 256, 1, 16, 128, 128, 0, 0, 1) >= 256
+
+
+def _fwd_args(**over):
+    a = dict(B=1, T=64, H=2, dk=16, dv=16, chunk=16, mu=-1.0, io=0, flags=0,
+             q=64, k=64, v=64, la=64, om=64, r=64, S0=None, p0=None, o=1 << 20, S_T=2 << 20,
+             p_T=3 << 20, ws=4 << 20, wsb=1 << 20)
+    a.update(over)
+    return a
+
+
+def _call(lib, a, variant=0):
+    fn = lib.kdn_diag_forward if variant == 0 else lib.kdn_iso_forward
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return fn(a["B"], a["T"], a["H"], a["dk"], a["dv"], a["chunk"], a["mu"], a["io"], a["flags"],
+              vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["la"]), vp(a["om"]), vp(a["r"]), vp(a["S0"]),
+              vp(a["p0"]), vp(a["o"]), vp(a["S_T"]), vp(a["p_T"]), vp(a["ws"]), a["wsb"], None)
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+def test_validation_rejects_before_launch(lib, variant):
+    # each case fails a host check, so nothing reaches the device
+    assert _call(lib, _fwd_args(dk=24), variant) == 6          # KDN_ERR_UNSUPPORTED
+    assert _call(lib, _fwd_args(chunk=8), variant) == 6
+    assert _call(lib, _fwd_args(io=3), variant) == 3           # KDN_ERR_DTYPE
+    assert _call(lib, _fwd_args(T=-1), variant) == 2           # KDN_ERR_SHAPE
+    assert _call(lib, _fwd_args(q=None), variant) == 1         # KDN_ERR_NULL
+    assert _call(lib, _fwd_args(S_T=None), variant) == 1
+    assert _call(lib, _fwd_args(ws=None), variant) == 5        # KDN_ERR_WORKSPACE
+    assert _call(lib, _fwd_args(wsb=16), variant) == 5
+    assert _call(lib, _fwd_args(k=72), variant) == 4           # KDN_ERR_ALIGN (72 % 16 != 0)
+    assert _call(lib, _fwd_args(o=64 + 16), variant) == 10     # KDN_ERR_ALIAS (o overlaps q)
+    assert _call(lib, _fwd_args(ws=1 << 20), variant) == 10    # workspace overlaps o
+
+
+def test_step_validation_rejects_before_launch(lib):
+    vp = ctypes.c_void_p
+    base = [0, 4, 2, 16, 16, -1.0, 0]
+    ptrs = [vp(1 << 12), vp(2 << 12), vp(3 << 12), vp(4 << 12), vp(5 << 12), vp(6 << 12),
+            vp(1 << 20), vp(2 << 20), vp(3 << 20)]
+    ws = [vp(4 << 20), 256, None]
+    assert lib.kdn_step(*base, *ptrs, None, 256, None) == 5
+    assert lib.kdn_step(*base, *ptrs, vp(4 << 20), 8, None) == 5
+    bad = list(base)
+    bad[3] = 48
+    assert lib.kdn_step(*bad, *ptrs, *ws) == 6
+    p2 = list(ptrs)
+    p2[6] = vp((1 << 20) + 8)
+    assert lib.kdn_step(*base, *p2, *ws) == 4
+    p3 = list(ptrs)
+    p3[8] = vp((1 << 20) + 64)                               # o overlaps S
+    assert lib.kdn_step(*base, *p3, *ws) == 10

@@ -1,0 +1,204 @@
+"""GPU forward parity against the fp64 oracle (Diagonal and Isotropic KDN).
+
+The CUDA path is called through the C ABI (the ctypes binding); the oracle
+runs the token-by-token recurrence on the same rounded inputs.  Shapes span
+several chunks and a ragged tail; edge cases cover T = 0, given initial
+states, in-place resume, the chunk-length invariance and split-sequence
+continuation.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from kdn_testutil import err, to_device, to_host, tol
+from uncertainty_aware_delta_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _kdn():
+    import uncertainty_aware_delta_gb300 as kdn
+    from uncertainty_aware_delta_gb300.build import build_library
+
+    build_library()
+    return kdn
+
+
+def _run(kdn, variant, t, **kw):
+    fn = kdn.kdn_diag_forward if variant == "diag" else kdn.kdn_iso_forward
+    return fn(t["q"], t["k"], t["v"], t["log_alpha"], t["omega"], t["r"], **kw)
+
+
+def _check(variant, x, got, ref, io, what=""):
+    o, S_T, p_T = (to_host(a) for a in got)
+    e = {"o": err(o, ref["o"], io), "S_T": err(S_T, ref["S_T"], io), "p_T": err(p_T, ref["p_T"], io)}
+    bound = tol(io)
+    assert all(v <= bound for v in e.values()), (variant, what, e)
+    return e
+
+
+CASES = [
+    # variant, B, T, H, dk, dv, chunk, io, mu
+    ("diag", 1, 64, 2, 16, 16, 16, "f32", None),
+    ("iso", 1, 64, 2, 16, 16, 16, "f32", None),
+    ("diag", 2, 100, 3, 32, 64, 32, "f32", None),       # ragged tail
+    ("iso", 2, 100, 3, 64, 32, 16, "f32", 1.0),
+    ("diag", 1, 200, 2, 128, 128, 64, "f32", 1.0),
+    ("diag", 2, 77, 2, 64, 64, 64, "f32", 0.0),
+    ("iso", 1, 150, 2, 128, 128, 64, "f32", None),
+    ("diag", 2, 300, 2, 128, 128, 64, "bf16", None),
+    ("iso", 2, 300, 2, 128, 128, 64, "bf16", None),
+    ("diag", 1, 1, 3, 128, 128, 64, "f32", None),       # a single token
+    ("diag", 1, 17, 1, 16, 128, 16, "bf16", None),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
+def test_forward_matches_oracle(case):
+    variant, B, T, H, dk, dv, chunk, io, mu = case
+    kdn = _kdn()
+    x = make_inputs(variant, B, T, H, dk, dv, io=io, seed=1000 + T + dk)
+    t = to_device(x)
+    got = _run(kdn, variant, t, chunk=chunk, mu=mu)
+    ref = oracle.forward(variant, x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"], mu=mu)
+    _check(variant, x, got, ref, io)
+
+
+@pytest.mark.parametrize("variant", ["diag", "iso"])
+def test_initial_state_and_in_place_resume(variant):
+    import torch
+
+    kdn = _kdn()
+    B, T, H, dk, dv = 2, 90, 2, 64, 64
+    x = make_inputs(variant, B, T, H, dk, dv, io="f32", seed=5)
+    rng = np.random.default_rng(6)
+    S0 = (0.3 * rng.standard_normal((B, H, dk, dv))).astype(np.float32)
+    p0 = rng.uniform(0.2, 2.0, size=(B, H, dk) if variant == "diag" else (B, H)).astype(np.float32)
+    t = to_device(x)
+    S0d, p0d = torch.from_numpy(S0).cuda(), torch.from_numpy(p0).cuda()
+    ref = oracle.forward(variant, x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"], S0=S0, p0=p0)
+    got = _run(kdn, variant, t, S0=S0d, p0=p0d, chunk=32)
+    _check(variant, x, got, ref, "f32", "given state")
+    # resume in place: S_T and p_T alias S0 and p0
+    o = torch.empty_like(got[0])
+    got2 = _run(kdn, variant, t, S0=S0d, p0=p0d, chunk=32, out=(o, S0d, p0d))
+    _check(variant, x, got2, ref, "f32", "in place")
+
+
+@pytest.mark.parametrize("variant", ["diag", "iso"])
+def test_chunk_length_does_not_change_the_result(variant):
+    kdn = _kdn()
+    x = make_inputs(variant, 1, 130, 2, 64, 64, io="f32", seed=9)
+    t = to_device(x)
+    ref = oracle.forward(variant, x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"])
+    outs = [_run(kdn, variant, t, chunk=c) for c in (16, 32, 64)]
+    for got in outs:
+        _check(variant, x, got, ref, "f32")
+    for a, b in zip(outs[0], outs[2]):
+        assert np.max(np.abs(to_host(a) - to_host(b))) <= 1e-4 * max(1.0, np.max(np.abs(to_host(b))))
+
+
+@pytest.mark.parametrize("variant", ["diag", "iso"])
+def test_split_sequence_continuation(variant):
+    import torch
+
+    kdn = _kdn()
+    x = make_inputs(variant, 2, 150, 2, 32, 32, io="f32", seed=11)
+    t = to_device(x)
+    T1 = 70
+    first = {n: v[:, :T1].contiguous() for n, v in t.items()}
+    second = {n: v[:, T1:].contiguous() for n, v in t.items()}
+    o1, S1, p1 = _run(kdn, variant, first, chunk=32)
+    o2, S2, p2 = _run(kdn, variant, second, S0=S1, p0=p1, chunk=32)
+    ref = oracle.forward(variant, x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"])
+    _check(variant, x, (torch.cat([o1, o2], 1), S2, p2), ref, "f32", "continuation")
+
+
+@pytest.mark.parametrize("variant", ["diag", "iso"])
+def test_empty_sequence_copies_state(variant):
+    import torch
+
+    kdn = _kdn()
+    B, H, d = 2, 3, 32
+    x = make_inputs(variant, B, 0, H, d, d, io="f32", seed=1)
+    t = to_device(x)
+    S0 = torch.randn(B, H, d, d, device="cuda")
+    pshape = (B, H, d) if variant == "diag" else (B, H)
+    p0 = torch.rand(pshape, device="cuda") + 0.5
+    o, S_T, p_T = _run(kdn, variant, t, S0=S0, p0=p0)
+    assert o.shape == (B, 0, H, d)
+    assert torch.equal(S_T, S0) and torch.equal(p_T, p0)
+    o, S_T, p_T = _run(kdn, variant, t)
+    assert torch.count_nonzero(S_T) == 0 and torch.all(p_T == 1.0)
+
+
+def test_empty_batch_is_a_no_op():
+    kdn = _kdn()
+    x = make_inputs("diag", 0, 10, 2, 16, 16, io="f32", seed=1)
+    o, S_T, p_T = _run(kdn, "diag", to_device(x))
+    assert o.numel() == 0 and S_T.numel() == 0 and p_T.numel() == 0
+
+
+def test_device_status_is_ok_after_a_normal_call():
+    import torch
+
+    kdn = _kdn()
+    x = make_inputs("diag", 1, 64, 1, 16, 16, io="f32", seed=2)
+    t = to_device(x)
+    ws = torch.empty(kdn.workspace_size(0, 1, 64, 1, 16, 16, 16, 0, 0), dtype=torch.uint8, device="cuda")
+    _run(kdn, "diag", t, chunk=16, workspace=ws)
+    assert kdn.kdn_read_device_status(ws) == 0
+
+
+def test_extreme_decay_is_reported_not_faulted():
+    """A chunk whose cumulative log-decay exceeds the supported range sets the
+    device status word (KDN_ERR_RANGE); the call itself completes."""
+    import torch
+
+    kdn = _kdn()
+    x = make_inputs("diag", 1, 64, 1, 16, 16, io="f32", seed=3)
+    x["log_alpha"][:] = -5.0     # 64 tokens x 5 = 320 > 160
+    t = to_device(x)
+    ws = torch.empty(kdn.workspace_size(0, 1, 64, 1, 16, 16, 64, 0, 0), dtype=torch.uint8, device="cuda")
+    _run(kdn, "diag", t, chunk=64, workspace=ws)
+    assert kdn.kdn_read_device_status(ws) == 9
+
+
+# ------------------------------------------------------------ full-size workloads
+def _sampled_parity(name, variant, seqs):
+    """Run a full-size workload on the GPU in the benchmark's launch
+    configuration and compare the sampled (b, h) sequences with the oracle."""
+    kdn = _kdn()
+    w = WORKLOADS[name]
+    x = workload_inputs(w, variant)
+    t = to_device(x)
+    got = _run(kdn, variant, t, chunk=w.chunk)
+    o, S_T, p_T = (to_host(a) for a in got)
+    errs = []
+    for b, h in seqs:
+        sl = lambda a: a[b:b + 1, :, h:h + 1]
+        ref = oracle.forward(variant, sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["log_alpha"]),
+                             sl(x["omega"]), sl(x["r"]))
+        e = (err(o[b:b + 1, :, h:h + 1], ref["o"], w.io), err(S_T[b:b + 1, h:h + 1], ref["S_T"], w.io),
+             err(p_T[b:b + 1, h:h + 1], ref["p_T"], w.io))
+        errs.append(e)
+        assert max(e) <= tol(w.io), (name, variant, b, h, e)
+    assert np.all(np.isfinite(o))
+    return errs
+
+
+@pytest.mark.parametrize("variant", ["diag", "iso"])
+def test_full_size_b8h16t4096(variant):
+    _sampled_parity("diag-bf16-b8h16t4096d128" if variant == "diag" else "iso-bf16-b8h16t4096d128",
+                    variant, [(0, 0), (7, 15), (3, 9)])
+
+
+@pytest.mark.parametrize("variant", ["diag", "iso"])
+def test_full_size_long_context(variant):
+    _sampled_parity("diag-bf16-b1h16t65536d128", variant, [(0, 5)])
+
+
+def test_small_workload_every_output():
+    w = WORKLOADS["diag-f32-b1h2t64d16"]
+    _sampled_parity(w.name, "diag", [(0, 0), (0, 1)])
+    _sampled_parity(w.name, "iso", [(0, 0), (0, 1)])

@@ -1,0 +1,108 @@
+"""GPU decode (kdn_step) parity against the fp64 oracle.
+
+A prefill runs through the forward path, then single-token steps update the
+state in place; the oracle runs the whole token sequence in one recurrence.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from kdn_testutil import err, max_rel, to_device, to_host, tol
+from uncertainty_aware_delta_gb300.inputs import WORKLOADS, decode_step_inputs, make_inputs, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _kdn():
+    import uncertainty_aware_delta_gb300 as kdn
+    from uncertainty_aware_delta_gb300.build import build_library
+
+    build_library()
+    return kdn
+
+
+def _prefill_then_steps(kdn, variant, x, prefill, steps, chunk=64, check_every=1, seqs=None):
+    import torch
+
+    t = to_device(x)
+    fwd = kdn.kdn_diag_forward if variant == "diag" else kdn.kdn_iso_forward
+    pre = {n: v[:, :prefill].contiguous() for n, v in t.items()}
+    _, S, p = fwd(pre["q"], pre["k"], pre["v"], pre["log_alpha"], pre["omega"], pre["r"], chunk=chunk)
+    ws = torch.empty(kdn.workspace_size(0, S.shape[0], 1, S.shape[1], S.shape[2], S.shape[3]),
+                     dtype=torch.uint8, device="cuda")
+    outs = []
+    for s in range(steps):
+        tt = prefill + s
+        o = kdn.kdn_step(variant, *(t[n][:, tt].contiguous() for n in ("q", "k", "v", "log_alpha", "omega", "r")),
+                         S, p, workspace=ws)
+        outs.append(o.clone())
+    torch.cuda.synchronize()
+    return torch.stack(outs, 1), S, p
+
+
+CASES = [("diag", 3, 2, 128, 128, "f32"), ("iso", 3, 2, 128, 128, "f32"), ("diag", 2, 3, 16, 64, "f32"),
+         ("iso", 2, 2, 64, 32, "f32"), ("diag", 2, 2, 128, 128, "bf16"), ("iso", 2, 2, 32, 128, "bf16")]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
+def test_steps_after_prefill(case):
+    variant, B, H, dk, dv, io = case
+    kdn = _kdn()
+    prefill, steps = 40, 12
+    x = make_inputs(variant, B, prefill + steps, H, dk, dv, io=io, seed=77 + dk)
+    o, S, p = _prefill_then_steps(kdn, variant, x, prefill, steps, chunk=16)
+    ref = oracle.forward(variant, x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"])
+    assert err(to_host(o), ref["o"][:, prefill:], io) <= tol(io)
+    assert err(to_host(S), ref["S_T"], io) <= tol(io)
+    assert err(to_host(p), ref["p_T"], io) <= tol(io)
+
+
+def test_step_from_zero_state_is_one_token_forward():
+    import torch
+
+    kdn = _kdn()
+    x = make_inputs("diag", 4, 1, 3, 64, 64, io="f32", seed=3)
+    t = to_device(x)
+    S = torch.zeros(4, 3, 64, 64, device="cuda")
+    p = torch.ones(4, 3, 64, device="cuda")
+    o = kdn.kdn_step("diag", *(t[n][:, 0].contiguous() for n in ("q", "k", "v", "log_alpha", "omega", "r")), S, p)
+    ref = oracle.forward("diag", x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"])
+    assert max_rel(to_host(o), ref["o"][:, 0]) <= 1e-4
+    assert max_rel(to_host(S), ref["S_T"]) <= 1e-4
+    assert max_rel(to_host(p), ref["p_T"]) <= 1e-4
+
+
+def test_decode_workload_sampled():
+    """The decode workload at full size (256 sequences x 16 heads, d = 128,
+    512-token prefill, 1024 steps): sampled sequences against the oracle."""
+    import torch
+
+    kdn = _kdn()
+    w = WORKLOADS["diag-decode-f32-s256h16d128"]
+    seqs = [(0, 0), (255, 15), (100, 7)]
+    x = workload_inputs(w)
+    t = to_device(x)
+    _, S, p = kdn.kdn_diag_forward(t["q"], t["k"], t["v"], t["log_alpha"], t["omega"], t["r"],
+                                   chunk=w.chunk)
+    del t
+    ws = torch.empty(kdn.workspace_size(0, w.B, 1, w.H, w.d, w.d), dtype=torch.uint8, device="cuda")
+    names = ("q", "k", "v", "log_alpha", "omega", "r")
+    host = {n: [x[n][b:b + 1, :, h:h + 1] for b, h in seqs] for n in names}
+    outs = []
+    for s in range(w.steps):
+        y = decode_step_inputs(w, s)
+        ty = to_device(y)
+        o = kdn.kdn_step("diag", *(ty[n][:, 0] for n in names), S, p, workspace=ws)
+        outs.append(torch.stack([o[b, h] for b, h in seqs]))
+        for n in names:
+            for j, (b, h) in enumerate(seqs):
+                host[n][j] = np.concatenate([host[n][j], y[n][b:b + 1, :, h:h + 1]], axis=1)
+    torch.cuda.synchronize()
+    o = to_host(torch.stack(outs, 1))          # [len(seqs), steps, dv]
+    S, p = to_host(S), to_host(p)
+    for j, (b, h) in enumerate(seqs):
+        ref = oracle.forward("diag", *(host[n][j] for n in names))
+        assert max_rel(o[j], ref["o"][0, w.prefill:, 0]) <= 1e-4, (b, h)
+        assert max_rel(S[b, h], ref["S_T"][0, 0]) <= 1e-4
+        assert max_rel(p[b, h], ref["p_T"][0, 0]) <= 1e-4
+    assert np.all(np.isfinite(o))

@@ -1,0 +1,206 @@
+"""Thin ctypes binding over ``libkdn.so`` (include/kdn.h).
+
+Argument marshalling only: every step of the mixer runs in the library's
+CUDA kernels.  Tensors are PyTorch CUDA tensors (PyTorch supplies device
+memory and the current stream); there is no CPU fallback, and a missing
+library raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkdn.so")
+_lock = threading.Lock()
+_lib = None
+
+KDN_F32, KDN_BF16 = 0, 1
+KDN_DIAG, KDN_ISO = 0, 1
+KDN_FLAG_PORTABLE = 0x1
+
+EXPORTED = (
+    "kdn_workspace_size", "kdn_diag_forward", "kdn_iso_forward", "kdn_step",
+    "kdn_read_device_status", "kdn_status_string", "kdn_abi_version",
+)
+
+
+class KDNError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _PATH
+
+
+def library():
+    """Load libkdn.so (once); raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_PATH):
+                raise RuntimeError(
+                    f"{_PATH} is missing: build it with uncertainty_aware_delta_gb300.build.build_library() "
+                    "(there is no fallback implementation)")
+            lib = ctypes.CDLL(_PATH)
+            vp, fp, i32, u32, f32, sz = (ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                         ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t)
+            lib.kdn_workspace_size.restype = sz
+            lib.kdn_workspace_size.argtypes = [i32] * 8 + [u32]
+            fwd = [i32] * 6 + [f32, i32, u32] + [vp] * 3 + [fp] * 5 + [vp, fp, fp] + [vp, sz, vp]
+            for name in ("kdn_diag_forward", "kdn_iso_forward"):
+                getattr(lib, name).restype = i32
+                getattr(lib, name).argtypes = fwd
+            lib.kdn_step.restype = i32
+            lib.kdn_step.argtypes = [i32] * 5 + [f32, i32] + [vp] * 3 + [fp] * 3 + [fp, fp, vp] + [vp, sz, vp]
+            lib.kdn_read_device_status.restype = i32
+            lib.kdn_read_device_status.argtypes = [vp, vp]
+            lib.kdn_status_string.restype = ctypes.c_char_p
+            lib.kdn_status_string.argtypes = [i32]
+            lib.kdn_abi_version.restype = i32
+            lib.kdn_abi_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return library().kdn_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype, shape, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_size(variant, B, T, H, dk, dv, chunk=0, io=KDN_BF16, flags=0) -> int:
+    return int(library().kdn_workspace_size(variant, B, T, H, dk, dv, chunk, io, flags))
+
+
+def _forward(variant, q, k, v, log_alpha, omega, r, S0, p0, mu, chunk, flags, out, workspace,
+             stream):
+    lib = library()
+    device = q.device
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    io = KDN_BF16 if q.dtype == torch.bfloat16 else KDN_F32
+    iot = torch.bfloat16 if io == KDN_BF16 else torch.float32
+    nu = (dk,) if variant == KDN_DIAG else ()
+    _check(q, "q", iot, (B, T, H, dk), device)
+    _check(k, "k", iot, (B, T, H, dk), device)
+    _check(v, "v", iot, (B, T, H, dv), device)
+    _check(log_alpha, "log_alpha", torch.float32, (B, T, H, dk), device)
+    _check(omega, "omega", torch.float32, (B, T, H) + nu, device)
+    _check(r, "r", torch.float32, (B, T, H), device)
+    _check(S0, "S0", torch.float32, (B, H, dk, dv), device)
+    _check(p0, "p0", torch.float32, (B, H) + nu, device)
+    if out is None:
+        o = torch.empty((B, T, H, dv), dtype=iot, device=device)
+        S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=device)
+        p_T = torch.empty((B, H) + nu, dtype=torch.float32, device=device)
+    else:
+        o, S_T, p_T = out
+        _check(o, "o", iot, (B, T, H, dv), device)
+        _check(S_T, "S_T", torch.float32, (B, H, dk, dv), device)
+        _check(p_T, "p_T", torch.float32, (B, H) + nu, device)
+    need = lib.kdn_workspace_size(variant, B, T, H, dk, dv, chunk, io, flags)
+    if need == 0:
+        raise KDNError(6, "kdn_workspace_size rejected the arguments")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds {workspace.numel()} bytes, {need} needed")
+    fn = lib.kdn_diag_forward if variant == KDN_DIAG else lib.kdn_iso_forward
+    mu = -1.0 if mu is None else float(mu)
+    with torch.cuda.device(device):
+        st = fn(B, T, H, dk, dv, int(chunk), mu, io, int(flags), _ptr(q), _ptr(k), _ptr(v),
+                _ptr(log_alpha), _ptr(omega), _ptr(r), _ptr(S0), _ptr(p0), _ptr(o), _ptr(S_T),
+                _ptr(p_T), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                _stream(stream, device))
+    if st != 0:
+        raise KDNError(st, fn.__name__)
+    return o, S_T, p_T
+
+
+def kdn_diag_forward(q, k, v, log_alpha, omega, r, S0=None, p0=None, *, mu=None, chunk=0, flags=0,
+                     out=None, workspace=None, stream=None):
+    """Diagonal KDN forward (KDN paper Sec. 4.1).  Returns (o, S_T, p_T).
+
+    q, k [B,T,H,dk] and v [B,T,H,dv] in fp32 or bf16; log_alpha, omega
+    [B,T,H,dk], r [B,T,H] fp32; optional S0 [B,H,dk,dv], p0 [B,H,dk] fp32.
+    mu=None selects d_k.  ``out=(o, S_T, p_T)`` writes into given tensors.
+    """
+    return _forward(KDN_DIAG, q, k, v, log_alpha, omega, r, S0, p0, mu, chunk, flags, out,
+                    workspace, stream)
+
+
+def kdn_iso_forward(q, k, v, log_alpha, omega, r, S0=None, p0=None, *, mu=None, chunk=0, flags=0,
+                    out=None, workspace=None, stream=None):
+    """Isotropic KDN forward (KDN paper Sec. 4.2): omega [B,T,H], p0/p_T [B,H]."""
+    return _forward(KDN_ISO, q, k, v, log_alpha, omega, r, S0, p0, mu, chunk, flags, out,
+                    workspace, stream)
+
+
+def kdn_step(variant, q, k, v, log_alpha, omega, r, S, p, *, mu=None, o=None, workspace=None,
+             stream=None):
+    """One decode token per sequence; S and p are updated in place.  Returns o [B,H,dv]."""
+    lib = library()
+    variant = {"diag": KDN_DIAG, "iso": KDN_ISO}.get(variant, variant)
+    device = q.device
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    io = KDN_BF16 if q.dtype == torch.bfloat16 else KDN_F32
+    iot = torch.bfloat16 if io == KDN_BF16 else torch.float32
+    nu = (dk,) if variant == KDN_DIAG else ()
+    _check(q, "q", iot, (B, H, dk), device)
+    _check(k, "k", iot, (B, H, dk), device)
+    _check(v, "v", iot, (B, H, dv), device)
+    _check(log_alpha, "log_alpha", torch.float32, (B, H, dk), device)
+    _check(omega, "omega", torch.float32, (B, H) + nu, device)
+    _check(r, "r", torch.float32, (B, H), device)
+    _check(S, "S", torch.float32, (B, H, dk, dv), device)
+    _check(p, "p", torch.float32, (B, H) + nu, device)
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=iot, device=device)
+    _check(o, "o", iot, (B, H, dv), device)
+    need = lib.kdn_workspace_size(variant, B, 1, H, dk, dv, 0, io, 0)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    mu = -1.0 if mu is None else float(mu)
+    with torch.cuda.device(device):
+        st = lib.kdn_step(variant, B, H, dk, dv, mu, io, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                          _ptr(omega), _ptr(r), _ptr(S), _ptr(p), _ptr(o), _ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _stream(stream, device))
+    if st != 0:
+        raise KDNError(st, "kdn_step")
+    return o
+
+
+def kdn_read_device_status(workspace, stream=None) -> int:
+    """Synchronise the stream and return the device status word of ``workspace``."""
+    lib = library()
+    with torch.cuda.device(workspace.device):
+        return int(lib.kdn_read_device_status(_ptr(workspace), _stream(stream, workspace.device)))

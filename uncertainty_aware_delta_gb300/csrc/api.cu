@@ -1,0 +1,252 @@
+// C ABI of the KDN mixer library: argument validation, workspace carving and
+// kernel dispatch.  See include/kdn.h for the contract of every entry point.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "kdn.h"
+#include "kdn_internal.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kStatusBytes = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool supported_dim(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+int resolve_chunk(int chunk, int T) {
+    if (chunk != 0) return chunk;
+    if (T >= 64) return 64;
+    if (T > 32) return 64;
+    if (T > 16) return 32;
+    return 16;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+    const void* p;
+    size_t n;
+};
+
+bool overlaps(Range a, Range b) {
+    if (!a.p || !b.p || a.n == 0 || b.n == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+// Tensor-core path availability (set by chunk_tc.cu when compiled in).
+bool use_tc_path(int io, int dk, int dv, int chunk, uint32_t flags) {
+    if (flags & KDN_FLAG_PORTABLE) return false;
+    return kdn::tc_path_supported(io, dk, dv, chunk);
+}
+
+struct WsLayout {
+    size_t total;
+    size_t kappa_off, summary_off, carry_off;
+    int nG;
+};
+
+WsLayout ws_layout(int variant, int B, int T, int H, int dk, int dv, int chunk, int io,
+                   uint32_t flags) {
+    WsLayout w;
+    memset(&w, 0, sizeof(w));
+    size_t off = kStatusBytes;
+    if (T > 0 && !use_tc_path(io, dk, dv, chunk, flags)) {
+        const int nu = variant == KDN_DIAG ? dk : 1;
+        const size_t BH = (size_t)B * H;
+        w.nG = (T + kdn::kGainChunk - 1) / kdn::kGainChunk;
+        w.kappa_off = off;
+        off = align_up(off + sizeof(float) * (size_t)B * T * H * dk);
+        w.summary_off = off;
+        off = align_up(off + sizeof(float) * 4 * BH * w.nG * nu);
+        w.carry_off = off;
+        off = align_up(off + sizeof(float) * BH * w.nG * nu);
+    }
+    w.total = off;
+    return w;
+}
+
+kdn_status validate_common(int variant, int B, int T, int H, int dk, int dv, int chunk, int io) {
+    if (variant != KDN_DIAG && variant != KDN_ISO) return KDN_ERR_SHAPE;
+    if (io != KDN_F32 && io != KDN_BF16) return KDN_ERR_DTYPE;
+    if (B < 0 || T < 0 || H < 0) return KDN_ERR_SHAPE;
+    if (!supported_dim(dk) || !supported_dim(dv)) return KDN_ERR_UNSUPPORTED;
+    if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return KDN_ERR_UNSUPPORTED;
+    // keep every element index of a [B,T,H,d] tensor below 2^40
+    if ((double)B * (double)T * (double)H * 128.0 > 1.0e12) return KDN_ERR_SHAPE;
+    if ((double)B * (double)H > 2.0e9) return KDN_ERR_SHAPE;
+    return KDN_OK;
+}
+
+kdn_status forward_impl(int variant, int B, int T, int H, int dk, int dv, int chunk, float mu,
+                        int io, uint32_t flags, const void* q, const void* k, const void* v,
+                        const float* log_alpha, const float* omega, const float* r,
+                        const float* S0, const float* p0, void* o, float* S_T, float* p_T,
+                        void* workspace, size_t workspace_bytes, kdn_stream_t stream) {
+    kdn_status st = validate_common(variant, B, T, H, dk, dv, chunk, io);
+    if (st != KDN_OK) return st;
+    chunk = resolve_chunk(chunk, T);
+    const size_t BH = (size_t)B * H;
+    const size_t esz = io == KDN_BF16 ? 2 : 4;
+    const size_t ntok = (size_t)B * T * H;
+    const size_t nu = variant == KDN_DIAG ? (size_t)dk : 1;
+    if (!workspace) return KDN_ERR_WORKSPACE;
+    if (BH > 0 && (!S_T || !p_T)) return KDN_ERR_NULL;
+    if (ntok > 0 && (!q || !k || !v || !log_alpha || !omega || !r || !o)) return KDN_ERR_NULL;
+    const void* ptrs[] = {q, k, v, log_alpha, omega, r, S0, p0, o, S_T, p_T, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KDN_ERR_ALIGN;
+    const WsLayout w = ws_layout(variant, B, T, H, dk, dv, chunk, io, flags);
+    if (workspace_bytes < w.total) return KDN_ERR_WORKSPACE;
+
+    const Range in[] = {{q, ntok * dk * esz}, {k, ntok * dk * esz}, {v, ntok * dv * esz},
+                        {log_alpha, ntok * dk * 4}, {omega, ntok * nu * 4}, {r, ntok * 4},
+                        {S0, BH * dk * dv * 4}, {p0, BH * nu * 4}};
+    const Range ro = {o, ntok * dv * esz}, rs = {S_T, BH * dk * dv * 4}, rp = {p_T, BH * nu * 4};
+    const Range rw = {workspace, w.total};
+    for (const Range& x : in) {
+        if (overlaps(ro, x) || overlaps(rw, x)) return KDN_ERR_ALIAS;
+        if (x.p != S0 && overlaps(rs, x)) return KDN_ERR_ALIAS;
+        if (x.p != p0 && overlaps(rp, x)) return KDN_ERR_ALIAS;
+    }
+    if (overlaps(ro, rs) || overlaps(ro, rp) || overlaps(rs, rp) || overlaps(rw, ro) ||
+        overlaps(rw, rs) || overlaps(rw, rp))
+        return KDN_ERR_ALIAS;
+    if (S0 && S0 != (const float*)S_T && overlaps(rs, Range{S0, BH * dk * dv * 4})) return KDN_ERR_ALIAS;
+    if (p0 && p0 != (const float*)p_T && overlaps(rp, Range{p0, BH * nu * 4})) return KDN_ERR_ALIAS;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t* status = static_cast<uint32_t*>(workspace);
+    if (cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess) return KDN_ERR_CUDA;
+    if (BH == 0) return KDN_OK;
+
+    kdn::ForwardArgs a;
+    a.variant = variant; a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
+    a.mu = mu < 0.f ? (float)dk : mu;
+    a.io = io; a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.omega = omega; a.r = r;
+    a.S0 = S0; a.p0 = p0; a.o = o; a.S_T = S_T; a.p_T = p_T; a.status = status;
+
+    cudaError_t e;
+    if (T == 0) {
+        e = kdn::launch_state_copy(a, s);
+    } else if (use_tc_path(io, dk, dv, chunk, flags)) {
+        e = kdn::launch_forward_tc(a, s);
+    } else {
+        char* base = static_cast<char*>(workspace);
+        kdn::ScanWorkspace sw;
+        sw.kappa = reinterpret_cast<float*>(base + w.kappa_off);
+        sw.summary = reinterpret_cast<float*>(base + w.summary_off);
+        sw.carry = reinterpret_cast<float*>(base + w.carry_off);
+        sw.chunk_g = kdn::kGainChunk;
+        sw.n_chunks_g = w.nG;
+        e = kdn::launch_gain_scan(a, sw, s);
+        if (e == cudaSuccess) e = kdn::launch_chunk_simt(a, sw.kappa, s);
+    }
+    return e == cudaSuccess ? KDN_OK : KDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kdn_workspace_size(int variant, int B, int T, int H, int dk, int dv, int chunk,
+                          int io_dtype, uint32_t flags) {
+    if (validate_common(variant, B, T, H, dk, dv, chunk, io_dtype) != KDN_OK) return 0;
+    chunk = resolve_chunk(chunk, T);
+    return ws_layout(variant, B, T, H, dk, dv, chunk, io_dtype, flags).total;
+}
+
+kdn_status kdn_diag_forward(int B, int T, int H, int dk, int dv, int chunk, float mu,
+                            int io_dtype, uint32_t flags, const void* q, const void* k,
+                            const void* v, const float* log_alpha, const float* omega,
+                            const float* r, const float* S0, const float* p0, void* o,
+                            float* S_T, float* p_T, void* workspace, size_t workspace_bytes,
+                            kdn_stream_t stream) {
+    return forward_impl(KDN_DIAG, B, T, H, dk, dv, chunk, mu, io_dtype, flags, q, k, v,
+                        log_alpha, omega, r, S0, p0, o, S_T, p_T, workspace, workspace_bytes,
+                        stream);
+}
+
+kdn_status kdn_iso_forward(int B, int T, int H, int dk, int dv, int chunk, float mu,
+                           int io_dtype, uint32_t flags, const void* q, const void* k,
+                           const void* v, const float* log_alpha, const float* omega,
+                           const float* r, const float* S0, const float* p0, void* o, float* S_T,
+                           float* p_T, void* workspace, size_t workspace_bytes,
+                           kdn_stream_t stream) {
+    return forward_impl(KDN_ISO, B, T, H, dk, dv, chunk, mu, io_dtype, flags, q, k, v, log_alpha,
+                        omega, r, S0, p0, o, S_T, p_T, workspace, workspace_bytes, stream);
+}
+
+kdn_status kdn_step(int variant, int B, int H, int dk, int dv, float mu, int io_dtype,
+                    const void* q, const void* k, const void* v, const float* log_alpha,
+                    const float* omega, const float* r, float* S, float* p, void* o,
+                    void* workspace, size_t workspace_bytes, kdn_stream_t stream) {
+    kdn_status st = validate_common(variant, B, 1, H, dk, dv, 0, io_dtype);
+    if (st != KDN_OK) return st;
+    if (!workspace) return KDN_ERR_WORKSPACE;
+    if (workspace_bytes < kStatusBytes) return KDN_ERR_WORKSPACE;
+    const size_t BH = (size_t)B * H;
+    if (BH > 0 && (!q || !k || !v || !log_alpha || !omega || !r || !S || !p || !o))
+        return KDN_ERR_NULL;
+    const void* ptrs[] = {q, k, v, log_alpha, omega, r, S, p, o, workspace};
+    for (const void* x : ptrs)
+        if (x && !aligned16(x)) return KDN_ERR_ALIGN;
+    const size_t esz = io_dtype == KDN_BF16 ? 2 : 4;
+    const size_t nu = variant == KDN_DIAG ? (size_t)dk : 1;
+    const Range in[] = {{q, BH * dk * esz}, {k, BH * dk * esz}, {v, BH * dv * esz},
+                        {log_alpha, BH * dk * 4}, {omega, BH * nu * 4}, {r, BH * 4}};
+    const Range rs = {S, BH * dk * dv * 4}, rp = {p, BH * nu * 4}, ro = {o, BH * dv * esz};
+    const Range rw = {workspace, kStatusBytes};
+    for (const Range& x : in)
+        if (overlaps(rs, x) || overlaps(rp, x) || overlaps(ro, x) || overlaps(rw, x))
+            return KDN_ERR_ALIAS;
+    if (overlaps(rs, rp) || overlaps(rs, ro) || overlaps(rp, ro) || overlaps(rw, rs) ||
+        overlaps(rw, rp) || overlaps(rw, ro))
+        return KDN_ERR_ALIAS;
+    kdn::StepArgs a;
+    a.variant = variant; a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.io = io_dtype;
+    a.mu = mu < 0.f ? (float)dk : mu;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.omega = omega; a.r = r;
+    a.S = S; a.p = p; a.o = o; a.status = static_cast<uint32_t*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (BH == 0) {
+        return cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) == cudaSuccess ? KDN_OK
+                                                                                  : KDN_ERR_CUDA;
+    }
+    return kdn::launch_step(a, s) == cudaSuccess ? KDN_OK : KDN_ERR_CUDA;
+}
+
+kdn_status kdn_read_device_status(const void* workspace, kdn_stream_t stream) {
+    if (!workspace) return KDN_ERR_NULL;
+    uint32_t word = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KDN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDN_ERR_CUDA;
+    return static_cast<kdn_status>(word);
+}
+
+const char* kdn_status_string(int status) {
+    switch (status) {
+        case KDN_OK: return "ok";
+        case KDN_ERR_NULL: return "a required pointer is NULL";
+        case KDN_ERR_SHAPE: return "invalid or inconsistent sizes";
+        case KDN_ERR_DTYPE: return "io dtype must be KDN_F32 or KDN_BF16";
+        case KDN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case KDN_ERR_WORKSPACE: return "workspace missing or too small";
+        case KDN_ERR_UNSUPPORTED: return "d_k, d_v or chunk outside the supported set";
+        case KDN_ERR_CUDA: return "a CUDA call or kernel launch failed";
+        case KDN_ERR_TIMEOUT: return "a bounded device wait gave up";
+        case KDN_ERR_RANGE: return "a chunk's cumulative log-decay is outside the supported range";
+        case KDN_ERR_ALIAS: return "an output overlaps an input";
+        default: return "unknown status";
+    }
+}
+
+int kdn_abi_version(void) { return 100; }
+
+}  // extern "C"

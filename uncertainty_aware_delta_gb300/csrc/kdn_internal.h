@@ -1,0 +1,58 @@
+// Internal launchers of the KDN library (host side; not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kdn {
+
+struct ForwardArgs {
+    int variant;  // 0 diagonal, 1 isotropic
+    int B, T, H, dk, dv, chunk;
+    float mu;
+    int io;       // 0 fp32, 1 bf16
+    const void *q, *k, *v;
+    const float *log_alpha, *omega, *r, *S0, *p0;
+    void* o;
+    float *S_T, *p_T;
+    uint32_t* status;  // device status word
+};
+
+// Gain-scan workspace (CUDA-core path): gains and Moebius chunk summaries.
+struct ScanWorkspace {
+    float* kappa;      // [B,T,H,dk]
+    float* summary;    // [B*H, nG, nu, 4]
+    float* carry;      // [B*H, nG, nu]
+    int chunk_g;       // tokens per gain chunk
+    int n_chunks_g;
+};
+
+constexpr int kGainChunk = 256;
+
+// Moebius 2x2 gain scan: writes kappa [B,T,H,dk] and p_T.  scan.cu
+cudaError_t launch_gain_scan(const ForwardArgs& a, const ScanWorkspace& w, cudaStream_t s);
+
+// CUDA-core chunkwise memory pass (compact-WY/UT form, fp32 FFMA).  chunk_simt.cu
+cudaError_t launch_chunk_simt(const ForwardArgs& a, const float* kappa, cudaStream_t s);
+
+// Single-token decode, state in place.  step.cu
+struct StepArgs {
+    int variant, B, H, dk, dv, io;
+    float mu;
+    const void *q, *k, *v;
+    const float *log_alpha, *omega, *r;
+    float *S, *p;
+    void* o;
+    uint32_t* status;
+};
+cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
+
+// Fused tensor-core forward (gain scan + compact-WY chunk pass).  chunk_tc.cu
+bool tc_path_supported(int io, int dk, int dv, int chunk);
+cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t s);
+
+// Copy the initial state to the outputs (T == 0).  chunk_simt.cu
+cudaError_t launch_state_copy(const ForwardArgs& a, cudaStream_t s);
+
+}  // namespace kdn

@@ -1,0 +1,246 @@
+// Moebius 2x2 gain scan (CUDA-core path).
+//
+// KDN paper Sec. 4.1 Eq. 32-37: with information scaling, the per-channel
+// posterior variance follows a fractional-linear (Moebius) map
+//     p_t = (a_t^2 p_{t-1} + w_t) / (u_t a_t^2 p_{t-1} + 1 + u_t w_t),
+//     u_t = mu k_t^2 / r_t,
+// i.e. [n; d]_t = M_t [n; d]_{t-1} with M_t = [[a^2, w], [u a^2, 1 + u w]] and
+// p = n / d.  Matrix products associate (but do not commute), so the
+// recurrence is evaluated as a chunked scan, the structure of the paper's
+// App. D gain pass: (A) ordered product of each chunk's matrices,
+// (B) exclusive carry over the chunks, (C) replay inside each chunk from its
+// carry, emitting the gains
+//     p_hat_t = a_t^2 p_{t-1} + w_t,   kappa_t = p_hat_t k_t / (r_t + sum_i p_hat_t,i k_t,i^2).
+// All matrix entries are positive, so products have no cancellation; they are
+// rescaled by exact powers of two after every token, which leaves n / d
+// unchanged (App. D's max-abs renormalisation, done without rounding).
+//
+// The Isotropic variant (Sec. 4.2 Eq. 40, App. C) runs the same three phases
+// on one scalar per head, with a_t = mean_i a_t,i^2 (trace projection) and
+// u_t = mu ||k_t||^2 / (d_k r_t); its gain is kappa_t = beta_t k_t.
+
+#include "common.cuh"
+#include "kdn_internal.h"
+
+namespace kdn {
+namespace {
+
+__device__ __forceinline__ void renorm4(float& m00, float& m01, float& m10, float& m11) {
+    const float mx = fmaxf(fmaxf(m00, m01), fmaxf(m10, m11));
+    int e;
+    frexpf(mx, &e);
+    const float s = ldexpf(1.0f, -e);
+    m00 *= s; m01 *= s; m10 *= s; m11 *= s;
+}
+
+// ---------------------------------------------------------------- diagonal
+template <typename TIO>
+__global__ void mobius_summary_diag(const TIO* __restrict__ k, const float* __restrict__ la,
+                                    const float* __restrict__ om, const float* __restrict__ r,
+                                    int Tn, int H, int dk, float mu, int Cg, int nG,
+                                    float* __restrict__ summary) {
+    const int bh = blockIdx.x, c = blockIdx.y, b = bh / H, h = bh % H;
+    const int i = threadIdx.x;
+    if (i >= dk) return;
+    const int t0 = c * Cg, t1 = min(Tn, t0 + Cg);
+    float m00 = 1.f, m01 = 0.f, m10 = 0.f, m11 = 1.f;
+    for (int t = t0; t < t1; ++t) {
+        const size_t th = ((size_t)b * Tn + t) * H + h;
+        const float kv = IO<TIO>::load(k, th * dk + i);
+        const float a2 = expf(2.0f * la[th * dk + i]);
+        const float w = om[th * dk + i];
+        const float u = mu * kv * kv / r[th];
+        // P <- M_t P (newest on the left)
+        const float n00 = a2 * m00 + w * m10;
+        const float n01 = a2 * m01 + w * m11;
+        const float n10 = u * a2 * m00 + (1.0f + u * w) * m10;
+        const float n11 = u * a2 * m01 + (1.0f + u * w) * m11;
+        m00 = n00; m01 = n01; m10 = n10; m11 = n11;
+        renorm4(m00, m01, m10, m11);
+    }
+    float4 out = make_float4(m00, m01, m10, m11);
+    reinterpret_cast<float4*>(summary)[((size_t)bh * nG + c) * dk + i] = out;
+}
+
+__global__ void mobius_carry(const float* __restrict__ summary, const float* __restrict__ p0,
+                             int BH, int nu, int nG, float* __restrict__ carry) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;  // (bh, channel)
+    if (e >= BH * nu) return;
+    const int bh = e / nu, i = e % nu;
+    float p = p0 ? p0[e] : 1.0f;
+    for (int c = 0; c < nG; ++c) {
+        const size_t idx = ((size_t)bh * nG + c) * nu + i;
+        carry[idx] = p;
+        const float4 m = reinterpret_cast<const float4*>(summary)[idx];
+        p = (m.x * p + m.y) / (m.z * p + m.w);
+    }
+}
+
+constexpr int kReplayGroup = 8;  // tokens whose channel sums are reduced together
+
+template <typename TIO>
+__global__ void gain_replay_diag(const TIO* __restrict__ k, const float* __restrict__ la,
+                                 const float* __restrict__ om, const float* __restrict__ r,
+                                 const float* __restrict__ carry, int Tn, int H, int dk, float mu,
+                                 int Cg, int nG, float* __restrict__ kappa, float* __restrict__ p_T) {
+    __shared__ float red[4][kReplayGroup];  // per warp partial sums (dk <= 128)
+    const int bh = blockIdx.x, c = blockIdx.y, b = bh / H, h = bh % H;
+    const int i = threadIdx.x, lane = i & 31, warp = i >> 5, nwarps = blockDim.x >> 5;
+    const bool act = i < dk;
+    float p = act ? carry[((size_t)bh * nG + c) * dk + i] : 0.f;
+    const int t0 = c * Cg, t1 = min(Tn, t0 + Cg);
+    for (int tb = t0; tb < t1; tb += kReplayGroup) {
+        float ph[kReplayGroup], kv[kReplayGroup], w[kReplayGroup];
+#pragma unroll
+        for (int j = 0; j < kReplayGroup; ++j) {
+            const int t = tb + j;
+            ph[j] = 0.f; kv[j] = 0.f; w[j] = 0.f;
+            if (act && t < t1) {
+                const size_t th = ((size_t)b * Tn + t) * H + h;
+                kv[j] = IO<TIO>::load(k, th * dk + i);
+                const float a2 = expf(2.0f * la[th * dk + i]);
+                ph[j] = a2 * p + om[th * dk + i];
+                w[j] = ph[j] * kv[j] * kv[j];
+                const float u = mu * kv[j] * kv[j] / r[th];
+                p = ph[j] / (1.0f + u * ph[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kReplayGroup; ++j) {
+            const float s = warp_sum(w[j]);
+            if (lane == 0) red[warp][j] = s;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < kReplayGroup; ++j) {
+            const int t = tb + j;
+            float z = 0.f;
+            for (int q = 0; q < nwarps; ++q) z += red[q][j];
+            if (act && t < t1) {
+                const size_t th = ((size_t)b * Tn + t) * H + h;
+                kappa[th * dk + i] = ph[j] * kv[j] / (r[th] + z);
+            }
+        }
+        __syncthreads();
+    }
+    if (act && c == nG - 1) p_T[(size_t)bh * dk + i] = p;
+}
+
+// ---------------------------------------------------------------- isotropic
+// Per-token channel reductions a_bar_t = mean_i exp(2 log_alpha_t,i) and
+// ||k_t||^2, one warp per token, into shared memory.
+template <typename TIO>
+__device__ void iso_token_stats(const TIO* __restrict__ k, const float* __restrict__ la, int b,
+                                int h, int Tn, int H, int dk, int t0, int t1, float* abar,
+                                float* kn2) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    for (int t = t0 + warp; t < t1; t += nwarps) {
+        const size_t th = ((size_t)b * Tn + t) * H + h;
+        float sa = 0.f, sk = 0.f;
+        for (int i = lane; i < dk; i += 32) {
+            sa += expf(2.0f * la[th * dk + i]);
+            const float kv = IO<TIO>::load(k, th * dk + i);
+            sk += kv * kv;
+        }
+        sa = warp_sum(sa);
+        sk = warp_sum(sk);
+        if (lane == 0) {
+            abar[t - t0] = sa / (float)dk;
+            kn2[t - t0] = sk;
+        }
+    }
+}
+
+template <typename TIO>
+__global__ void mobius_summary_iso(const TIO* __restrict__ k, const float* __restrict__ la,
+                                   const float* __restrict__ om, const float* __restrict__ r,
+                                   int Tn, int H, int dk, float mu, int Cg, int nG,
+                                   float* __restrict__ summary) {
+    extern __shared__ float sm[];
+    float* abar = sm;
+    float* kn2 = sm + Cg;
+    const int bh = blockIdx.x, c = blockIdx.y, b = bh / H, h = bh % H;
+    const int t0 = c * Cg, t1 = min(Tn, t0 + Cg);
+    iso_token_stats(k, la, b, h, Tn, H, dk, t0, t1, abar, kn2);
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    float m00 = 1.f, m01 = 0.f, m10 = 0.f, m11 = 1.f;
+    for (int t = t0; t < t1; ++t) {
+        const size_t th = ((size_t)b * Tn + t) * H + h;
+        const float a = abar[t - t0], w = om[th];
+        const float u = mu * kn2[t - t0] / ((float)dk * r[th]);
+        const float n00 = a * m00 + w * m10;
+        const float n01 = a * m01 + w * m11;
+        const float n10 = u * a * m00 + (1.0f + u * w) * m10;
+        const float n11 = u * a * m01 + (1.0f + u * w) * m11;
+        m00 = n00; m01 = n01; m10 = n10; m11 = n11;
+        renorm4(m00, m01, m10, m11);
+    }
+    reinterpret_cast<float4*>(summary)[(size_t)bh * nG + c] = make_float4(m00, m01, m10, m11);
+}
+
+template <typename TIO>
+__global__ void gain_replay_iso(const TIO* __restrict__ k, const float* __restrict__ la,
+                                const float* __restrict__ om, const float* __restrict__ r,
+                                const float* __restrict__ carry, int Tn, int H, int dk, float mu,
+                                int Cg, int nG, float* __restrict__ kappa,
+                                float* __restrict__ p_T) {
+    extern __shared__ float sm[];
+    float* abar = sm;
+    float* kn2 = sm + Cg;
+    float* beta = sm + 2 * Cg;
+    const int bh = blockIdx.x, c = blockIdx.y, b = bh / H, h = bh % H;
+    const int t0 = c * Cg, t1 = min(Tn, t0 + Cg);
+    iso_token_stats(k, la, b, h, Tn, H, dk, t0, t1, abar, kn2);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float p = carry[(size_t)bh * nG + c];
+        for (int t = t0; t < t1; ++t) {
+            const size_t th = ((size_t)b * Tn + t) * H + h;
+            const float ph = abar[t - t0] * p + om[th];
+            beta[t - t0] = ph / (r[th] + ph * kn2[t - t0]);
+            const float u = mu * kn2[t - t0] / ((float)dk * r[th]);
+            p = ph / (1.0f + u * ph);
+        }
+        if (c == nG - 1) p_T[bh] = p;
+    }
+    __syncthreads();
+    const int n = (t1 - t0) * dk;
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+        const int tt = e / dk, i = e % dk;
+        const size_t th = ((size_t)b * Tn + t0 + tt) * H + h;
+        kappa[th * dk + i] = beta[tt] * IO<TIO>::load(k, th * dk + i);
+    }
+}
+
+template <typename TIO>
+cudaError_t launch_scan_t(const ForwardArgs& a, const ScanWorkspace& w, cudaStream_t s) {
+    const TIO* k = static_cast<const TIO*>(a.k);
+    const int BH = a.B * a.H, Cg = w.chunk_g, nG = w.n_chunks_g;
+    const dim3 grid(BH, nG);
+    if (a.variant == 0) {
+        const int nt = ((a.dk + 31) / 32) * 32;
+        mobius_summary_diag<TIO><<<grid, nt, 0, s>>>(k, a.log_alpha, a.omega, a.r, a.T, a.H, a.dk,
+                                                     a.mu, Cg, nG, w.summary);
+        const int tot = BH * a.dk;
+        mobius_carry<<<(tot + 127) / 128, 128, 0, s>>>(w.summary, a.p0, BH, a.dk, nG, w.carry);
+        gain_replay_diag<TIO><<<grid, nt, 0, s>>>(k, a.log_alpha, a.omega, a.r, w.carry, a.T, a.H,
+                                                  a.dk, a.mu, Cg, nG, w.kappa, a.p_T);
+    } else {
+        mobius_summary_iso<TIO><<<grid, 128, 2 * Cg * sizeof(float), s>>>(
+            k, a.log_alpha, a.omega, a.r, a.T, a.H, a.dk, a.mu, Cg, nG, w.summary);
+        mobius_carry<<<(BH + 127) / 128, 128, 0, s>>>(w.summary, a.p0, BH, 1, nG, w.carry);
+        gain_replay_iso<TIO><<<grid, 128, 3 * Cg * sizeof(float), s>>>(
+            k, a.log_alpha, a.omega, a.r, w.carry, a.T, a.H, a.dk, a.mu, Cg, nG, w.kappa, a.p_T);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gain_scan(const ForwardArgs& a, const ScanWorkspace& w, cudaStream_t s) {
+    if (a.io == 1) return launch_scan_t<__nv_bfloat16>(a, w, s);
+    return launch_scan_t<float>(a, w, s);
+}
+
+}  // namespace kdn

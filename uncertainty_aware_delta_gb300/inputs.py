@@ -106,5 +106,15 @@ def make_inputs(variant: str, B: int, T: int, H: int, dk: int, dv: int, io: str 
 def workload_inputs(w: Workload, variant: str | None = None):
     """Inputs of a named workload.  ``variant`` overrides the workload's own
     (the isotropic variant is also run on the diagonal workloads' shapes, with
-    its own per-(b,t,h) omega drawn from the same seed)."""
-    return make_inputs(variant or w.variant, w.B, w.T, w.H, w.d, w.d, w.io, w.seed, w.log_alpha_range)
+    its own per-(b,t,h) omega drawn from the same seed).  For a decode
+    workload this returns the prefill tokens only; see :func:`decode_step_inputs`."""
+    T = w.prefill if w.steps else w.T
+    return make_inputs(variant or w.variant, w.B, T, w.H, w.d, w.d, w.io, w.seed, w.log_alpha_range)
+
+
+def decode_step_inputs(w: Workload, step: int, variant: str | None = None):
+    """Inputs of decode step ``step`` (0-based) of a decode workload: one token
+    per (sequence, head), drawn with the recipe above from seed
+    ``w.seed * 4096 + 1 + step`` so any step can be regenerated on its own."""
+    return make_inputs(variant or w.variant, w.B, 1, w.H, w.d, w.d, w.io, w.seed * 4096 + 1 + step,
+                       w.log_alpha_range)
