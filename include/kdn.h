@@ -164,6 +164,14 @@ kdn_status kdn_step(int variant, int B, int H, int dk, int dv, float mu, int io_
  */
 kdn_status kdn_read_device_status(const void *workspace, kdn_stream_t stream);
 
+/*
+ * Number of kernels one forward call with these arguments enqueues on its
+ * stream (the status-word memset is not a kernel).  0 for rejected arguments
+ * or an empty batch.  For capture into CUDA graphs and for launch accounting.
+ */
+int kdn_forward_kernel_count(int variant, int B, int T, int H, int dk, int dv, int chunk,
+                             int io_dtype, uint32_t flags);
+
 /* Static description of a status code (never NULL). */
 const char *kdn_status_string(int status);
 

@@ -32,7 +32,8 @@ def lib():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("kdn_diag_forward", "kdn_iso_forward", "kdn_step", "kdn_workspace_size",
-              "kdn_read_device_status", "kdn_status_string", "kdn_abi_version"):
+              "kdn_read_device_status", "kdn_status_string", "kdn_abi_version",
+              "kdn_forward_kernel_count"):
         assert n in names
 
 
@@ -68,6 +69,16 @@ def test_workspace_size_rules(lib):
     assert n % 256 == 0
     # decode needs only the status word
     assert ws(0, 256, 1, 16, 128, 128, 0, 0, 1) >= 256
+
+
+def test_forward_kernel_count(lib):
+    import uncertainty_aware_delta_gb300 as kdn
+
+    assert kdn.forward_kernel_count(0, 1, 64, 2, 16, 16, 16, 0, 0) == 4   # scan (3) + chunk pass
+    assert kdn.forward_kernel_count(1, 1, 64, 2, 16, 16, 16, 0, 1) == 4
+    assert kdn.forward_kernel_count(0, 1, 0, 2, 16, 16, 0, 0, 0) == 1     # state copy
+    assert kdn.forward_kernel_count(0, 0, 64, 2, 16, 16, 0, 0, 0) == 0
+    assert kdn.forward_kernel_count(0, 1, 64, 2, 24, 16, 0, 0, 0) == 0
 
 
 def _fwd_args(**over):

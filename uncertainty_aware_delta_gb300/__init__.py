@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     kdn_iso_forward,
     kdn_read_device_status,
     kdn_step,
+    forward_kernel_count,
     library,
     library_path,
     status_string,

@@ -23,7 +23,7 @@ KDN_FLAG_PORTABLE = 0x1
 
 EXPORTED = (
     "kdn_workspace_size", "kdn_diag_forward", "kdn_iso_forward", "kdn_step",
-    "kdn_read_device_status", "kdn_status_string", "kdn_abi_version",
+    "kdn_read_device_status", "kdn_status_string", "kdn_abi_version", "kdn_forward_kernel_count",
 )
 
 
@@ -61,6 +61,8 @@ def library():
             lib.kdn_read_device_status.argtypes = [vp, vp]
             lib.kdn_status_string.restype = ctypes.c_char_p
             lib.kdn_status_string.argtypes = [i32]
+            lib.kdn_forward_kernel_count.restype = i32
+            lib.kdn_forward_kernel_count.argtypes = [i32] * 8 + [u32]
             lib.kdn_abi_version.restype = i32
             lib.kdn_abi_version.argtypes = []
             _lib = lib
@@ -98,6 +100,11 @@ def _check(t, name, dtype, shape, device):
 
 def workspace_size(variant, B, T, H, dk, dv, chunk=0, io=KDN_BF16, flags=0) -> int:
     return int(library().kdn_workspace_size(variant, B, T, H, dk, dv, chunk, io, flags))
+
+
+def forward_kernel_count(variant, B, T, H, dk, dv, chunk=0, io=KDN_BF16, flags=0) -> int:
+    """Kernels one forward call with these arguments enqueues."""
+    return int(library().kdn_forward_kernel_count(variant, B, T, H, dk, dv, chunk, io, flags))
 
 
 def _forward(variant, q, k, v, log_alpha, omega, r, S0, p0, mu, chunk, flags, out, workspace,

@@ -230,6 +230,15 @@ kdn_status kdn_read_device_status(const void* workspace, kdn_stream_t stream) {
     return static_cast<kdn_status>(word);
 }
 
+int kdn_forward_kernel_count(int variant, int B, int T, int H, int dk, int dv, int chunk,
+                             int io_dtype, uint32_t flags) {
+    if (validate_common(variant, B, T, H, dk, dv, chunk, io_dtype) != KDN_OK) return 0;
+    if ((size_t)B * H == 0) return 0;
+    if (T == 0) return 1;
+    chunk = resolve_chunk(chunk, T);
+    return use_tc_path(io_dtype, dk, dv, chunk, flags) ? kdn::tc_kernel_count() : 4;
+}
+
 const char* kdn_status_string(int status) {
     switch (status) {
         case KDN_OK: return "ok";

@@ -7,4 +7,6 @@ bool tc_path_supported(int, int, int, int) { return false; }
 
 cudaError_t launch_forward_tc(const ForwardArgs&, cudaStream_t) { return cudaErrorNotSupported; }
 
+int tc_kernel_count() { return 1; }
+
 }  // namespace kdn

@@ -51,6 +51,7 @@ cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 // Fused tensor-core forward (gain scan + compact-WY chunk pass).  chunk_tc.cu
 bool tc_path_supported(int io, int dk, int dv, int chunk);
 cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t s);
+int tc_kernel_count();
 
 // Copy the initial state to the outputs (T == 0).  chunk_simt.cu
 cudaError_t launch_state_copy(const ForwardArgs& a, cudaStream_t s);
