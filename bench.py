@@ -1,0 +1,463 @@
+#!/usr/bin/env python
+"""Benchmark of the KDN mixer forward on GB300 (one JSON line on stdout).
+
+Headline workload: Diagonal KDN forward, bf16 q/k/v/o with fp32 state and
+accumulation, B=8 sequences x H=16 heads x T=4096 tokens, d_k = d_v = 128,
+chunk 64 (the 1.3B-layer-shaped mixer).  One step = one forward call over the
+whole batch (gain scan, chunkwise memory pass, readout, final state).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kdn|reference]
+
+For N > 1 the script runs under torchrun, one rank per GPU; every rank runs
+its own batch (weak scaling, no collective on the data path) and the reported
+value is the tokens of all ranks over the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle instead (the slow
+token-by-token recurrence) on the host cores, on a bounded sample of the same
+workload per step; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDN mixer tokens/s (H16,d128,T4096,bf16) and % of GB300 roofline"
+HEADLINE = "diag-bf16-b8h16t4096d128"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------- setup
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kdn", "reference"], default="kdn")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-tokens", type=int, default=2048,
+                    help="tokens per sequence in the CPU oracle sample (all B x H sequences)")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- inputs
+def device_inputs(torch, w, variant, seed, device, T=None, B=None):
+    """Synthetic inputs on the device with the workload recipe (q, k ~ N(0,1)
+    L2-normalised per token-head; v ~ N(0,1); log_alpha = -U(lo, hi);
+    r = softplus(N(0,1)) + 1e-3; omega ~ U(1e-4, 1e-2)), drawn with torch's
+    device generator so large batches are ready in milliseconds."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    B = w.B if B is None else B
+    T = w.T if T is None else T
+    H, d = w.H, w.d
+    iot = torch.bfloat16 if w.io == "bf16" else torch.float32
+    f = dict(device=device, generator=g)
+    q = torch.nn.functional.normalize(torch.randn(B, T, H, d, **f), dim=-1).to(iot)
+    k = torch.nn.functional.normalize(torch.randn(B, T, H, d, **f), dim=-1).to(iot)
+    v = torch.randn(B, T, H, d, **f).to(iot)
+    lo, hi = w.log_alpha_range
+    la = -(lo + (hi - lo) * torch.rand(B, T, H, d, **f))
+    r = torch.nn.functional.softplus(torch.randn(B, T, H, **f)) + 1e-3
+    oshape = (B, T, H, d) if variant == "diag" else (B, T, H)
+    om = 1e-4 + (1e-2 - 1e-4) * torch.rand(*oshape, **f)
+    return {"q": q, "k": k, "v": v, "log_alpha": la, "omega": om, "r": r}
+
+
+def algorithmic_bytes(B, T, H, dk, dv, io, variant):
+    """Method inputs and outputs only: q, k, v, log_alpha, omega, r read once,
+    o written once, final S_T and p_T written once (S_0 = 0, p_0 = 1 are not read)."""
+    e = 2 if io == "bf16" else 4
+    per_tok = e * (2 * dk + dv) + 4 * dk + 4 * (dk if variant == "diag" else 1) + 4 + e * dv
+    nu = dk if variant == "diag" else 1
+    return B * T * H * per_tok + B * H * (dk * dv + nu) * 4
+
+
+def algorithmic_flops(B, T, H, dk, dv, C):
+    """Triangle-aware chunk-form flops per token-head: 5*C*d + 6*d^2 (d = d_k = d_v)."""
+    d = dk
+    return B * T * H * (5 * C * d + 6 * d * d)
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            self.t0 = time.time()
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, fl in rows for i, x in enumerate(fl) if x.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- timing
+def reduce_max(torch, dist, x, world, device):
+    """Maximum of a per-rank float over all ranks (the slowest rank's time)."""
+    if world == 1:
+        return float(x)
+    dev = device if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tokens_per_s(tokens_per_rank, ms_max, world):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms_max / 1e3)
+
+
+def time_calls(torch, fn, steps, warmup, barrier):
+    """Warm up, then time exactly `steps` calls with CUDA events on the current
+    stream, barrier + synchronize on both sides.  Returns ms per call."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def traffic_for(kernel, workload):
+    """dram read + write bytes per launch from the committed ncu summary, or
+    None when absent or taken on a different version of the kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("workload") != workload:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return rec["bytes_per_launch"] if sha == rec.get("source_sha256") else None
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_tokens_per_s(x_host, variant, tokens, nthreads=0):
+    import oracle
+
+    sl = {n: np.ascontiguousarray(v[:, :tokens]) for n, v in x_host.items()}
+    t0 = time.perf_counter()
+    oracle.forward(variant, sl["q"], sl["k"], sl["v"], sl["log_alpha"], sl["omega"], sl["r"],
+                   nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    B = sl["q"].shape[0]
+    return B * tokens / dt, dt
+
+
+def host_sample(torch, x, tokens):
+    return {n: v[:, :tokens].float().cpu().numpy().astype(np.float64) for n, v in x.items()}
+
+
+def run_reference(args):
+    """Reference arm: the fp64 oracle on the host cores, a bounded sample per step."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    from uncertainty_aware_delta_gb300.inputs import WORKLOADS
+
+    oracle.build_oracle()
+    w = WORKLOADS[args.workload]
+    tokens = min(w.T, 256)
+    x = device_inputs(torch, w, w.variant, w.seed, "cpu", T=tokens)
+    xh = {n: v.float().numpy().astype(np.float64) for n, v in x.items()}
+    cores = oracle.recurrence.default_threads()
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(xh, w.variant, tokens)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_tokens_per_s(xh, w.variant, tokens)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = w.B * tokens / dt
+    sample = f"all {w.B}x{w.H} sequences, first {tokens} of {w.T} tokens per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- main arm
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    import uncertainty_aware_delta_gb300 as kdn
+    from uncertainty_aware_delta_gb300.build import build_library
+    from uncertainty_aware_delta_gb300.inputs import WORKLOADS
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    if rank == 0:
+        build_library()
+    if world > 1:
+        dist.barrier()
+    build_library()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        return reduce_max(torch, dist, x, world, device)
+
+    peaks, peak_src = load_peaks()
+    w = WORKLOADS[args.workload]
+    variant = w.variant
+    fwd = kdn.kdn_diag_forward if variant == "diag" else kdn.kdn_iso_forward
+    vcode = kdn.KDN_DIAG if variant == "diag" else kdn.KDN_ISO
+    io = kdn.KDN_BF16 if w.io == "bf16" else kdn.KDN_F32
+    x = device_inputs(torch, w, variant, w.seed + 7919 * rank, device)
+    nkern = kdn.forward_kernel_count(vcode, w.B, w.T, w.H, w.d, w.d, w.chunk, io, 0)
+    tc_path = nkern == 1
+    ws = torch.empty(kdn.workspace_size(vcode, w.B, w.T, w.H, w.d, w.d, w.chunk, io, 0),
+                     dtype=torch.uint8, device=device)
+    o = torch.empty(w.B, w.T, w.H, w.d, dtype=x["q"].dtype, device=device)
+    S_T = torch.empty(w.B, w.H, w.d, w.d, dtype=torch.float32, device=device)
+    p_T = torch.empty((w.B, w.H, w.d) if variant == "diag" else (w.B, w.H), dtype=torch.float32,
+                      device=device)
+
+    def step():
+        fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"], chunk=w.chunk,
+            out=(o, S_T, p_T), workspace=ws)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms = time_calls(torch, step, args.steps, args.warmup, barrier)
+    clk = clocks.stop()
+    status = kdn.kdn_read_device_status(ws)
+    ms = max_over_ranks(ms)
+    tokens = w.B * w.T
+    value = aggregate_tokens_per_s(tokens, ms, world)
+
+    # ---- roofline of the dominant kernel (whole step when it is one kernel)
+    abytes = algorithmic_bytes(w.B, w.T, w.H, w.d, w.d, w.io, variant)
+    aflops = algorithmic_flops(w.B, w.T, w.H, w.d, w.d, w.chunk)
+    hbm = float(peaks["hbm_gbs"])
+    achieved = abytes / (ms / 1e3) / 1e9
+    kernel_name = "kdn_fused_tc_kernel" if tc_path else "forward (gain scan + chunk_simt_kernel)"
+    t_roof = max(abytes / (hbm * 1e9), aflops / (float(peaks["bf16_tflops"]) * 1e12))
+    roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs",
+                "algorithmic_bytes_per_launch": abytes,
+                "traffic": traffic_for(kernel_name, w.name),
+                "step_fraction_of_roofline_time": t_roof / (ms / 1e3)}
+
+    # ---- end to end: pinned host inputs -> device -> forward -> host outputs
+    stream = torch.cuda.current_stream(device)
+    hx = {n: t.cpu().pin_memory() for n, t in x.items()}
+    dx = {n: torch.empty_like(t) for n, t in x.items()}
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hS = torch.empty(S_T.shape, dtype=S_T.dtype).pin_memory()
+    hp = torch.empty(p_T.shape, dtype=p_T.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hx.values())
+    d2h = ho.numel() * ho.element_size() + hS.numel() * 4 + hp.numel() * 4
+
+    def e2e_step():
+        for n in dx:
+            dx[n].copy_(hx[n], non_blocking=True)
+        fwd(dx["q"], dx["k"], dx["v"], dx["log_alpha"], dx["omega"], dx["r"], chunk=w.chunk,
+            out=(o, S_T, p_T), workspace=ws)
+        ho.copy_(o, non_blocking=True)
+        hS.copy_(S_T, non_blocking=True)
+        hp.copy_(p_T, non_blocking=True)
+
+    e2e_ms = max_over_ranks(time_calls(torch, e2e_step, max(3, args.steps // 4), 2, barrier))
+    del hx, dx
+
+    # ---- other workloads (single rank view, timing only)
+    extra = {}
+    if not args.no_extra:
+        extra = other_workloads(torch, kdn, WORKLOADS, device, barrier, peaks)
+
+    # ---- CPU oracle baseline (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+
+        oracle.build_oracle()
+        ntok = min(args.cpu_tokens, w.T)
+        xh = host_sample(torch, x, ntok)
+        cval, cdt = oracle_tokens_per_s(xh, variant, ntok)
+        cpu = {"value": cval, "unit": "tokens/s", "cores": oracle.recurrence.default_threads(),
+               "kind": "oracle", "wall_s": cdt,
+               "sample": f"all {w.B}x{w.H} sequences of the workload, first {ntok} of {w.T} tokens"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if tc_path else "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "variant": "diagonal" if variant == "diag" else "isotropic",
+            "B": w.B, "H": w.H, "T": w.T, "d_k": w.d, "d_v": w.d, "chunk": w.chunk, "mu": w.d,
+            "io": w.io, "state": "fp32",
+            "path": "tensor-core (tcgen05, fused)" if tc_path else "cuda-core (gain scan + FFMA chunk pass)",
+            "l2": f"no flush: the inputs ({abytes / 1e9:.2f} GB per step) are larger than L2 (129 MB)",
+            "parallelism": f"{world} replica(s), each GPU its own batch (weak)",
+            "device_status": status,
+        },
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": nkern * args.steps,
+        "clocks": clk,
+        "workloads": extra,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def other_workloads(torch, kdn, WORKLOADS, device, barrier, peaks):
+    out = {}
+    hbm = float(peaks["hbm_gbs"])
+    for name, variant in (("iso-bf16-b8h16t4096d128", "iso"), ("diag-bf16-b1h16t65536d128", "diag")):
+        w = WORKLOADS[name]
+        x = device_inputs(torch, w, variant, w.seed, device)
+        fwd = kdn.kdn_diag_forward if variant == "diag" else kdn.kdn_iso_forward
+        ms = time_calls(torch, lambda: fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"],
+                                           chunk=w.chunk), 5, 2, barrier)
+        ab = algorithmic_bytes(w.B, w.T, w.H, w.d, w.d, w.io, variant)
+        out[name] = {"tokens_per_s": w.B * w.T / (ms / 1e3), "ms": ms,
+                     "hbm_frac": ab / (ms / 1e3) / 1e9 / hbm}
+        del x
+    # decode: 512-token prefill through the forward path, then 1024 single-token steps
+    w = WORKLOADS["diag-decode-f32-s256h16d128"]
+    pre = device_inputs(torch, w, "diag", w.seed, device, T=w.prefill)
+    _, S, p = kdn.kdn_diag_forward(pre["q"], pre["k"], pre["v"], pre["log_alpha"], pre["omega"],
+                                   pre["r"], chunk=w.chunk)
+    del pre
+    per = []
+    for s in range(w.steps):
+        y = device_inputs(torch, w, "diag", w.seed * 4096 + 1 + s, device, T=1)
+        per.append({n: t[:, 0] for n, t in y.items()})
+    S0, p0 = S.clone(), p.clone()
+    ws = torch.empty(kdn.workspace_size(0, w.B, 1, w.H, w.d, w.d), dtype=torch.uint8, device=device)
+    o = torch.empty(w.B, w.H, w.d, device=device)
+
+    def loop():
+        for y in per:
+            kdn.kdn_step("diag", y["q"], y["k"], y["v"], y["log_alpha"], y["omega"], y["r"], S, p,
+                         o=o, workspace=ws)
+
+    for _ in range(1):
+        loop()
+    S.copy_(S0)
+    p.copy_(p0)
+    ms = time_calls(torch, loop, 1, 0, barrier)
+    per_step = ms / w.steps
+    step_bytes = w.B * w.H * (2 * 4 * w.d * w.d + 2 * 4 * w.d + 4 * (3 * w.d + 2 * w.d + 1) + 4 * w.d)
+    out[w.name] = {"tokens_per_s": w.B * w.steps / (ms / 1e3), "ms_per_step": per_step,
+                   "hbm_frac": step_bytes / (per_step / 1e3) / 1e9 / hbm,
+                   "algorithmic_bytes_per_step": step_bytes}
+    return out
+
+
+if __name__ == "__main__":
+    sys.exit(main())
