@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--profile", action="store_true",
+                    help="only the warm-up and timed forward calls of the workload (for ncu captures)")
     ap.add_argument("--cpu-tokens", type=int, default=2048,
                     help="tokens per sequence in the CPU oracle sample (all B x H sequences)")
     return ap.parse_args()
@@ -318,6 +320,12 @@ def main():
     def step():
         fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"], chunk=w.chunk,
             out=(o, S_T, p_T), workspace=ws)
+
+    if args.profile:
+        time_calls(torch, step, args.steps, args.warmup, barrier)
+        print(json.dumps({"profile": w.name, "kernels_per_step": nkern,
+                          "device_status": kdn.kdn_read_device_status(ws)}), flush=True)
+        return 0
 
     clocks = ClockSampler(local)
     clocks.start()
