@@ -158,6 +158,53 @@ kdn_status kdn_step(int variant, int B, int H, int dk, int dv, float mu, int io_
                     void *workspace, size_t workspace_bytes, kdn_stream_t stream);
 
 /*
+ * Forward without a caller workspace.  The paper has no counterpart: this is
+ * a convenience of the library for callers that cannot allocate device
+ * memory at the point where they run the mixer -- for example code inside a
+ * host framework that owns every device allocation and forbids cudaMalloc in
+ * its execution callbacks, or a latency-critical loop that must not pay for
+ * cudaMalloc/cudaFree, which can synchronise the whole device.
+ *
+ * The scratch the forward needs (per-token gains, Moebius chunk summaries,
+ * the status word) comes from a library-owned static device array of
+ * KDN_STATIC_SCRATCH_BYTES, which every GPU that loads the library holds
+ * until the process exits.  This entry point calls no cudaMalloc, cudaFree
+ * or other allocating routine.
+ *
+ * variant: KDN_DIAG or KDN_ISO.  Every other argument means what it means
+ * for kdn_diag_forward / kdn_iso_forward; inputs and outputs are still
+ * caller-owned device buffers.  status_out: NULL, or a caller-owned device
+ * uint32_t (4-byte aligned) that receives this call's device status word on
+ * `stream` (the codes kdn_read_device_status returns).
+ *
+ * Set-up: the first call on a device looks up the device address of the
+ * static array, with that device current; make that first call before any
+ * stream capture begins on the device.
+ *
+ * Sharing: all calls in the process share the one array per device and it
+ * keeps the last call's contents; each call clears what must start at zero
+ * (the status word) and writes everything else before reading it.  Calls
+ * whose work overlaps on the GPU (other streams, other host threads on the
+ * same device) race on the array and corrupt each other's results: order
+ * them on one stream or synchronise between them.
+ *
+ * Errors: KDN_ERR_WORKSPACE when the problem needs more scratch than
+ * KDN_STATIC_SCRATCH_BYTES (kdn_workspace_size() gives the need; with
+ * flags = 0 a bf16 forward with d_k = d_v = 128 needs about
+ * 4 * B * T * H * d_k bytes on the CUDA-core path); otherwise as
+ * kdn_diag_forward.
+ */
+#define KDN_STATIC_SCRATCH_BYTES (32u << 20)
+
+kdn_status kdn_forward_noalloc(int variant, int B, int T, int H, int dk, int dv, int chunk,
+                               float mu, int io_dtype, uint32_t flags,
+                               const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *omega, const float *r,
+                               const float *S0, const float *p0,
+                               void *o, float *S_T, float *p_T, uint32_t *status_out,
+                               kdn_stream_t stream);
+
+/*
  * Synchronise `stream` and return the device status word the last call that
  * used `workspace` left there: KDN_OK, KDN_ERR_TIMEOUT or KDN_ERR_RANGE (or
  * KDN_ERR_CUDA if the copy itself fails, KDN_ERR_NULL for a NULL workspace).

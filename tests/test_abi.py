@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("kdn_diag_forward", "kdn_iso_forward", "kdn_step", "kdn_workspace_size",
               "kdn_read_device_status", "kdn_status_string", "kdn_abi_version",
-              "kdn_forward_kernel_count"):
+              "kdn_forward_kernel_count", "kdn_forward_noalloc"):
         assert n in names
 
 

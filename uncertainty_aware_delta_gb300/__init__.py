@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     KDN_ISO,
     KDNError,
     kdn_diag_forward,
+    kdn_forward_noalloc,
     kdn_iso_forward,
     kdn_read_device_status,
     kdn_step,

@@ -24,6 +24,7 @@ KDN_FLAG_PORTABLE = 0x1
 EXPORTED = (
     "kdn_workspace_size", "kdn_diag_forward", "kdn_iso_forward", "kdn_step",
     "kdn_read_device_status", "kdn_status_string", "kdn_abi_version", "kdn_forward_kernel_count",
+    "kdn_forward_noalloc",
 )
 
 
@@ -63,6 +64,9 @@ def library():
             lib.kdn_status_string.argtypes = [i32]
             lib.kdn_forward_kernel_count.restype = i32
             lib.kdn_forward_kernel_count.argtypes = [i32] * 8 + [u32]
+            lib.kdn_forward_noalloc.restype = i32
+            lib.kdn_forward_noalloc.argtypes = [i32] * 7 + [f32, i32, u32] + [vp] * 3 + [fp] * 5 + \
+                [vp, fp, fp, vp, vp]
             lib.kdn_abi_version.restype = i32
             lib.kdn_abi_version.argtypes = []
             _lib = lib
@@ -204,6 +208,45 @@ def kdn_step(variant, q, k, v, log_alpha, omega, r, S, p, *, mu=None, o=None, wo
     if st != 0:
         raise KDNError(st, "kdn_step")
     return o
+
+
+def kdn_forward_noalloc(variant, q, k, v, log_alpha, omega, r, S0=None, p0=None, *, mu=None,
+                        chunk=0, flags=0, out, status_out=None, stream=None):
+    """Forward that allocates nothing: for callers that may not allocate device
+    memory where they run the mixer.  Its scratch is the library's built-in
+    static device array (include/kdn.h, KDN_STATIC_SCRATCH_BYTES), shared by
+    every call in the process, so calls must not overlap on the GPU.  The
+    outputs ``out=(o, S_T, p_T)`` are required (this wrapper creates no
+    tensors); ``status_out`` is an optional int32 CUDA tensor of one element
+    that receives the device status word.
+    """
+    lib = library()
+    variant = {"diag": KDN_DIAG, "iso": KDN_ISO}.get(variant, variant)
+    device = q.device
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    io = KDN_BF16 if q.dtype == torch.bfloat16 else KDN_F32
+    iot = torch.bfloat16 if io == KDN_BF16 else torch.float32
+    nu = (dk,) if variant == KDN_DIAG else ()
+    o, S_T, p_T = out
+    for t, name, dt, shp in ((q, "q", iot, (B, T, H, dk)), (k, "k", iot, (B, T, H, dk)),
+                             (v, "v", iot, (B, T, H, dv)), (log_alpha, "log_alpha", torch.float32, (B, T, H, dk)),
+                             (omega, "omega", torch.float32, (B, T, H) + nu), (r, "r", torch.float32, (B, T, H)),
+                             (S0, "S0", torch.float32, (B, H, dk, dv)), (p0, "p0", torch.float32, (B, H) + nu),
+                             (o, "o", iot, (B, T, H, dv)), (S_T, "S_T", torch.float32, (B, H, dk, dv)),
+                             (p_T, "p_T", torch.float32, (B, H) + nu)):
+        _check(t, name, dt, shp, device)
+    if status_out is not None:
+        _check(status_out, "status_out", torch.int32, (1,), device)
+    mu = -1.0 if mu is None else float(mu)
+    with torch.cuda.device(device):
+        st = lib.kdn_forward_noalloc(variant, B, T, H, dk, dv, int(chunk), mu, io, int(flags), _ptr(q),
+                                     _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(omega), _ptr(r), _ptr(S0),
+                                     _ptr(p0), _ptr(o), _ptr(S_T), _ptr(p_T), _ptr(status_out),
+                                     _stream(stream, device))
+    if st != 0:
+        raise KDNError(st, "kdn_forward_noalloc")
+    return o, S_T, p_T
 
 
 def kdn_read_device_status(workspace, stream=None) -> int:
