@@ -202,3 +202,33 @@ def test_small_workload_every_output():
     w = WORKLOADS["diag-f32-b1h2t64d16"]
     _sampled_parity(w.name, "diag", [(0, 0), (0, 1)])
     _sampled_parity(w.name, "iso", [(0, 0), (0, 1)])
+
+
+# ------------------------------------------------------------ tensor-core path
+TC_CASES = [
+    # variant, B, T, H  (bf16 io, d_k = d_v = 128, chunk 64 -> fused tensor-core kernel)
+    ("diag", 2, 333, 3), ("iso", 2, 333, 3), ("diag", 1, 50, 2), ("iso", 1, 50, 2),
+    ("diag", 1, 1, 2), ("diag", 3, 128, 1),
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_tensor_core_path_matches_oracle_and_portable_path(case):
+    import torch
+
+    variant, B, T, H = case
+    kdn = _kdn()
+    vcode = kdn.KDN_DIAG if variant == "diag" else kdn.KDN_ISO
+    assert kdn.forward_kernel_count(vcode, B, T, H, 128, 128, 64, kdn.KDN_BF16, 0) == 1
+    x = make_inputs(variant, B, T, H, 128, 128, io="bf16", seed=500 + T)
+    rng = np.random.default_rng(T)
+    S0 = (0.2 * rng.standard_normal((B, H, 128, 128))).astype(np.float32)
+    p0 = rng.uniform(0.3, 2.0, size=(B, H, 128) if variant == "diag" else (B, H)).astype(np.float32)
+    t = to_device(x)
+    S0d, p0d = torch.from_numpy(S0).cuda(), torch.from_numpy(p0).cuda()
+    ref = oracle.forward(variant, x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"], S0=S0, p0=p0)
+    tc = _run(kdn, variant, t, S0=S0d, p0=p0d, chunk=64)
+    e = _check(variant, x, tc, ref, "bf16", "tensor-core")
+    simt = _run(kdn, variant, t, S0=S0d, p0=p0d, chunk=64, flags=kdn.KDN_FLAG_PORTABLE)
+    for a, b_ in zip(tc, simt):
+        assert np.max(np.abs(to_host(a) - to_host(b_))) <= 2e-2 * max(1e-3, np.max(np.abs(to_host(b_)))), e
