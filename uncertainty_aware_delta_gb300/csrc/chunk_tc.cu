@@ -59,7 +59,8 @@ constexpr uint32_t OFF_VIN = 32768;    // v tile (MN-major A operand of U^T)
 constexpr uint32_t OFF_LA = 49152;     // log_alpha [64][128] fp32 -> cumulative G in place
 constexpr uint32_t OFF_OM = 81920;     // omega [64][128] fp32 -> p_hat in place (diagonal)
 constexpr uint32_t OFF_KQ = 114688;    // [K_bar; Q_bar] 128 rows x 128, two 16 KB K-atoms
-constexpr uint32_t OFF_DT = OFF_KQ;    //   later Delta^T [128 j][64 t] bf16
+constexpr uint32_t OFF_DT = OFF_KQ;    //   later Delta^T [128 j][64 t] bf16, then the o tile
+constexpr uint32_t OFF_OST = OFF_KQ;   //   o tile [64 t][128 j] bf16 staged for the TMA store
 constexpr uint32_t OFF_KT = 147456;    // K_til [64 s][128 i], two 8 KB K-atoms
 constexpr uint32_t OFF_AQ = 163840;    // A [64 t][64 s] bf16
 constexpr uint32_t OFF_LF = 172032;    // L fp32 [64][kLDF]
@@ -86,7 +87,7 @@ static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
 constexpr uint32_t TM_S = 0, TM_D = 128, TM_O = 192, TM_G = 256, TM_W = 320, TM_COLS = 512;
 
 struct TcParams {
-    CUtensorMap tq, tk, tv, tla, tom;
+    CUtensorMap tq, tk, tv, tla, tom, to;
     const float* r;
     const float* om_iso;
     const float* S0;
@@ -241,6 +242,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             sm[SM_MUR + t] = P.mu / rr;
             sm[SM_OMI + t] = om;
         }
+        if (tid == 0) bulk_wait_read();  // previous o tile read out of the staging buffer
         wait_or_abort(bar_in, ph_in);
         ph_in ^= 1u;
         in_pending = false;
@@ -257,30 +259,48 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             for (int hf = 0; hf < 2; ++hf) {
                 float w[32], w2[32];
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int t = hf * 32 + u;
-                    const float lav = LA[t * kD + i];
-                    const float kv = __bfloat162float(
-                        *reinterpret_cast<const __nv_bfloat16*>(kin + sw128_off(t, kch)));
-                    float ph = 0.0f, wv = 0.0f, a2v = 0.0f;
-                    if (t < nv) {
-                        G += lav;
-                        const float a2 = __expf(2.0f * lav);
-                        const float k2 = kv * kv;
+                for (int qt = 0; qt < 2; ++qt) {
+                    // loads and token-local arithmetic first (independent of the carry) ...
+                    float a2[16], k2[16], om[16], gq[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int t = hf * 32 + qt * 16 + u;
+                        const float lav = LA[t * kD + i];
+                        const float kv = __bfloat162float(
+                            *reinterpret_cast<const __nv_bfloat16*>(kin + sw128_off(t, kch)));
+                        a2[u] = __expf(2.0f * lav);
+                        k2[u] = kv * kv;
+                        om[u] = ISO ? 0.0f : OM[t * kD + i];
+                        gq[u] = lav;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int t = hf * 32 + qt * 16 + u;
+                        if (t < nv) G += gq[u];
+                        gq[u] = G;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) LA[(hf * 32 + qt * 16 + u) * kD + i] = gq[u];
+                    // ... then the serial carry chain
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int t = hf * 32 + qt * 16 + u;
+                        const bool valid = t < nv;
                         if (!ISO) {
-                            ph = fmaf(a2, p_reg, OM[t * kD + i]);
-                            wv = ph * k2;
-                            const float den = fmaf(sm[SM_MUR + t] * k2, ph, 1.0f);
-                            p_reg = __fdividef(ph, den);
+                            const float ph = fmaf(a2[u], p_reg, om[u]);
+                            const float pn = __fdividef(ph, fmaf(sm[SM_MUR + t] * k2[u], ph, 1.0f));
+                            p_reg = valid ? pn : p_reg;
+                            om[u] = valid ? ph : 0.0f;
+                            w[qt * 16 + u] = valid ? ph * k2[u] : 0.0f;
                         } else {
-                            wv = k2;
-                            a2v = a2;
+                            w[qt * 16 + u] = valid ? k2[u] : 0.0f;
+                            w2[qt * 16 + u] = valid ? a2[u] : 0.0f;
                         }
                     }
-                    LA[t * kD + i] = G;
-                    if (!ISO) OM[t * kD + i] = ph;
-                    w[u] = wv;
-                    w2[u] = a2v;
+                    if (!ISO) {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) OM[(hf * 32 + qt * 16 + u) * kD + i] = om[u];
+                    }
                 }
                 sm[SM_ZP + w4 * 64 + hf * 32 + lane] = butterfly_sum32(w, lane);
                 if (ISO) sm[SM_AP + w4 * 64 + hf * 32 + lane] = butterfly_sum32(w2, lane);
@@ -670,7 +690,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             mma_commit(bar_mma);
         }
         mma_pending = true;
-        // ---------------- K: outputs
+        // ---------------- K: outputs, staged as a [64 t][128 j] tile and stored by TMA
         if (tid < 128) {
             wait_or_abort(bar_mma, ph_mma);
             tc_fence_after();
@@ -679,10 +699,16 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             tmem_ld32(lane_base + TM_O, v0);
             tmem_ld32(lane_base + TM_O + 32, v1);
             tmem_wait_ld();
-            __nv_bfloat16* op = P.o + (static_cast<size_t>(b) * T + t0) * H * kD + static_cast<size_t>(h) * kD + j;
+            __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(base + OFF_OST) + j;
 #pragma unroll
             for (int t = 0; t < kC; ++t)
-                if (t < nv) op[static_cast<size_t>(t) * H * kD] = __float2bfloat16_rn(__uint_as_float(t < 32 ? v0[t] : v1[t - 32]));
+                ost[t * kD] = __float2bfloat16_rn(__uint_as_float(t < 32 ? v0[t] : v1[t - 32]));
+            fence_proxy_async();
+            named_bar(2, 128);
+            if (tid == 0) {
+                tma_store_4d(&P.to, sb + OFF_OST, 0, h, t0, b);  // rows past T are clipped
+                bulk_commit();
+            }
         }
         ph_mma ^= 1u;
         mma_pending = false;
@@ -690,6 +716,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         __syncthreads();
         if (*s_abort) break;
     }
+    if (tid == 0) bulk_wait_all();
 
     const bool aborted = *s_abort != 0;
     if (!aborted) {
@@ -780,6 +807,7 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t s) {
               encode_4d(&P.tla, a.log_alpha, F32, 4, a.B, a.T, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (ok && a.variant == 0)
         ok = encode_4d(&P.tom, a.omega, F32, 4, a.B, a.T, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (ok) ok = encode_4d(&P.to, a.o, BF, 2, a.B, a.T, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return cudaErrorInvalidValue;
     P.r = a.r;
     P.om_iso = a.variant == 1 ? a.omega : nullptr;
