@@ -74,7 +74,8 @@ constexpr int kLDF = 68;
 constexpr int kLDX = 36;
 // small region, float offsets
 constexpr int SM_R = 0, SM_MUR = 64, SM_INVZ = 128, SM_ZP = 192, SM_AP = 448, SM_GREF = 704,
-              SM_CF = 832, SM_FOUT = 960, SM_OMI = 1088, SM_FLAG = 1152, SM_FLOATS = 1160;
+              SM_FOUT = 832, SM_OMI = 960, SM_FLAG = 1024, SM_CF = 1032 /* [2][128] by chunk parity */,
+              SM_FLOATS = 1288;
 constexpr uint32_t OFF_BAR = OFF_SMALL + SM_FLOATS * 4;
 constexpr uint32_t kSmemBytes = OFF_BAR + 64;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
@@ -128,6 +129,55 @@ __device__ __forceinline__ void mob_renorm(Mob& m) {  // exact power-of-two resc
     frexpf(mx, &e);
     const float s = ldexpf(1.0f, -e);
     m.a *= s; m.b *= s; m.c *= s; m.d *= s;
+}
+
+// ---- warp-level TF32 MMA helpers for the triangular inverse (fp32 row-major tiles in shared memory)
+__device__ __forceinline__ uint32_t tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// x[n8 tile][4] = A[16 x 8*k1] (k-steps k0..k1-1) * B[8*k1 x 16]; A, B row-major with strides lda, ldb.
+__device__ __forceinline__ void mma_tile_16xN(float (&x)[2][4], const float* A, int lda, const float* B, int ldb,
+                                              int k0, int k1) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[n][e] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+        if (ks < k0 || ks >= k1) continue;
+        const float* a = A + 8 * ks;
+        const uint32_t a0 = tf32(a[g * lda + q]), a1 = tf32(a[(g + 8) * lda + q]);
+        const uint32_t a2 = tf32(a[g * lda + q + 4]), a3 = tf32(a[(g + 8) * lda + q + 4]);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const float* bp = B + (8 * ks) * ldb + 8 * n;
+            mma_tf32(x[n], a0, a1, a2, a3, tf32(bp[q * ldb + g]), tf32(bp[(q + 4) * ldb + g]));
+        }
+    }
+}
+__device__ __forceinline__ void mma_tile_16x16(float (&x)[2][4], const float* A, int lda, const float* B, int ldb,
+                                               int ksteps) {
+    mma_tile_16xN(x, A, lda, B, ldb, 0, ksteps);
+}
+__device__ __forceinline__ void store_tile_16x16(const float (&x)[2][4], float* D, int ldd, float scale, int g,
+                                                 int q) {
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        D[g * ldd + 8 * n + 2 * q] = scale * x[n][0];
+        D[g * ldd + 8 * n + 2 * q + 1] = scale * x[n][1];
+        D[(g + 8) * ldd + 8 * n + 2 * q] = scale * x[n][2];
+        D[(g + 8) * ldd + 8 * n + 2 * q + 1] = scale * x[n][3];
+    }
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -212,8 +262,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     tc_fence_after();
 
     uint32_t ph_in = 0, ph_v = 0, ph_mma = 0;
-    bool in_pending = nchunks > 0, v_pending = nchunks > 0, mma_pending = false;
+    int n_in_issued = nchunks > 0 ? 1 : 0, n_v_issued = n_in_issued, n_mma_issued = 0;
     auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
+        if (*s_abort) return;
         if (!mbar_wait(bar, parity, kWaitLimit)) {
             set_status(P.status, kStatusTimeout);
             *s_abort = 1;
@@ -226,15 +277,16 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     float* TF = reinterpret_cast<float*>(base + OFF_TF);
     float* XT = reinterpret_cast<float*>(base + OFF_XT);
 
-#pragma unroll 1
-    for (int n = 0; n < nchunks; ++n) {
-        const int t0 = n * kC, nv = min(kC, T - t0);
-        // ---------------- A0: per-token scalars
-        if (tid < kC) {
-            const int t = tid;
+    // Warps 4-7: per-token scalars of chunk c, then (inputs landed) the uncertainty
+    // recurrence and cumulative log-decay of chunk c.  Runs one chunk ahead of the
+    // memory pass of warps 0-3.
+    auto prep_gains = [&](int c) {
+        const int t0c = c * kC, nvc = min(kC, T - t0c);
+        if (tid < 128 + kC) {
+            const int t = tid - 128;
             float rr = 1.0f, om = 0.0f;
-            if (t < nv) {
-                const size_t th = (static_cast<size_t>(b) * T + t0 + t) * H + h;
+            if (t < nvc) {
+                const size_t th = (static_cast<size_t>(b) * T + t0c + t) * H + h;
                 rr = P.r[th];
                 if (ISO) om = P.om_iso[th];
             }
@@ -242,135 +294,139 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             sm[SM_MUR + t] = P.mu / rr;
             sm[SM_OMI + t] = om;
         }
-        if (tid == 0) bulk_wait_read();  // previous o tile read out of the staging buffer
         wait_or_abort(bar_in, ph_in);
-        ph_in ^= 1u;
-        in_pending = false;
-        __syncthreads();
-        if (*s_abort) break;
-
-        // ---------------- A1: uncertainty recurrence, cumulative log-decay
-        if (tid >= 128) {
-            const int i = tid - 128, w4 = warp - 4;
-            const unsigned char* kin = base + OFF_KIN + (i >> 6) * 8192 + (i & 7) * 2;
-            const int kch = (i & 63) >> 3;
-            float G = 0.0f;
-#pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
-                float w[32], w2[32];
-#pragma unroll
-                for (int qt = 0; qt < 2; ++qt) {
-                    // loads and token-local arithmetic first (independent of the carry) ...
-                    float a2[16], k2[16], om[16], gq[16];
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int t = hf * 32 + qt * 16 + u;
-                        const float lav = LA[t * kD + i];
-                        const float kv = __bfloat162float(
-                            *reinterpret_cast<const __nv_bfloat16*>(kin + sw128_off(t, kch)));
-                        a2[u] = __expf(2.0f * lav);
-                        k2[u] = kv * kv;
-                        om[u] = ISO ? 0.0f : OM[t * kD + i];
-                        gq[u] = lav;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int t = hf * 32 + qt * 16 + u;
-                        if (t < nv) G += gq[u];
-                        gq[u] = G;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) LA[(hf * 32 + qt * 16 + u) * kD + i] = gq[u];
-                    // ... then the serial carry chain
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int t = hf * 32 + qt * 16 + u;
-                        const bool valid = t < nv;
+        named_bar(1, 128);
+            if (tid >= 128) {
+                const int i = tid - 128, w4 = warp - 4;
+                const unsigned char* kin = base + OFF_KIN + (i >> 6) * 8192 + (i & 7) * 2;
+                const int kch = (i & 63) >> 3;
+                float G = 0.0f;
+    #pragma unroll 1
+                for (int hf = 0; hf < 2; ++hf) {
+                    float w[32], w2[32];
+    #pragma unroll
+                    for (int qt = 0; qt < 2; ++qt) {
+                        // loads and token-local arithmetic first (independent of the carry) ...
+                        float a2[16], k2[16], om[16], gq[16];
+    #pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const int t = hf * 32 + qt * 16 + u;
+                            const float lav = LA[t * kD + i];
+                            const float kv = __bfloat162float(
+                                *reinterpret_cast<const __nv_bfloat16*>(kin + sw128_off(t, kch)));
+                            a2[u] = __expf(2.0f * lav);
+                            k2[u] = kv * kv;
+                            om[u] = ISO ? 0.0f : OM[t * kD + i];
+                            gq[u] = lav;
+                        }
+    #pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const int t = hf * 32 + qt * 16 + u;
+                            if (t < nvc) G += gq[u];
+                            gq[u] = G;
+                        }
+    #pragma unroll
+                        for (int u = 0; u < 16; ++u) LA[(hf * 32 + qt * 16 + u) * kD + i] = gq[u];
+                        // ... then the serial carry chain
+    #pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const int t = hf * 32 + qt * 16 + u;
+                            const bool valid = t < nvc;
+                            if (!ISO) {
+                                const float ph = fmaf(a2[u], p_reg, om[u]);
+                                const float pn = __fdividef(ph, fmaf(sm[SM_MUR + t] * k2[u], ph, 1.0f));
+                                p_reg = valid ? pn : p_reg;
+                                om[u] = valid ? ph : 0.0f;
+                                w[qt * 16 + u] = valid ? ph * k2[u] : 0.0f;
+                            } else {
+                                w[qt * 16 + u] = valid ? k2[u] : 0.0f;
+                                w2[qt * 16 + u] = valid ? a2[u] : 0.0f;
+                            }
+                        }
                         if (!ISO) {
-                            const float ph = fmaf(a2[u], p_reg, om[u]);
-                            const float pn = __fdividef(ph, fmaf(sm[SM_MUR + t] * k2[u], ph, 1.0f));
-                            p_reg = valid ? pn : p_reg;
-                            om[u] = valid ? ph : 0.0f;
-                            w[qt * 16 + u] = valid ? ph * k2[u] : 0.0f;
-                        } else {
-                            w[qt * 16 + u] = valid ? k2[u] : 0.0f;
-                            w2[qt * 16 + u] = valid ? a2[u] : 0.0f;
+    #pragma unroll
+                            for (int u = 0; u < 16; ++u) OM[(hf * 32 + qt * 16 + u) * kD + i] = om[u];
                         }
                     }
-                    if (!ISO) {
-#pragma unroll
-                        for (int u = 0; u < 16; ++u) OM[(hf * 32 + qt * 16 + u) * kD + i] = om[u];
+                    sm[SM_ZP + w4 * 64 + hf * 32 + lane] = butterfly_sum32(w, lane);
+                    if (ISO) sm[SM_AP + w4 * 64 + hf * 32 + lane] = butterfly_sum32(w2, lane);
+                }
+                const float gref = 0.5f * G;
+                sm[SM_GREF + i] = gref;
+                sm[SM_CF + (c & 1) * 128 + i] = __expf(pend + gref);
+                pend = G - gref;
+                sm[SM_FOUT + i] = __expf(pend);
+                if (!(fabsf(G) <= kMaxChunkLogDecay)) set_status(P.status, kStatusRange);
+                if (ISO) {
+                    named_bar(1, 128);
+                    if (w4 == 0) {
+                        // Moebius scan of the scalar recurrence over the chunk, 2 tokens per lane
+                        float aa[2], uu[2], oo[2], kk[2], rr[2];
+                        Mob m[2];
+    #pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int t = 2 * lane + e;
+                            const float asum = sm[SM_AP + t] + sm[SM_AP + 64 + t] + sm[SM_AP + 128 + t] +
+                                               sm[SM_AP + 192 + t];
+                            kk[e] = sm[SM_ZP + t] + sm[SM_ZP + 64 + t] + sm[SM_ZP + 128 + t] +
+                                    sm[SM_ZP + 192 + t];
+                            aa[e] = asum * (1.0f / kD);
+                            rr[e] = sm[SM_R + t];
+                            oo[e] = sm[SM_OMI + t];
+                            uu[e] = P.mu * kk[e] / (kD * rr[e]);
+                            if (t < nvc)
+                                m[e] = {aa[e], oo[e], uu[e] * aa[e], fmaf(uu[e], oo[e], 1.0f)};
+                            else
+                                m[e] = {1.0f, 0.0f, 0.0f, 1.0f};
+                        }
+                        Mob pr = mob_mul(m[1], m[0]);
+                        mob_renorm(pr);
+    #pragma unroll
+                        for (int d = 1; d < 32; d <<= 1) {
+                            Mob q;
+                            q.a = __shfl_up_sync(0xffffffffu, pr.a, d);
+                            q.b = __shfl_up_sync(0xffffffffu, pr.b, d);
+                            q.c = __shfl_up_sync(0xffffffffu, pr.c, d);
+                            q.d = __shfl_up_sync(0xffffffffu, pr.d, d);
+                            if (lane >= d) {
+                                pr = mob_mul(pr, q);
+                                mob_renorm(pr);
+                            }
+                        }
+                        Mob ex;
+                        ex.a = __shfl_up_sync(0xffffffffu, pr.a, 1);
+                        ex.b = __shfl_up_sync(0xffffffffu, pr.b, 1);
+                        ex.c = __shfl_up_sync(0xffffffffu, pr.c, 1);
+                        ex.d = __shfl_up_sync(0xffffffffu, pr.d, 1);
+                        if (lane == 0) ex = {1.0f, 0.0f, 0.0f, 1.0f};
+                        float bb = (ex.a * b_iso + ex.b) / (ex.c * b_iso + ex.d);
+    #pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int t = 2 * lane + e;
+                            float beta = 0.0f;
+                            if (t < nvc) {
+                                const float bhat = fmaf(aa[e], bb, oo[e]);
+                                beta = bhat / (rr[e] + bhat * kk[e]);
+                                bb = bhat / fmaf(uu[e], bhat, 1.0f);
+                            }
+                            sm[SM_INVZ + t] = beta;
+                        }
+                        b_iso = __shfl_sync(0xffffffffu, bb, 31);
                     }
                 }
-                sm[SM_ZP + w4 * 64 + hf * 32 + lane] = butterfly_sum32(w, lane);
-                if (ISO) sm[SM_AP + w4 * 64 + hf * 32 + lane] = butterfly_sum32(w2, lane);
             }
-            const float gref = 0.5f * G;
-            sm[SM_GREF + i] = gref;
-            sm[SM_CF + i] = __expf(pend + gref);
-            pend = G - gref;
-            sm[SM_FOUT + i] = __expf(pend);
-            if (!(fabsf(G) <= kMaxChunkLogDecay)) set_status(P.status, kStatusRange);
-            if (ISO) {
-                named_bar(1, 128);
-                if (w4 == 0) {
-                    // Moebius scan of the scalar recurrence over the chunk, 2 tokens per lane
-                    float aa[2], uu[2], oo[2], kk[2], rr[2];
-                    Mob m[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int t = 2 * lane + e;
-                        const float asum = sm[SM_AP + t] + sm[SM_AP + 64 + t] + sm[SM_AP + 128 + t] +
-                                           sm[SM_AP + 192 + t];
-                        kk[e] = sm[SM_ZP + t] + sm[SM_ZP + 64 + t] + sm[SM_ZP + 128 + t] +
-                                sm[SM_ZP + 192 + t];
-                        aa[e] = asum * (1.0f / kD);
-                        rr[e] = sm[SM_R + t];
-                        oo[e] = sm[SM_OMI + t];
-                        uu[e] = P.mu * kk[e] / (kD * rr[e]);
-                        if (t < nv)
-                            m[e] = {aa[e], oo[e], uu[e] * aa[e], fmaf(uu[e], oo[e], 1.0f)};
-                        else
-                            m[e] = {1.0f, 0.0f, 0.0f, 1.0f};
-                    }
-                    Mob pr = mob_mul(m[1], m[0]);
-                    mob_renorm(pr);
-#pragma unroll
-                    for (int d = 1; d < 32; d <<= 1) {
-                        Mob q;
-                        q.a = __shfl_up_sync(0xffffffffu, pr.a, d);
-                        q.b = __shfl_up_sync(0xffffffffu, pr.b, d);
-                        q.c = __shfl_up_sync(0xffffffffu, pr.c, d);
-                        q.d = __shfl_up_sync(0xffffffffu, pr.d, d);
-                        if (lane >= d) {
-                            pr = mob_mul(pr, q);
-                            mob_renorm(pr);
-                        }
-                    }
-                    Mob ex;
-                    ex.a = __shfl_up_sync(0xffffffffu, pr.a, 1);
-                    ex.b = __shfl_up_sync(0xffffffffu, pr.b, 1);
-                    ex.c = __shfl_up_sync(0xffffffffu, pr.c, 1);
-                    ex.d = __shfl_up_sync(0xffffffffu, pr.d, 1);
-                    if (lane == 0) ex = {1.0f, 0.0f, 0.0f, 1.0f};
-                    float bb = (ex.a * b_iso + ex.b) / (ex.c * b_iso + ex.d);
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int t = 2 * lane + e;
-                        float beta = 0.0f;
-                        if (t < nv) {
-                            const float bhat = fmaf(aa[e], bb, oo[e]);
-                            beta = bhat / (rr[e] + bhat * kk[e]);
-                            bb = bhat / fmaf(uu[e], bhat, 1.0f);
-                        }
-                        sm[SM_INVZ + t] = beta;
-                    }
-                    b_iso = __shfl_sync(0xffffffffu, bb, 31);
-                }
-            }
-        }
-        __syncthreads();
-        // ---------------- A2: gain denominators, then decayed bf16 operands
+
+    };
+
+    if (tid >= 128 && nchunks > 0) prep_gains(0);
+    ph_in ^= 1u;
+    __syncthreads();
+
+#pragma unroll 1
+    for (int n = 0; n < nchunks; ++n) {
+        const int t0 = n * kC, nv = min(kC, T - t0);
+        // ---------------- A2: gain denominators, then decayed bf16 operands (all warps)
+        if (tid == 0) bulk_wait_read();  // the previous o tile has left the staging buffer
         if (!ISO && tid < kC) {
             const int t = tid;
             const float z = sm[SM_ZP + t] + sm[SM_ZP + 64 + t] + sm[SM_ZP + 128 + t] + sm[SM_ZP + 192 + t];
@@ -422,11 +478,12 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         }
         fence_proxy_async();
         __syncthreads();
-        // ---------------- B: Gram MMA; prefetch the next chunk's q, k, log_alpha, omega
+        if (*s_abort) break;
+        // ---------------- B: prefetch the next chunk's q, k, log_alpha, omega; Gram MMA
         if (tid == 0) {
             if (n + 1 < nchunks) {
                 issue_inputs(n + 1);
-                in_pending = true;
+                ++n_in_issued;
             }
             tc_fence_after();
             const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
@@ -437,282 +494,262 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 mma_bf16(tmem + TM_G, ad, bd, id, ks > 0);
             }
             mma_commit(bar_mma);
+            ++n_mma_issued;
         }
-        mma_pending = true;
-        // ---------------- C: Gram rows out of TMEM (L fp32, A bf16)
         if (tid < 128) {
-            wait_or_abort(bar_mma, ph_mma);
-            tc_fence_after();
-            uint32_t v0[32], v1[32];
-            tmem_ld32(lane_base + TM_G, v0);
-            tmem_ld32(lane_base + TM_G + 32, v1);
-            tmem_wait_ld();
-            if (tid < 64) {
-                const int t = tid;
-                float* row = LF + t * kLDF;
-#pragma unroll
-                for (int c4 = 0; c4 < 16; ++c4) {
-                    float4 x;
-                    const int s = 4 * c4;
-                    x.x = (s + 0 < t) ? __uint_as_float(s + 0 < 32 ? v0[s + 0] : v1[s + 0 - 32]) : 0.0f;
-                    x.y = (s + 1 < t) ? __uint_as_float(s + 1 < 32 ? v0[s + 1] : v1[s + 1 - 32]) : 0.0f;
-                    x.z = (s + 2 < t) ? __uint_as_float(s + 2 < 32 ? v0[s + 2] : v1[s + 2 - 32]) : 0.0f;
-                    x.w = (s + 3 < t) ? __uint_as_float(s + 3 < 32 ? v0[s + 3] : v1[s + 3 - 32]) : 0.0f;
-                    *reinterpret_cast<float4*>(row + s) = x;
-                }
-            } else {
-                const int t = tid - 64;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s = 8 * ch + 2 * e;
-                        const float a0 = (s <= t) ? __uint_as_float(s < 32 ? v0[s] : v1[s - 32]) : 0.0f;
-                        const float a1 = (s + 1 <= t) ? __uint_as_float(s + 1 < 32 ? v0[s + 1] : v1[s + 1 - 32]) : 0.0f;
-                        pk[e] = pack_bf16(a0, a1);
-                    }
-                    *reinterpret_cast<uint4*>(base + OFF_AQ + sw128_off(t, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
-            }
-        }
-        ph_mma ^= 1u;
-        mma_pending = false;
-        fence_proxy_async();
-        __syncthreads();
-        if (*s_abort) break;
-        // ---------------- D: T = (I + L)^{-1}
-        if (tid < 64) {  // 16x16 diagonal blocks, one column per thread
-            const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
-            float x[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = (r == c) ? 1.0f : 0.0f;
-#pragma unroll
-                for (int s = 0; s < r; ++s) acc = fmaf(-LF[(o + r) * kLDF + o + s], x[s], acc);
-                x[r] = acc;
-            }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) TF[(o + r) * kLDF + o + c] = x[r];
-        }
-        __syncthreads();
-        if (tid < 128) {  // 16 -> 32: X = L_ij D_j for (i, j) = (1, 0), (3, 2)
-            const int pm = tid >> 6, r = (tid >> 2) & 15, c4 = tid & 3, i = 2 * pm + 1, j = 2 * pm;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                const float l = LF[(16 * i + r) * kLDF + 16 * j + s];
-                const float4 d = *reinterpret_cast<const float4*>(TF + (16 * j + s) * kLDF + 16 * j + 4 * c4);
-                acc.x = fmaf(l, d.x, acc.x); acc.y = fmaf(l, d.y, acc.y);
-                acc.z = fmaf(l, d.z, acc.z); acc.w = fmaf(l, d.w, acc.w);
-            }
-            *reinterpret_cast<float4*>(XT + (16 * pm + r) * kLDX + 4 * c4) = acc;
-        }
-        __syncthreads();
-        if (tid < 128) {  // T_ij = -D_i X
-            const int pm = tid >> 6, r = (tid >> 2) & 15, c4 = tid & 3, i = 2 * pm + 1, j = 2 * pm;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                const float d = TF[(16 * i + r) * kLDF + 16 * i + s];
-                const float4 x = *reinterpret_cast<const float4*>(XT + (16 * pm + s) * kLDX + 4 * c4);
-                acc.x = fmaf(d, x.x, acc.x); acc.y = fmaf(d, x.y, acc.y);
-                acc.z = fmaf(d, x.z, acc.z); acc.w = fmaf(d, x.w, acc.w);
-            }
-            *reinterpret_cast<float4*>(TF + (16 * i + r) * kLDF + 16 * j + 4 * c4) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        }
-        __syncthreads();
-        {  // 32 -> 64: X = L[32:64, 0:32] T[0:32, 0:32]
-            const int r = tid >> 3, c4 = tid & 7, s0 = (4 * c4 >= 16) ? 16 : 0;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int s = s0; s < 32; ++s) {
-                const float l = LF[(32 + r) * kLDF + s];
-                const float4 d = *reinterpret_cast<const float4*>(TF + s * kLDF + 4 * c4);
-                acc.x = fmaf(l, d.x, acc.x); acc.y = fmaf(l, d.y, acc.y);
-                acc.z = fmaf(l, d.z, acc.z); acc.w = fmaf(l, d.w, acc.w);
-            }
-            *reinterpret_cast<float4*>(XT + r * kLDX + 4 * c4) = acc;
-        }
-        __syncthreads();
-        {  // T[32:64, 0:32] = -T[32:64, 32:64] X
-            const int r = tid >> 3, c4 = tid & 7, s1 = (r < 16) ? 16 : 32;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int s = 0; s < s1; ++s) {
-                const float d = TF[(32 + r) * kLDF + 32 + s];
-                const float4 x = *reinterpret_cast<const float4*>(XT + s * kLDX + 4 * c4);
-                acc.x = fmaf(d, x.x, acc.x); acc.y = fmaf(d, x.y, acc.y);
-                acc.z = fmaf(d, x.z, acc.z); acc.w = fmaf(d, x.w, acc.w);
-            }
-            *reinterpret_cast<float4*>(TF + (32 + r) * kLDF + 4 * c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        }
-        __syncthreads();
-        {  // T (lower triangle incl. diagonal) -> bf16 [t][s]
-            const int t = tid >> 2, q = tid & 3;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int ch = 2 * q + hh;
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int s = 8 * ch + 2 * e;
-                    const float a0 = (s <= t) ? TF[t * kLDF + s] : 0.0f;
-                    const float a1 = (s + 1 <= t) ? TF[t * kLDF + s + 1] : 0.0f;
-                    pk[e] = pack_bf16(a0, a1);
-                }
-                *reinterpret_cast<uint4*>(base + OFF_TT + sw128_off(t, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-        }
-        fence_proxy_async();
-        __syncthreads();
-        // ---------------- E: W^T = K_bar^T T^T, U^T = V^T T^T
-        if (tid == 0) {
-            wait_or_abort(bar_v, ph_v);
-            tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 64, 1, 0, 0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t bd = sw128_desc(sb + OFF_TT + ks * 32, 16, 1024);
-                mma_bf16(tmem + TM_W, sw128_desc(sb + OFF_KQ + ks * 2048, 16384, 1024), bd, id, ks > 0);
-                mma_bf16(tmem + TM_D, sw128_desc(sb + OFF_VIN + ks * 2048, 8192, 1024), bd, id, ks > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        ph_v ^= 1u;
-        v_pending = false;
-        mma_pending = true;
-        // ---------------- F: W^T rows -> bf16 W (MN-major B operand); prefetch next v
-        if (tid < 128) {
-            wait_or_abort(bar_mma, ph_mma);
-            tc_fence_after();
-            if (tid == 0 && n + 1 < nchunks) issue_v(n + 1);
-            const int i = tid;
-            uint32_t v0[32], v1[32];
-            tmem_ld32(lane_base + TM_W, v0);
-            tmem_ld32(lane_base + TM_W + 32, v1);
-            tmem_wait_ld();
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = 8 * ch + 2 * e;
-                    pk[e] = pack_bf16(__uint_as_float(t < 32 ? v0[t] : v1[t - 32]),
-                                      __uint_as_float(t + 1 < 32 ? v0[t + 1] : v1[t + 1 - 32]));
-                }
-                *reinterpret_cast<uint4*>(base + OFF_W + sw128_off(i, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-            // ---------------- G: state into the chunk's reference frame
-            const int j = tid;
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + TM_S + q * 32, r);
+            // ======== warps 0-3: memory pass of chunk n
+            // ---------------- C: Gram rows out of TMEM (L fp32, A bf16)
+            {
+                wait_or_abort(bar_mma, ph_mma);
+                tc_fence_after();
+                uint32_t v0[32], v1[32];
+                tmem_ld32(lane_base + TM_G, v0);
+                tmem_ld32(lane_base + TM_G + 32, v1);
                 tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * sm[SM_CF + q * 32 + c]);
-                tmem_st32(lane_base + TM_S + q * 32, r);
-                const int katom = q >> 1;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        pk[e] = pack_bf16(__uint_as_float(r[8 * cc + 2 * e]), __uint_as_float(r[8 * cc + 2 * e + 1]));
-                    *reinterpret_cast<uint4*>(base + OFF_SM + katom * 16384 + sw128_off(j, (q & 1) * 4 + cc)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                if (tid < 64) {
+                    const int t = tid;
+                    float* row = LF + t * kLDF;
+    #pragma unroll
+                    for (int c4 = 0; c4 < 16; ++c4) {
+                        float4 x;
+                        const int s = 4 * c4;
+                        x.x = (s + 0 < t) ? __uint_as_float(s + 0 < 32 ? v0[s + 0] : v1[s + 0 - 32]) : 0.0f;
+                        x.y = (s + 1 < t) ? __uint_as_float(s + 1 < 32 ? v0[s + 1] : v1[s + 1 - 32]) : 0.0f;
+                        x.z = (s + 2 < t) ? __uint_as_float(s + 2 < 32 ? v0[s + 2] : v1[s + 2 - 32]) : 0.0f;
+                        x.w = (s + 3 < t) ? __uint_as_float(s + 3 < 32 ? v0[s + 3] : v1[s + 3 - 32]) : 0.0f;
+                        *reinterpret_cast<float4*>(row + s) = x;
+                    }
+                } else {
+                    const int t = tid - 64;
+    #pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint32_t pk[4];
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int s = 8 * ch + 2 * e;
+                            const float a0 = (s <= t) ? __uint_as_float(s < 32 ? v0[s] : v1[s - 32]) : 0.0f;
+                            const float a1 = (s + 1 <= t) ? __uint_as_float(s + 1 < 32 ? v0[s + 1] : v1[s + 1 - 32]) : 0.0f;
+                            pk[e] = pack_bf16(a0, a1);
+                        }
+                        *reinterpret_cast<uint4*>(base + OFF_AQ + sw128_off(t, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
                 }
             }
-            tmem_wait_st();
-        }
-        ph_mma ^= 1u;
-        mma_pending = false;
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        if (*s_abort) break;
-        // ---------------- H: Delta^T = U^T - S_m^T W^T ; O^T = S_m^T Q_bar^T
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id_d = idesc_bf16(128, 64, 0, 1, 1);
-            const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t ad = sw128_desc(sb + OFF_SM + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                mma_bf16(tmem + TM_D, ad, sw128_desc(sb + OFF_W + ks * 2048, 16, 1024), id_d, 1u);
-                mma_bf16(tmem + TM_O, ad,
-                         sw128_desc(sb + OFF_KQ + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_o,
-                         ks > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        // ---------------- I: Delta^T rows -> bf16 (A operand)
-        if (tid < 128) {
-            wait_or_abort(bar_mma, ph_mma);
-            tc_fence_after();
-            const int j = tid;
-            uint32_t v0[32], v1[32];
-            tmem_ld32(lane_base + TM_D, v0);
-            tmem_ld32(lane_base + TM_D + 32, v1);
-            tmem_wait_ld();
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = 8 * ch + 2 * e;
-                    pk[e] = pack_bf16(__uint_as_float(t < 32 ? v0[t] : v1[t - 32]),
-                                      __uint_as_float(t + 1 < 32 ? v0[t + 1] : v1[t + 1 - 32]));
-                }
-                *reinterpret_cast<uint4*>(base + OFF_DT + sw128_off(j, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-        }
-        ph_mma ^= 1u;
-        mma_pending = false;
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        if (*s_abort) break;
-        // ---------------- J: O^T += Delta^T A^T ; S^T += Delta^T K_til
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
-            const uint32_t id_s = idesc_bf16(128, 128, 0, 1, 0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ad = sw128_desc(sb + OFF_DT + ks * 32, 16, 1024);
-                mma_bf16(tmem + TM_O, ad, sw128_desc(sb + OFF_AQ + ks * 32, 16, 1024), id_o, 1u);
-                mma_bf16(tmem + TM_S, ad, sw128_desc(sb + OFF_KT + ks * 2048, 8192, 1024), id_s, 1u);
-            }
-            mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        // ---------------- K: outputs, staged as a [64 t][128 j] tile and stored by TMA
-        if (tid < 128) {
-            wait_or_abort(bar_mma, ph_mma);
-            tc_fence_after();
-            const int j = tid;
-            uint32_t v0[32], v1[32];
-            tmem_ld32(lane_base + TM_O, v0);
-            tmem_ld32(lane_base + TM_O + 32, v1);
-            tmem_wait_ld();
-            __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(base + OFF_OST) + j;
-#pragma unroll
-            for (int t = 0; t < kC; ++t)
-                ost[t * kD] = __float2bfloat16_rn(__uint_as_float(t < 32 ? v0[t] : v1[t - 32]));
+
+            ph_mma ^= 1u;
             fence_proxy_async();
             named_bar(2, 128);
-            if (tid == 0) {
-                tma_store_4d(&P.to, sb + OFF_OST, 0, h, t0, b);  // rows past T are clipped
-                bulk_commit();
+            // ---------------- D: T = (I + L)^{-1}  (warps 0-3)
+            {
+                if (tid < 64) {  // 16x16 diagonal blocks: right-looking substitution, one column per thread
+                    const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
+                    float acc[16];
+    #pragma unroll
+                    for (int r = 0; r < 16; ++r) acc[r] = (r == c) ? 1.0f : 0.0f;
+    #pragma unroll
+                    for (int s = 0; s < 16; ++s) {
+                        const float xs = acc[s];
+    #pragma unroll
+                        for (int r = s + 1; r < 16; ++r) acc[r] = fmaf(-LF[(o + r) * kLDF + o + s], xs, acc[r]);
+                    }
+    #pragma unroll
+                    for (int r = 0; r < 16; ++r) TF[(o + r) * kLDF + o + c] = acc[r];
+                }
+                named_bar(2, 128);
+                const int g = lane >> 2, q4 = lane & 3;
+                if (warp < 2) {  // 16 -> 32 merges: T_ij = -D_i (L_ij D_j), (i, j) = (1, 0), (3, 2)
+                    const int i = 2 * warp + 1, j = 2 * warp;
+                    float x[2][4];
+                    mma_tile_16x16(x, LF + (16 * i) * kLDF + 16 * j, kLDF, TF + (16 * j) * kLDF + 16 * j, kLDF, 2);
+                    float* xs = XT + (16 * warp) * kLDX;
+                    store_tile_16x16(x, xs, kLDX, 1.0f, g, q4);
+                    __syncwarp();
+                    mma_tile_16x16(x, TF + (16 * i) * kLDF + 16 * i, kLDF, xs, kLDX, 2);
+                    store_tile_16x16(x, TF + (16 * i) * kLDF + 16 * j, kLDF, -1.0f, g, q4);
+                }
+                named_bar(2, 128);
+                {  // 32 -> 64: X = L[32:64, 0:32] T[0:32, 0:32]; T[32:64, 0:32] = -T[32:64, 32:64] X
+                    const int mt = warp >> 1, nt0 = 2 * (warp & 1);
+                    float x[2][4];
+                    // T[0:16, 16:32] is zero: columns 16-31 take k-steps 2-3 only
+                    mma_tile_16xN(x, LF + (32 + 16 * mt) * kLDF, kLDF, TF + 8 * nt0, kLDF, nt0 >= 2 ? 2 : 0, 4);
+                    store_tile_16x16(x, XT + (16 * mt) * kLDX + 8 * nt0, kLDX, 1.0f, g, q4);
+                    named_bar(2, 128);
+                    // T[32:48, 48:64] is zero: rows 32-47 take k-steps 0-1 only
+                    mma_tile_16xN(x, TF + (32 + 16 * mt) * kLDF + 32, kLDF, XT + 8 * nt0, kLDX, 0, mt == 0 ? 2 : 4);
+                    store_tile_16x16(x, TF + (32 + 16 * mt) * kLDF + 8 * nt0, kLDF, -1.0f, g, q4);
+                }
+                named_bar(2, 128);
+                {  // T (lower triangle incl. diagonal) -> bf16 [t][s]
+                    const int t = tid >> 1, hf = tid & 1;
+    #pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int ch = 4 * hf + cc;
+                        uint32_t pk[4];
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int s = 8 * ch + 2 * e;
+                            const float a0 = (s <= t) ? TF[t * kLDF + s] : 0.0f;
+                            const float a1 = (s + 1 <= t) ? TF[t * kLDF + s + 1] : 0.0f;
+                            pk[e] = pack_bf16(a0, a1);
+                        }
+                        *reinterpret_cast<uint4*>(base + OFF_TT + sw128_off(t, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
             }
+            fence_proxy_async();
+            named_bar(2, 128);
+            // ---------------- E: W^T = K_bar^T T^T, U^T = V^T T^T
+            if (tid == 0) {
+                wait_or_abort(bar_v, ph_v);
+                tc_fence_after();
+                const uint32_t id = idesc_bf16(128, 64, 1, 0, 0);
+    #pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t bd = sw128_desc(sb + OFF_TT + ks * 32, 16, 1024);
+                    mma_bf16(tmem + TM_W, sw128_desc(sb + OFF_KQ + ks * 2048, 16384, 1024), bd, id, ks > 0);
+                    mma_bf16(tmem + TM_D, sw128_desc(sb + OFF_VIN + ks * 2048, 8192, 1024), bd, id, ks > 0);
+                }
+                mma_commit(bar_mma);
+                ++n_mma_issued;
+            }
+            ph_v ^= 1u;
+            // ---------------- F: W^T rows -> bf16 W (MN-major B operand); prefetch next v
+            {
+                wait_or_abort(bar_mma, ph_mma);
+                tc_fence_after();
+                if (tid == 0 && n + 1 < nchunks) {
+                    issue_v(n + 1);
+                    ++n_v_issued;
+                }
+                const int i = tid;
+                uint32_t v0[32], v1[32];
+                tmem_ld32(lane_base + TM_W, v0);
+                tmem_ld32(lane_base + TM_W + 32, v1);
+                tmem_wait_ld();
+    #pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t pk[4];
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int t = 8 * ch + 2 * e;
+                        pk[e] = pack_bf16(__uint_as_float(t < 32 ? v0[t] : v1[t - 32]),
+                                          __uint_as_float(t + 1 < 32 ? v0[t + 1] : v1[t + 1 - 32]));
+                    }
+                    *reinterpret_cast<uint4*>(base + OFF_W + sw128_off(i, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                // ---------------- G: state into the chunk's reference frame
+                const int j = tid;
+    #pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + TM_S + q * 32, r);
+                    tmem_wait_ld();
+    #pragma unroll
+                    for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * sm[SM_CF + (n & 1) * 128 + q * 32 + c]);
+                    tmem_st32(lane_base + TM_S + q * 32, r);
+                    const int katom = q >> 1;
+    #pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t pk[4];
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            pk[e] = pack_bf16(__uint_as_float(r[8 * cc + 2 * e]), __uint_as_float(r[8 * cc + 2 * e + 1]));
+                        *reinterpret_cast<uint4*>(base + OFF_SM + katom * 16384 + sw128_off(j, (q & 1) * 4 + cc)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
+                tmem_wait_st();
+            }
+
+            ph_mma ^= 1u;
+            fence_proxy_async();
+            tc_fence_before();
+            named_bar(2, 128);
+            // ---------------- H: Delta^T = U^T - S_m^T W^T ; O^T = S_m^T Q_bar^T
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t id_d = idesc_bf16(128, 64, 0, 1, 1);
+                const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
+    #pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t ad = sw128_desc(sb + OFF_SM + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                    mma_bf16(tmem + TM_D, ad, sw128_desc(sb + OFF_W + ks * 2048, 16, 1024), id_d, 1u);
+                    mma_bf16(tmem + TM_O, ad,
+                             sw128_desc(sb + OFF_KQ + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_o,
+                             ks > 0);
+                }
+                mma_commit(bar_mma);
+                ++n_mma_issued;
+            }
+            // ---------------- I: Delta^T rows -> bf16 (A operand)
+            {
+                wait_or_abort(bar_mma, ph_mma);
+                tc_fence_after();
+                const int j = tid;
+                uint32_t v0[32], v1[32];
+                tmem_ld32(lane_base + TM_D, v0);
+                tmem_ld32(lane_base + TM_D + 32, v1);
+                tmem_wait_ld();
+    #pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t pk[4];
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int t = 8 * ch + 2 * e;
+                        pk[e] = pack_bf16(__uint_as_float(t < 32 ? v0[t] : v1[t - 32]),
+                                          __uint_as_float(t + 1 < 32 ? v0[t + 1] : v1[t + 1 - 32]));
+                    }
+                    *reinterpret_cast<uint4*>(base + OFF_DT + sw128_off(j, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
+
+            ph_mma ^= 1u;
+            fence_proxy_async();
+            tc_fence_before();
+            named_bar(2, 128);
+            // ---------------- J: O^T += Delta^T A^T ; S^T += Delta^T K_til
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
+                const uint32_t id_s = idesc_bf16(128, 128, 0, 1, 0);
+    #pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t ad = sw128_desc(sb + OFF_DT + ks * 32, 16, 1024);
+                    mma_bf16(tmem + TM_O, ad, sw128_desc(sb + OFF_AQ + ks * 32, 16, 1024), id_o, 1u);
+                    mma_bf16(tmem + TM_S, ad, sw128_desc(sb + OFF_KT + ks * 2048, 8192, 1024), id_s, 1u);
+                }
+                mma_commit(bar_mma);
+                ++n_mma_issued;
+            }
+            // ---------------- K: outputs, staged as a [64 t][128 j] tile and stored by TMA
+            {
+                wait_or_abort(bar_mma, ph_mma);
+                tc_fence_after();
+                const int j = tid;
+                uint32_t v0[32], v1[32];
+                tmem_ld32(lane_base + TM_O, v0);
+                tmem_ld32(lane_base + TM_O + 32, v1);
+                tmem_wait_ld();
+                __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(base + OFF_OST) + j;
+    #pragma unroll
+                for (int t = 0; t < kC; ++t)
+                    ost[t * kD] = __float2bfloat16_rn(__uint_as_float(t < 32 ? v0[t] : v1[t - 32]));
+                fence_proxy_async();
+                named_bar(2, 128);
+                if (tid == 0) {
+                    tma_store_4d(&P.to, sb + OFF_OST, 0, h, t0, b);  // rows past T are clipped
+                    bulk_commit();
+                }
+            }
+
+            ph_mma ^= 1u;
+            tc_fence_before();
+        } else if (n + 1 < nchunks) {
+            // ======== warps 4-7: gains of chunk n + 1
+            prep_gains(n + 1);
         }
-        ph_mma ^= 1u;
-        mma_pending = false;
-        tc_fence_before();
+        if (n + 1 < nchunks) ph_in ^= 1u;
         __syncthreads();
         if (*s_abort) break;
     }
@@ -743,9 +780,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         }
     } else if (tid == 0) {
         // let copies and MMAs already issued land before the CTA's resources go away
-        if (mma_pending) mbar_wait(bar_mma, ph_mma, kWaitLimit);
-        if (in_pending) mbar_wait(bar_in, ph_in, kWaitLimit);
-        if (v_pending) mbar_wait(bar_v, ph_v, kWaitLimit);
+        if (n_mma_issued > 0) mbar_wait(bar_mma, (n_mma_issued - 1) & 1, kWaitLimit);
+        if (n_in_issued > 0) mbar_wait(bar_in, (n_in_issued - 1) & 1, kWaitLimit);
+        if (n_v_issued > 0) mbar_wait(bar_v, (n_v_issued - 1) & 1, kWaitLimit);
     }
     tc_fence_before();
     __syncthreads();
