@@ -507,17 +507,17 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 tmem_ld32(lane_base + TM_G + 32, v1);
                 tmem_wait_ld();
                 if (tid < 64) {
+                    // L rows as they come: only entries below the diagonal are ever read
                     const int t = tid;
                     float* row = LF + t * kLDF;
     #pragma unroll
                     for (int c4 = 0; c4 < 16; ++c4) {
-                        float4 x;
                         const int s = 4 * c4;
-                        x.x = (s + 0 < t) ? __uint_as_float(s + 0 < 32 ? v0[s + 0] : v1[s + 0 - 32]) : 0.0f;
-                        x.y = (s + 1 < t) ? __uint_as_float(s + 1 < 32 ? v0[s + 1] : v1[s + 1 - 32]) : 0.0f;
-                        x.z = (s + 2 < t) ? __uint_as_float(s + 2 < 32 ? v0[s + 2] : v1[s + 2 - 32]) : 0.0f;
-                        x.w = (s + 3 < t) ? __uint_as_float(s + 3 < 32 ? v0[s + 3] : v1[s + 3 - 32]) : 0.0f;
-                        *reinterpret_cast<float4*>(row + s) = x;
+                        *reinterpret_cast<float4*>(row + s) =
+                            make_float4(__uint_as_float(s + 0 < 32 ? v0[s + 0] : v1[s + 0 - 32]),
+                                        __uint_as_float(s + 1 < 32 ? v0[s + 1] : v1[s + 1 - 32]),
+                                        __uint_as_float(s + 2 < 32 ? v0[s + 2] : v1[s + 2 - 32]),
+                                        __uint_as_float(s + 3 < 32 ? v0[s + 3] : v1[s + 3 - 32]));
                     }
                 } else {
                     const int t = tid - 64;
@@ -646,7 +646,13 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     tmem_ld32(lane_base + TM_S + q * 32, r);
                     tmem_wait_ld();
     #pragma unroll
-                    for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * sm[SM_CF + (n & 1) * 128 + q * 32 + c]);
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 f = *reinterpret_cast<const float4*>(sm + SM_CF + (n & 1) * 128 + q * 32 + 4 * c4);
+                        r[4 * c4 + 0] = __float_as_uint(__uint_as_float(r[4 * c4 + 0]) * f.x);
+                        r[4 * c4 + 1] = __float_as_uint(__uint_as_float(r[4 * c4 + 1]) * f.y);
+                        r[4 * c4 + 2] = __float_as_uint(__uint_as_float(r[4 * c4 + 2]) * f.z);
+                        r[4 * c4 + 3] = __float_as_uint(__uint_as_float(r[4 * c4 + 3]) * f.w);
+                    }
                     tmem_st32(lane_base + TM_S + q * 32, r);
                     const int katom = q >> 1;
     #pragma unroll

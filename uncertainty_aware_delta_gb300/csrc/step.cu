@@ -23,7 +23,7 @@ constexpr int kStepNT = 256;
 constexpr int kMaxRegF4 = 16;  // float4 of S per thread for d_k = d_v = 128
 
 template <typename TIO>
-__global__ void __launch_bounds__(kStepNT)
+__global__ void __launch_bounds__(kStepNT, 2)
 step_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TIO* __restrict__ v,
             const float* __restrict__ la, const float* __restrict__ om, const float* __restrict__ r,
             float* __restrict__ S, float* __restrict__ p, TIO* __restrict__ o, int variant, int DK,
@@ -36,6 +36,18 @@ step_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TIO* __r
 
     const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (bh == 0 && tid == 0 && status) *status = 0u;
+    // -- the one read of this head's S (128-bit loads), issued first so its latency
+    //    overlaps the gain computation below
+    const int NC4 = DV / 4;                 // float4 columns
+    const int NRG = kStepNT / NC4;          // row groups
+    const int c4 = tid % NC4, rg = tid / NC4;
+    float4* S4 = reinterpret_cast<float4*>(S + (size_t)bh * DK * DV);
+    float4 reg[kMaxRegF4];
+#pragma unroll
+    for (int m = 0; m < kMaxRegF4; ++m) {
+        const int i = rg + m * NRG;
+        if (i < DK) reg[m] = S4[(size_t)i * NC4 + c4];
+    }
     const size_t vec = (size_t)bh * DK;
     const float rt = r[bh];
 
@@ -98,18 +110,12 @@ step_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TIO* __r
     kq = 0.f;
     for (int w = 0; w < kStepNT / 32; ++w) kq += s_red[w][3];
 
-    // -- one read of S: per column, sum_i (a_i k_i) S_ij and sum_i (a_i q_i) S_ij
-    const int NC4 = DV / 4;                 // float4 columns
-    const int NRG = kStepNT / NC4;          // row groups
-    const int c4 = tid % NC4, rg = tid / NC4;
-    float4* S4 = reinterpret_cast<float4*>(S + (size_t)bh * DK * DV);
-    float4 reg[kMaxRegF4];
+    // -- per column, sum_i (a_i k_i) S_ij and sum_i (a_i q_i) S_ij from the registers
     float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int m = 0; m < kMaxRegF4; ++m) {
         const int i = rg + m * NRG;
         if (i < DK) {
-            reg[m] = S4[(size_t)i * NC4 + c4];
             const float ak = s_ak[i], aq = s_aq[i];
             pk[0] = fmaf(ak, reg[m].x, pk[0]); pk[1] = fmaf(ak, reg[m].y, pk[1]);
             pk[2] = fmaf(ak, reg[m].z, pk[2]); pk[3] = fmaf(ak, reg[m].w, pk[3]);
