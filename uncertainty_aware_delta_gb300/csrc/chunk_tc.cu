@@ -198,6 +198,21 @@ __device__ __forceinline__ void store_tile_16x16(const float (&x)[2][4], float* 
     }
 }
 
+// The same tile, scaled, as bf16 pairs into a 128-byte-swizzled [row][col] tile
+// (rows r0.., columns c0..; 64 bf16 per row).
+__device__ __forceinline__ void store_tile_bf16(const float (&x)[2][4], unsigned char* tile, int r0, int c0,
+                                                float scale, int g, int q) {
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        const int col = c0 + 8 * n + 2 * q;
+        const uint32_t off = (col & 7) * 2;
+        *reinterpret_cast<uint32_t*>(tile + sw128_off(r0 + g, col >> 3) + off) =
+            pack_bf16(scale * x[n][0], scale * x[n][1]);
+        *reinterpret_cast<uint32_t*>(tile + sw128_off(r0 + g + 8, col >> 3) + off) =
+            pack_bf16(scale * x[n][2], scale * x[n][3]);
+    }
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
@@ -251,11 +266,15 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         tma_load_4d(sb + OFF_VIN + 8192, &P.tv, 64, h, n * kC, b, bar_v);
     };
     __syncthreads();
-    int n_in_issued = 0, n_v_issued = 0, n_mma_issued = 0, n_o_issued = 0;   // meaningful in thread 0
+    // copies and MMAs issued so far (thread 0: v, MMAs; thread 128: q, k, log_alpha, omega)
+    int n_in_issued = 0, n_v_issued = 0, n_mma_issued = 0, n_o_issued = 0;
     if (tid == 0 && nchunks > 0) {
-        issue_inputs(0);
         issue_v(0);
-        n_in_issued = n_v_issued = 1;
+        n_v_issued = 1;
+    }
+    if (tid == 128 && nchunks > 0) {
+        issue_inputs(0);
+        n_in_issued = 1;
     }
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
@@ -281,6 +300,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             tmem_st32(lane_base + TM_S + q * 32, r);
         }
         tmem_wait_st();
+    } else {
+        // blocks of T above the diagonal are never written: zero its bf16 tile once
+        uint4* tt4 = reinterpret_cast<uint4*>(base + OFF_TT);
+        for (int e = tid - 128; e < 8192 / 16; e += 256) tt4[e] = make_uint4(0u, 0u, 0u, 0u);
     }
     tc_fence_before();
     __syncthreads();
@@ -528,7 +551,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             // Diagonal: the gain denominator z_t = r_t + sum_i p_hat_t,i k_t,i^2 is the
             // half-warp sum of K_bar . K_til' (the decay factors cancel), and K_til = K_til' / z.
             const int u = tid - 128, g = u & 15, tr = u >> 4;
-#pragma unroll 1
+#pragma unroll 2
             for (int m4 = 0; m4 < 4; ++m4) {
                 const int t = tr + 16 * m4;
                 const uint32_t sw = sw128_off(t, g >> 1) + (g & 1) * 8;
@@ -555,9 +578,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 }
                 float sc;
                 if (!ISO) {
-                    float dot = 0.0f;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) dot = fmaf(kb[c], kt[c], dot);
+                    float dot = fmaf(kb[0], kt[0], kb[1] * kt[1]) + fmaf(kb[2], kt[2], kb[3] * kt[3]) +
+                                (fmaf(kb[4], kt[4], kb[5] * kt[5]) + fmaf(kb[6], kt[6], kb[7] * kt[7]));
 #pragma unroll
                     for (int x = 8; x >= 1; x >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, x);
                     sc = t < nv ? __fdividef(1.0f, sm[SM_R + t] + dot) : 0.0f;
@@ -580,12 +602,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         tc_fence_before();
         __syncthreads();
         if (*s_abort) break;
-        // ================= step 2: prefetch the next inputs; Gram and query MMAs (thread 0)
+        // ================= step 2: Gram and query MMAs (thread 0), prefetch of the next inputs (thread 128)
         if (tid == 0) {
-            if (n + 1 < nchunks) {
-                issue_inputs(n + 1);
-                ++n_in_issued;
-            }
             tc_fence_after();
             const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
 #pragma unroll
@@ -603,6 +621,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                                 ks > 0);
             mma_commit(bar_o);
             ++n_o_issued;
+        }
+        if (tid == 128 && n + 1 < nchunks) {   // the operand pass has consumed the inputs
+            issue_inputs(n + 1);
+            ++n_in_issued;
         }
         // ================= step 3
         if (wg2) {
@@ -643,7 +665,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             }
             tc_fence_before();
             named_bar(kBarWG2, 128);
-            // ---- T = (I + L)^{-1}
+            // ---- T = (I + L)^{-1}; each finished block also goes to the bf16 tile T [t][s]
+            //      (its blocks above the diagonal stay zero from the start)
+            unsigned char* tt = base + OFF_TT;
             if (lt < 64) {  // 16x16 diagonal blocks: right-looking substitution, one column per thread
                 const int blk = lt >> 4, c = lt & 15, o = 16 * blk;
                 float acc[16];
@@ -655,8 +679,13 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 #pragma unroll
                     for (int r = s + 1; r < 16; ++r) acc[r] = fmaf(-LF[(o + r) * kLDF + o + s], xs, acc[r]);
                 }
+                __nv_bfloat16* tcol = reinterpret_cast<__nv_bfloat16*>(tt + ((o + c) & 7) * 2);
 #pragma unroll
-                for (int r = 0; r < 16; ++r) TF[(o + r) * kLDF + o + c] = acc[r];
+                for (int r = 0; r < 16; ++r) {
+                    TF[(o + r) * kLDF + o + c] = acc[r];
+                    *reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<unsigned char*>(tcol) +
+                                                       sw128_off(o + r, (o + c) >> 3)) = __float2bfloat16_rn(acc[r]);
+                }
             }
             named_bar(kBarWG2, 128);
             const int g8 = lane >> 2, q4 = lane & 3;
@@ -669,6 +698,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 __syncwarp();
                 mma_tile_16x16(x, TF + (16 * i) * kLDF + 16 * i, kLDF, xs, kLDX, 2);
                 store_tile_16x16(x, TF + (16 * i) * kLDF + 16 * j, kLDF, -1.0f, g8, q4);
+                store_tile_bf16(x, tt, 16 * i, 16 * j, -1.0f, g8, q4);
             }
             named_bar(kBarWG2, 128);
             {  // 32 -> 64: X = L[32:64, 0:32] T[0:32, 0:32]; T[32:64, 0:32] = -T[32:64, 32:64] X
@@ -680,24 +710,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 named_bar(kBarWG2, 128);
                 // T[32:48, 48:64] is zero: rows 32-47 take k-steps 0-1 only
                 mma_tile_16xN(x, TF + (32 + 16 * mt) * kLDF + 32, kLDF, XT + 8 * nt0, kLDX, 0, mt == 0 ? 2 : 4);
-                store_tile_16x16(x, TF + (32 + 16 * mt) * kLDF + 8 * nt0, kLDF, -1.0f, g8, q4);
-            }
-            named_bar(kBarWG2, 128);
-            {  // T (lower triangle incl. diagonal) -> bf16 [t][s]
-                const int t = lt >> 1, hf = lt & 1;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int ch = 4 * hf + cc;
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s = 8 * ch + 2 * e;
-                        const float a0 = (s <= t) ? TF[t * kLDF + s] : 0.0f;
-                        const float a1 = (s + 1 <= t) ? TF[t * kLDF + s + 1] : 0.0f;
-                        pk[e] = pack_bf16(a0, a1);
-                    }
-                    *reinterpret_cast<uint4*>(base + OFF_TT + sw128_off(t, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
+                store_tile_bf16(x, tt, 32 + 16 * mt, 8 * nt0, -1.0f, g8, q4);
             }
             fence_proxy_async();
             named_bar(kBarTReady, 256);   // -> warps 0-3 issue the W/U MMAs
@@ -827,12 +840,14 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             if (!ISO) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = p_reg;
             else if (tid == 128) P.p_T[bh] = b_iso;
         }
-    } else if (tid == 0) {
+    } else {
         // let copies and MMAs already issued land before the CTA's resources go away
-        if (n_mma_issued > 0) mbar_wait(bar_mma, (n_mma_issued - 1) & 1, kWaitLimit);
-        if (n_o_issued > 0) mbar_wait(bar_o, (n_o_issued - 1) & 1, kWaitLimit);
-        if (n_in_issued > 0) mbar_wait(bar_in, (n_in_issued - 1) & 1, kWaitLimit);
-        if (n_v_issued > 0) mbar_wait(bar_v, (n_v_issued - 1) & 1, kWaitLimit);
+        if (tid == 0) {
+            if (n_mma_issued > 0) mbar_wait(bar_mma, (n_mma_issued - 1) & 1, kWaitLimit);
+            if (n_o_issued > 0) mbar_wait(bar_o, (n_o_issued - 1) & 1, kWaitLimit);
+            if (n_v_issued > 0) mbar_wait(bar_v, (n_v_issued - 1) & 1, kWaitLimit);
+        }
+        if (tid == 128 && n_in_issued > 0) mbar_wait(bar_in, (n_in_issued - 1) & 1, kWaitLimit);
     }
     tc_fence_before();
     __syncthreads();
