@@ -4,37 +4,40 @@
 // One CTA owns one (b, h) sequence and walks its chunks in order; per chunk:
 //   A1  uncertainty recurrence (KDN paper Sec. 4.1 Eq. 23-27 with the
 //       information-scaled update Eq. 60-65, i.e. the Moebius map of Eq. 32-37
-//       applied token by token; the chunk carry is the per-channel variance
-//       held in a register).  Isotropic variant (Sec. 4.2 Eq. 40, App. C): the
+//       applied token by token in projective form (numerator, denominator),
+//       which keeps the carry chain free of divisions; the chunk carry is the
+//       per-channel variance as that pair, held in registers).  Isotropic variant (Sec. 4.2 Eq. 40, App. C): the
 //       scalar map is composed as 2x2 Moebius matrices with a warp-shuffle
 //       inclusive scan over the chunk's tokens, then replayed from the carry.
 //       The decay factors relative to the chunk's per-channel reference
 //       G_ref = G_C / 2 (App. D: decay ratios from differences of cumulative
 //       log-decay) are running products e1_t = e^{G_t - G_ref}, e2_t = 1 / e1_t.
 //   A2  decayed operands (bf16, 128-byte-swizzled, tensor-core layouts):
-//         K_bar = k e1, Q_bar = q e1, K_til = p_hat k e2 / z  (diagonal),
-//       where the gain denominator z_t = r_t + sum_i p_hat_t,i k_t,i^2 (Eq. 25)
-//       is the half-warp sum of K_bar . (p_hat k e2) over the token's row (the
-//       decay factors cancel); the isotropic variant scales k e2 by its gain.
-//   B   Gram MMA  [K_bar; Q_bar] K_til^T  (M = 128: rows 0-63 give L, rows
-//       64-127 the query-write matrix A, diagonal kept); the query MMA
-//       O^T = S_m^T Q_bar^T is issued with it.
-//   C,D T = (I + strict_lower(L))^{-1}, 16x16 diagonal blocks by forward
-//       substitution, merged 16 -> 32 -> 64 (tf32 mma.sync).
-//   E   W^T = K_bar^T T^T and U^T = V^T T^T (MMA, fp32 in TMEM).
+//         K_bar = k e1, Q_bar = q e1, K_til' = p_hat k e2  (the isotropic
+//       variant uses its scalar b_hat in place of p_hat).
+//   B   Gram MMA  [K_bar; Q_bar] K_til'^T  (M = 128: rows 0-63 give the key
+//       block, rows 64-127 the query-write matrix A', diagonal kept), and the
+//       prediction/query MMA [Z^T | O^T] = S_m^T [K_bar; Q_bar]^T (N = 128).
+//   C,D The gains are kappa = p_hat k / z with z_t = r_t + sum_i p_hat_t,i k_t,i^2
+//       (Eq. 25).  Since K_bar_t . K_til'_t = sum_i p_hat_t,i k_t,i^2 (the decay
+//       factors cancel), the scaled innovations Delta' = diag(1/z) Delta solve
+//       M Delta' = V - K_bar S_m  with  M = diag(r) + lower_incl(K_bar K_til'^T),
+//       so z comes out of the Gram MMA.  T = M^{-1}: 16x16 diagonal blocks by
+//       forward substitution, merged 16 -> 32 -> 64 (tf32 mma.sync).
 //   G   state: S_m^T = S_in^T diag(e^{G_ref}) in TMEM, plus a bf16 copy in TMEM
-//       that is the A operand of the next MMAs.
-//   H   Delta^T = U^T - S_m^T W^T  (innovations; -W is stored so the MMA adds).
-//   J   O^T += Delta^T A^T ; S^T += Delta^T K_til  (Delta^T in bf16 in TMEM as
-//       the A operand; the state stays in TMEM, the pending factor
+//       that is the A operand of the prediction/query MMA.
+//   H   Delta'^T = (V^T - Z^T) T^T = V^T T^T + (-Z^T) T^T (-Z^T in bf16 in TMEM
+//       as an A operand).
+//   J   O^T += Delta'^T A'^T ; S^T += Delta'^T K_til'  (Delta'^T in bf16 in TMEM
+//       as the A operand; the state stays in TMEM, the pending factor
 //       e^{G_C - G_ref} is folded into the next chunk's scaling).
-//   K   o = O (bf16) to global memory by TMA, one chunk later (O is double
-//       buffered in TMEM).
-// Schedule per chunk n: warps 0-3 move the state into the chunk's frame while
-// warps 4-11 build the operands; one thread issues the Gram and query MMAs and
-// prefetches chunk n+1; then warps 8-11 read out the Gram matrix and invert the
-// triangular system, warps 0-3 store the outputs of chunk n-1 and run E-J, and
-// warps 4-7 compute the gains of chunk n+1 (A1) at the same time.
+//   K   o = O (bf16) to global memory by TMA at the start of the next chunk.
+// Schedule per chunk n: warps 0-3 store the outputs of chunk n-1 and move the
+// state into the chunk's frame while warps 4-11 build the operands; one thread
+// issues the Gram and prediction/query MMAs, another prefetches chunk n+1; then
+// warps 8-11 read out the Gram matrix and invert the triangular system while
+// warps 0-3 convert the prediction and run H-J, and warps 4-7 compute the gains
+// of chunk n+1 (A1).
 // This is the compact-WY / UT chunk form of the paper's App. D evaluated with
 // per-channel decay; Preconditioned DeltaNet prints the same algebra without
 // decay (its Eq. 6 / App. F.2.1).  All MMAs are tcgen05 kind::f16 (bf16
@@ -75,12 +78,11 @@ constexpr uint32_t OFF_KIN = 16384;    // k tile
 constexpr uint32_t OFF_VIN = 32768;    // v tile (MN-major A operand of U^T)
 constexpr uint32_t OFF_LA = 49152;     // log_alpha [64][128] fp32 -> e1 in place
 constexpr uint32_t OFF_OM = 81920;     // omega [64][128] fp32 -> p_hat e2 (diagonal) / e2 (isotropic)
-constexpr uint32_t OFF_KQ = 114688;    // [K_bar; Q_bar] 128 rows x 128, two 16 KB K-atoms; the
-                                       //   Q_bar halves later stage the o tile ([64 t][64 j] each)
+constexpr uint32_t OFF_KQ = 114688;    // [K_bar; Q_bar] 128 rows x 128, two 16 KB K-atoms
 constexpr uint32_t OFF_KT = 147456;    // K_til' [64 s][128 i], two 8 KB K-atoms
 constexpr uint32_t OFF_AQ = 163840;    // A [64 t][64 s] bf16
-constexpr uint32_t OFF_LF = 172032;    // L fp32 [64][kLDF]
-constexpr uint32_t OFF_W = OFF_LF;     //   later -W [128 i][64 t] bf16 (MN-major B)
+constexpr uint32_t OFF_LF = 172032;    // L fp32 [64][kLDF]; before that (step 1) the o tile of the
+                                       //   previous chunk, two [64 t][64 j] bf16 tiles for TMA stores
 constexpr uint32_t OFF_TT = 189440;    // T [64 t][64 s] bf16
 constexpr uint32_t OFF_TF = 197632;    // T fp32 [64][kLDF]
 constexpr uint32_t OFF_XT = 215040;    // merge temporaries fp32 [32][kLDX]
@@ -88,9 +90,9 @@ constexpr uint32_t OFF_SMALL = 219648;
 constexpr int kLDF = 68;
 constexpr int kLDX = 36;
 // small region, float offsets
-constexpr int SM_R = 0, SM_MUR = 64, SM_INVZ = 128, SM_ZP = 192, SM_AP = 448, 
+constexpr int SM_R = 0, SM_MUR = 64, SM_BHAT = 128, SM_ZP = 192, SM_AP = 448, SM_RZ = 704 /* [2][64] */,
               SM_FOUT = 832, SM_OMI = 960, SM_FLAG = 1024, SM_CF = 1032 /* [2][128] by chunk parity */,
-              SM_FLOATS = 1288;
+              SM_INVD = 1288, SM_FLOATS = 1352;
 constexpr uint32_t OFF_BAR = OFF_SMALL + SM_FLOATS * 4;
 constexpr uint32_t kSmemBytes = OFF_BAR + 64;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
@@ -99,11 +101,11 @@ static_assert(OFF_XT + 32 * kLDX * 4 <= OFF_SMALL, "merge scratch before the sma
 static_assert(OFF_LF + 64 * kLDF * 4 <= OFF_TT, "L fp32 before T");
 static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
 
-// TMEM columns (one CTA per SM, all 512 allocated): state S^T (fp32), U^T then
-// Delta^T, O^T double-buffered by chunk parity, Gram then W^T, the bf16 copy of
-// S_m^T (A operand, two values per column) and the bf16 Delta^T.
-constexpr uint32_t TM_S = 0, TM_D = 128, TM_O = 192 /* [2] x 64 */, TM_GW = 320, TM_SMB = 384,
-                   TM_DB = 448, TM_COLS = 512;
+// TMEM columns (one CTA per SM, 512 allocated): state S^T (fp32); Z^T = S_m^T K_bar^T
+// then Delta^T, directly followed by O^T (one N = 128 MMA writes both Z^T and O^T);
+// the Gram matrix; the bf16 copy of S_m^T (A operand, two values per column); and
+// the bf16 A operand -Z^T, later Delta^T.
+constexpr uint32_t TM_S = 0, TM_ZD = 128, TM_O = 192, TM_G = 256, TM_SMB = 320, TM_DB = 384, TM_COLS = 512;
 
 struct TcParams {
     CUtensorMap tq, tk, tv, tla, tom, to;
@@ -216,6 +218,11 @@ __device__ __forceinline__ void store_tile_bf16(const float (&x)[2][4], unsigned
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
+__device__ __forceinline__ float rcp_approx(float x) {   // 1 / x, hardware approximation
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float ex2(float x) {   // 2^x, hardware approximation
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -281,10 +288,12 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
 
     // per-thread recurrent state
-    float p_reg = 1.0f;   // diagonal: variance of channel tid - 128 (warps 4-7)
+    // diagonal: variance of channel tid - 128 (warps 4-7) in projective form p = pn / pd,
+    // pd renormalised to [1, 2) by powers of two
+    float pn = 1.0f, pd = 1.0f;
     float pend2 = 0.0f;   // pending log2-factor of the previous chunk, (G_C - G_ref) log2(e) (warps 4-7)
     float b_iso = 1.0f;   // isotropic scalar variance (warp 4)
-    if (wg1 && !ISO && P.p0) p_reg = P.p0[static_cast<size_t>(bh) * kD + (tid - 128)];
+    if (wg1 && !ISO && P.p0) pn = P.p0[static_cast<size_t>(bh) * kD + (tid - 128)];
     if (ISO && warp == 4 && P.p0) b_iso = P.p0[bh];
     // initial state S^T into TMEM: lane j = value column, columns = key channel
     if (wg0) {
@@ -310,10 +319,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     tc_fence_after();
 
     uint32_t ph_in = 0, ph_v = 0;
-    // bar_mma completes four phases per chunk, in this order and with these parities:
-    // Gram (0), W/U (1), innovations (0), update (1).  bar_o completes once per chunk
-    // (query MMA), parity = chunk & 1.
-    constexpr uint32_t kParGram = 0, kParWU = 1, kParInno = 0, kParUpd = 1;
+    // bar_mma completes three phases per chunk n: Gram (parity n & 1), innovations
+    // ((n + 1) & 1), update (n & 1).  bar_o completes once per chunk (query and
+    // prediction MMA), parity n & 1.
     auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
         if (*s_abort) return;
         if (!mbar_wait(bar, parity, kWaitLimit)) {
@@ -350,6 +358,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 if (ISO) om = P.om_iso[th];
             }
             sm[SM_R + t] = rr;
+            sm[SM_RZ + (c & 1) * 64 + t] = rr;
             sm[SM_MUR + t] = P.mu / rr;
             sm[SM_OMI + t] = om;
         }
@@ -397,7 +406,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     mr[4 * u4 + 2] = m4.z;
                     mr[4 * u4 + 3] = m4.w;
                 }
-                // ... then the carries: variance and decay factors
+                // ... then the carries: variance and decay factors.  The variance map
+                // p -> a^2 p + omega -> p_hat / (1 + c p_hat), c = mu k^2 / r, is the
+                // Moebius matrix [[a^2, omega], [c a^2, 1 + c omega]] acting on (pn, pd):
+                // two independent multiply-adds per token, p_hat_t = pn_t / pd_{t-1}.
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int t = tb + u;
@@ -407,9 +419,18 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     e2 *= ial;
                     LA[t * kD + i] = e1;
                     if (!ISO) {
-                        const float ph = fmaf(a2, p_reg, om[u]);
-                        p_reg = __fdividef(ph, fmaf(mr[u] * k2, ph, 1.0f));
-                        OM[t * kD + i] = ph * e2;
+                        const float c = mr[u] * k2, rd = rcp_approx(pd);
+                        const float n1 = fmaf(a2, pn, om[u] * pd);
+                        const float d1 = fmaf(c * a2, pn, fmaf(c, om[u], 1.0f) * pd);
+                        OM[t * kD + i] = (n1 * rd) * e2;
+                        pn = n1;
+                        pd = d1;
+                        if ((u & 3) == 3) {   // exact rescale: pd back to [1, 2)
+                            const int ex = min((__float_as_int(pd) >> 23) & 0xff, 253);
+                            const float sc = __int_as_float((254 - ex) << 23);
+                            pn *= sc;
+                            pd *= sc;
+                        }
                     } else {
                         OM[t * kD + i] = e2;
                         w[qt * 16 + u] = k2;
@@ -466,13 +487,12 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int t = 2 * lane + e;
-                    float beta = 0.0f;
+                    float bhat = 0.0f;
                     if (t < nvc) {
-                        const float bhat = fmaf(aa[e], bb, oo[e]);
-                        beta = bhat / (rr[e] + bhat * kk[e]);
+                        bhat = fmaf(aa[e], bb, oo[e]);
                         bb = bhat / fmaf(uu[e], bhat, 1.0f);
                     }
-                    sm[SM_INVZ + t] = beta;
+                    sm[SM_BHAT + t] = bhat;
                 }
                 b_iso = __shfl_sync(0xffffffffu, bb, 31);
             }
@@ -481,27 +501,26 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 
     // ------------------------------------------------------------------ warps 0-3
     // Outputs of a finished chunk: O^T rows out of TMEM, staged as two [64 t][64 j]
-    // tiles in the Q_bar halves of the operand buffer (free once the Gram and
-    // query MMAs completed), two TMA stores (rows past T are clipped).
+    // tiles over the L region (free until the Gram readout), two TMA stores (rows
+    // past T are clipped).
     auto emit_outputs = [&](int c) {
         uint32_t v0[32], v1[32];
         tc_fence_after();
-        tmem_ld64(TM_O + 64 * (c & 1), v0, v1);
-        __nv_bfloat16* ost =
-            reinterpret_cast<__nv_bfloat16*>(base + OFF_KQ + (tid >> 6) * 16384 + 8192) + (tid & 63);
+        tmem_ld64(TM_O, v0, v1);
+        __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(base + OFF_LF + (tid >> 6) * 8192) + (tid & 63);
 #pragma unroll
         for (int t = 0; t < kC; ++t)
             ost[t * 64] = __float2bfloat16_rn(__uint_as_float(t < 32 ? v0[t] : v1[t - 32]));
         fence_proxy_async();
         named_bar(kBarWG0, 128);
         if (tid == 0 && !*s_abort) {
-            tma_store_4d(&P.to, sb + OFF_KQ + 8192, 0, h, c * kC, b);
-            tma_store_4d(&P.to, sb + OFF_KQ + 16384 + 8192, 64, h, c * kC, b);
+            tma_store_4d(&P.to, sb + OFF_LF, 0, h, c * kC, b);
+            tma_store_4d(&P.to, sb + OFF_LF + 8192, 64, h, c * kC, b);
             bulk_commit();
         }
     };
     // State of chunk c into its reference frame: S_m^T = S^T diag(cf) in TMEM, and
-    // its bf16 copy (A operand of the query and innovation MMAs) in TMEM.
+    // its bf16 copy (A operand of the query and prediction MMA) in TMEM.
     auto scale_state = [&](int c) {
         tc_fence_after();
 #pragma unroll 1
@@ -541,20 +560,24 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 #pragma unroll 1
     for (int n = 0; n < nchunks; ++n) {
         const int t0 = n * kC, nv = min(kC, T - t0);
-        // ================= step 1: state frame || operands
-        if (n > 0) wait_or_abort(bar_mma, kParUpd);   // update of chunk n-1 has landed
+        const uint32_t pb = static_cast<uint32_t>(n) & 1u;
+        // ================= step 1: outputs of chunk n-1, state frame || operands
+        if (n > 0) wait_or_abort(bar_mma, pb ^ 1u);   // update of chunk n-1 has landed
         if (wg0) {
+            if (n > 0) emit_outputs(n - 1);
             scale_state(n);
+            if (tid == 0) bulk_wait_read();   // the o tile has left the L region
         } else {
             // decayed bf16 operands (warps 4-11): thread -> 4 channels in each K-atom
             // (8-byte pieces of the swizzled rows), 16 threads (half a warp) per token row.
-            // Diagonal: the gain denominator z_t = r_t + sum_i p_hat_t,i k_t,i^2 is the
-            // half-warp sum of K_bar . K_til' (the decay factors cancel), and K_til = K_til' / z.
+            // K_til' = p_hat k e2 (isotropic: b_hat k e2); the gain denominator enters
+            // through the diagonal of the triangular system.
             const int u = tid - 128, g = u & 15, tr = u >> 4;
 #pragma unroll 2
             for (int m4 = 0; m4 < 4; ++m4) {
                 const int t = tr + 16 * m4;
                 const uint32_t sw = sw128_off(t, g >> 1) + (g & 1) * 8;
+                const float sc = ISO ? sm[SM_BHAT + t] : 1.0f;
                 float kb[8], qb[8], kt[8];
 #pragma unroll
                 for (int a = 0; a < 2; ++a) {
@@ -576,16 +599,6 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     kt[4 * a + 2] = k2 * kp.z;
                     kt[4 * a + 3] = k3 * kp.w;
                 }
-                float sc;
-                if (!ISO) {
-                    float dot = fmaf(kb[0], kt[0], kb[1] * kt[1]) + fmaf(kb[2], kt[2], kb[3] * kt[3]) +
-                                (fmaf(kb[4], kt[4], kb[5] * kt[5]) + fmaf(kb[6], kt[6], kb[7] * kt[7]));
-#pragma unroll
-                    for (int x = 8; x >= 1; x >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, x);
-                    sc = t < nv ? __fdividef(1.0f, sm[SM_R + t] + dot) : 0.0f;
-                } else {
-                    sc = sm[SM_INVZ + t];
-                }
 #pragma unroll
                 for (int a = 0; a < 2; ++a) {
                     *reinterpret_cast<uint2*>(base + OFF_KQ + a * 16384 + sw) =
@@ -602,7 +615,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         tc_fence_before();
         __syncthreads();
         if (*s_abort) break;
-        // ================= step 2: Gram and query MMAs (thread 0), prefetch of the next inputs (thread 128)
+        // ================= step 2: Gram and prediction/query MMAs (thread 0), prefetch of the next inputs (thread 128)
         if (tid == 0) {
             tc_fence_after();
             const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
@@ -610,14 +623,16 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             for (int ks = 0; ks < 8; ++ks) {
                 const uint64_t ad = sw128_desc(sb + OFF_KQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
                 const uint64_t bd = sw128_desc(sb + OFF_KT + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-                mma_bf16(tmem + TM_GW, ad, bd, id, ks > 0);
+                mma_bf16(tmem + TM_G, ad, bd, id, ks > 0);
             }
             mma_commit(bar_mma);
             ++n_mma_issued;
+            // [Z^T | O^T] = S_m^T [K_bar; Q_bar]^T  (N = 128: prediction and query together)
+            const uint32_t id_zo = idesc_bf16(128, 128, 0, 0, 0);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                mma_bf16_tmem_a(tmem + TM_O + 64 * (n & 1), tmem + TM_SMB + 8 * ks,
-                                sw128_desc(sb + OFF_KQ + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id,
+                mma_bf16_tmem_a(tmem + TM_ZD, tmem + TM_SMB + 8 * ks,
+                                sw128_desc(sb + OFF_KQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_zo,
                                 ks > 0);
             mma_commit(bar_o);
             ++n_o_issued;
@@ -628,15 +643,16 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         }
         // ================= step 3
         if (wg2) {
-            // ---- Gram rows out of TMEM: L (fp32, columns scaled by 1 / z), query-write matrix A (bf16)
+            // ---- Gram rows out of TMEM: M (fp32), query-write matrix A' (bf16)
             const int lt = tid - 256, lw = warp - 8;
             {
-                wait_or_abort(bar_mma, kParGram);
+                wait_or_abort(bar_mma, pb);
                 tc_fence_after();
                 uint32_t v0[32], v1[32];
-                tmem_ld64(TM_GW, v0, v1);
+                tmem_ld64(TM_G, v0, v1);
                 if (lt < 64) {
-                    // only entries below the diagonal of L are ever read
+                    // M = diag(r) + lower_incl(K_bar K_til'^T): its diagonal is the gain
+                    // denominator z_t = r_t + sum_i p_hat_t,i k_t,i^2 (the decay factors cancel)
                     float* row = LF + lt * kLDF;
 #pragma unroll
                     for (int c4 = 0; c4 < 16; ++c4) {
@@ -647,6 +663,19 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                                         __uint_as_float(s + 2 < 32 ? v0[s + 2] : v1[s + 2 - 32]),
                                         __uint_as_float(s + 3 < 32 ? v0[s + 3] : v1[s + 3 - 32]));
                     }
+                    // column lt of row lt: a 5-level select tree on the lane bits
+                    uint32_t x[32];
+#pragma unroll
+                    for (int s = 0; s < 32; ++s) x[s] = lt < 32 ? v0[s] : v1[s];
+#pragma unroll
+                    for (int lv = 0; lv < 5; ++lv) {
+                        const bool hi = (lane >> lv) & 1;
+#pragma unroll
+                        for (int j = 0; j < (16 >> lv); ++j) x[j] = hi ? x[2 * j + 1] : x[2 * j];
+                    }
+                    const float z = sm[SM_RZ + pb * 64 + lt] + __uint_as_float(x[0]);
+                    row[lt] = z;
+                    sm[SM_INVD + lt] = 1.0f / z;
                 } else {
                     const int t = lt - 64;
 #pragma unroll
@@ -665,17 +694,26 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             }
             tc_fence_before();
             named_bar(kBarWG2, 128);
-            // ---- T = (I + L)^{-1}; each finished block also goes to the bf16 tile T [t][s]
+            // ---- T = M^{-1}; each finished block also goes to the bf16 tile T [t][s]
             //      (its blocks above the diagonal stay zero from the start)
             unsigned char* tt = base + OFF_TT;
             if (lt < 64) {  // 16x16 diagonal blocks: right-looking substitution, one column per thread
                 const int blk = lt >> 4, c = lt & 15, o = 16 * blk;
-                float acc[16];
+                float acc[16], inv[16];
+#pragma unroll
+                for (int r4 = 0; r4 < 4; ++r4) {
+                    const float4 d4 = *reinterpret_cast<const float4*>(sm + SM_INVD + o + 4 * r4);
+                    inv[4 * r4 + 0] = d4.x;
+                    inv[4 * r4 + 1] = d4.y;
+                    inv[4 * r4 + 2] = d4.z;
+                    inv[4 * r4 + 3] = d4.w;
+                }
 #pragma unroll
                 for (int r = 0; r < 16; ++r) acc[r] = (r == c) ? 1.0f : 0.0f;
 #pragma unroll
                 for (int s = 0; s < 16; ++s) {
-                    const float xs = acc[s];
+                    const float xs = acc[s] * inv[s];
+                    acc[s] = xs;
 #pragma unroll
                     for (int r = s + 1; r < 16; ++r) acc[r] = fmaf(-LF[(o + r) * kLDF + o + s], xs, acc[r]);
                 }
@@ -689,7 +727,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             }
             named_bar(kBarWG2, 128);
             const int g8 = lane >> 2, q4 = lane & 3;
-            if (lw < 2) {  // 16 -> 32 merges: T_ij = -D_i (L_ij D_j), (i, j) = (1, 0), (3, 2)
+            if (lw < 2) {  // 16 -> 32 merges: T_ij = -T_ii (M_ij T_jj), (i, j) = (1, 0), (3, 2)
                 const int i = 2 * lw + 1, j = 2 * lw;
                 float x[2][4];
                 mma_tile_16x16(x, LF + (16 * i) * kLDF + 16 * j, kLDF, TF + (16 * j) * kLDF + 16 * j, kLDF, 2);
@@ -701,7 +739,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 store_tile_bf16(x, tt, 16 * i, 16 * j, -1.0f, g8, q4);
             }
             named_bar(kBarWG2, 128);
-            {  // 32 -> 64: X = L[32:64, 0:32] T[0:32, 0:32]; T[32:64, 0:32] = -T[32:64, 32:64] X
+            {  // 32 -> 64: X = M[32:64, 0:32] T[0:32, 0:32]; T[32:64, 0:32] = -T[32:64, 32:64] X
                 const int mt = lw >> 1, nt0 = 2 * (lw & 1);
                 float x[2][4];
                 // T[0:16, 16:32] is zero: columns 16-31 take k-steps 2-3 only
@@ -713,71 +751,51 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 store_tile_bf16(x, tt, 32 + 16 * mt, 8 * nt0, -1.0f, g8, q4);
             }
             fence_proxy_async();
-            named_bar(kBarTReady, 256);   // -> warps 0-3 issue the W/U MMAs
+            named_bar(kBarTReady, 256);   // -> warps 0-3 issue the innovation MMAs
         } else if (wg0) {
-            // ---- outputs of the previous chunk, once the query MMA has read Q_bar
-            if (n > 0) {
-                wait_or_abort(bar_o, n & 1);
-                emit_outputs(n - 1);
+            // ---- -Z^T (the prediction S_m^T K_bar^T, negated) -> bf16 A operand in TMEM
+            {
+                wait_or_abort(bar_o, pb);
+                tc_fence_after();
+                uint32_t v0[32], v1[32], pk[32];
+                tmem_ld64(TM_ZD, v0, v1);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    pk[e] = pack_bf16(-__uint_as_float(v0[2 * e]), -__uint_as_float(v0[2 * e + 1]));
+                    pk[16 + e] = pack_bf16(-__uint_as_float(v1[2 * e]), -__uint_as_float(v1[2 * e + 1]));
+                }
+                tmem_st32(lane_base + TM_DB, pk);
+                tmem_wait_st();
             }
-            // ---- W^T = K_bar^T T^T, U^T = V^T T^T
+            tc_fence_before();
+            // ---- Delta'^T = (V^T - Z^T) T^T = V^T T^T + (-Z^T) T^T
             named_bar(kBarTReady, 256);
             if (tid == 0 && !*s_abort) {
                 wait_or_abort(bar_v, ph_v);
                 tc_fence_after();
-                const uint32_t id = idesc_bf16(128, 64, 1, 0, 0);
+                const uint32_t id_v = idesc_bf16(128, 64, 1, 0, 0), id_z = idesc_bf16(128, 64, 0, 0, 0);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t bd = sw128_desc(sb + OFF_TT + ks * 32, 16, 1024);
-                    mma_bf16(tmem + TM_GW, sw128_desc(sb + OFF_KQ + ks * 2048, 16384, 1024), bd, id, ks > 0);
-                    mma_bf16(tmem + TM_D, sw128_desc(sb + OFF_VIN + ks * 2048, 8192, 1024), bd, id, ks > 0);
-                }
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem + TM_ZD, sw128_desc(sb + OFF_VIN + ks * 2048, 8192, 1024),
+                             sw128_desc(sb + OFF_TT + ks * 32, 16, 1024), id_v, ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16_tmem_a(tmem + TM_ZD, tmem + TM_DB + 8 * ks, sw128_desc(sb + OFF_TT + ks * 32, 16, 1024),
+                                    id_z, 1u);
                 mma_commit(bar_mma);
                 ++n_mma_issued;
             }
             ph_v ^= 1u;
-            // ---- -W^T rows -> bf16 [i][t] (MN-major B operand of the innovations); prefetch the next v
+            // ---- Delta'^T -> bf16 in TMEM (A operand); prefetch the next v
             {
-                wait_or_abort(bar_mma, kParWU);
+                wait_or_abort(bar_mma, pb ^ 1u);
                 tc_fence_after();
                 if (tid == 0 && n + 1 < nchunks && !*s_abort) {
-                    issue_v(n + 1);   // the W/U MMAs that read v have completed
+                    issue_v(n + 1);   // the innovation MMAs that read v have completed
                     ++n_v_issued;
                 }
-                uint32_t v0[32], v1[32];
-                tmem_ld64(TM_GW, v0, v1);
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int t = 8 * ch + 2 * e;
-                        pk[e] = pack_bf16(-__uint_as_float(t < 32 ? v0[t] : v1[t - 32]),
-                                          -__uint_as_float(t + 1 < 32 ? v0[t + 1] : v1[t + 1 - 32]));
-                    }
-                    *reinterpret_cast<uint4*>(base + OFF_W + sw128_off(tid, ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
-            }
-            fence_proxy_async();
-            tc_fence_before();
-            named_bar(kBarWG0, 128);
-            // ---- Delta^T = U^T + S_m^T (-W^T)
-            if (tid == 0 && !*s_abort) {
-                tc_fence_after();
-                const uint32_t id_d = idesc_bf16(128, 64, 0, 1, 0);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_tmem_a(tmem + TM_D, tmem + TM_SMB + 8 * ks, sw128_desc(sb + OFF_W + ks * 2048, 16, 1024),
-                                    id_d, 1u);
-                mma_commit(bar_mma);
-                ++n_mma_issued;
-            }
-            // ---- Delta^T -> bf16 in TMEM (A operand)
-            {
-                wait_or_abort(bar_mma, kParInno);
-                tc_fence_after();
                 uint32_t v0[32], v1[32], pk[32];
-                tmem_ld64(TM_D, v0, v1);
+                tmem_ld64(TM_ZD, v0, v1);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     pk[e] = pack_bf16(__uint_as_float(v0[2 * e]), __uint_as_float(v0[2 * e + 1]));
@@ -788,7 +806,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             }
             tc_fence_before();
             named_bar(kBarWG0, 128);
-            // ---- O^T += Delta^T A^T ; S^T += Delta^T K_til
+            // ---- O^T += Delta'^T A'^T ; S^T += Delta'^T K_til'
             if (tid == 0 && !*s_abort) {
                 tc_fence_after();
                 const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
@@ -796,13 +814,12 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint32_t a = tmem + TM_DB + 8 * ks;
-                    mma_bf16_tmem_a(tmem + TM_O + 64 * (n & 1), a, sw128_desc(sb + OFF_AQ + ks * 32, 16, 1024), id_o, 1u);
+                    mma_bf16_tmem_a(tmem + TM_O, a, sw128_desc(sb + OFF_AQ + ks * 32, 16, 1024), id_o, 1u);
                     mma_bf16_tmem_a(tmem + TM_S, a, sw128_desc(sb + OFF_KT + ks * 2048, 8192, 1024), id_s, 1u);
                 }
                 mma_commit(bar_mma);
                 ++n_mma_issued;
             }
-            if (tid == 0) bulk_wait_read();   // the o tile has left the operand buffer
         } else if (n + 1 < nchunks) {
             // ---- warps 4-7: gains of chunk n + 1
             prep_gains(n + 1);
@@ -815,7 +832,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 
     const bool aborted = *s_abort != 0;
     if (!aborted && nchunks > 0) {
-        wait_or_abort(bar_mma, kParUpd);   // update of the last chunk has landed
+        wait_or_abort(bar_mma, static_cast<uint32_t>(nchunks - 1) & 1u);   // update of the last chunk has landed
         if (wg0) emit_outputs(nchunks - 1);
     }
     if (tid == 0) bulk_wait_all();
@@ -837,7 +854,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 }
             }
         } else if (wg1) {
-            if (!ISO) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = p_reg;
+            if (!ISO) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = pn / pd;
             else if (tid == 128) P.p_T[bh] = b_iso;
         }
     } else {
