@@ -11,9 +11,10 @@
 //       inclusive scan over the chunk's tokens, then replayed from the carry.
 //       The decay factors relative to the chunk's per-channel reference
 //       G_ref = G_C / 2 (App. D: decay ratios from differences of cumulative
-//       log-decay) are running products e1_t = e^{G_t - G_ref}, e2_t = 1 / e1_t.
+//       log-decay) are running products e1_t = e^{G_t - G_ref}; their
+//       reciprocals e2 = 1 / e1 are taken in the operand pass.
 //   A2  decayed operands (bf16, 128-byte-swizzled, tensor-core layouts):
-//         K_bar = k e1, Q_bar = q e1, K_til' = p_hat k e2  (the isotropic
+//         K_bar = k e1, Q_bar = q e1, K_til' = p_hat k / e1  (the isotropic
 //       variant uses its scalar b_hat in place of p_hat).
 //   B   Gram MMA  [K_bar; Q_bar] K_til'^T  (M = 128: rows 0-63 give the key
 //       block, rows 64-127 the query-write matrix A', diagonal kept), and the
@@ -31,7 +32,7 @@
 //   J   O^T += Delta'^T A'^T ; S^T += Delta'^T K_til'  (Delta'^T in bf16 in TMEM
 //       as the A operand; the state stays in TMEM, the pending factor
 //       e^{G_C - G_ref} is folded into the next chunk's scaling).
-//   K   o = O (bf16) to global memory by TMA at the start of the next chunk.
+//   K   o = O (bf16) to global memory at the start of the next chunk.
 // Schedule per chunk n: warps 0-3 store the outputs of chunk n-1 and move the
 // state into the chunk's frame while warps 4-11 build the operands; one thread
 // issues the Gram and prediction/query MMAs, another prefetches chunk n+1; then
@@ -67,7 +68,7 @@ constexpr int kD = 128;    // d_k = d_v
 // triangular system.  Operands are built by warps 4-11.
 constexpr int kNT = 384;
 // named barriers
-constexpr int kBarWG1 = 1, kBarWG0 = 2, kBarTReady = 3, kBarWG2 = 6;
+constexpr int kBarWG1 = 1, kBarWG0 = 2, kBarTReady = 3, kBarOps = 5, kBarWG2 = 6;
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -77,12 +78,11 @@ constexpr uint32_t OFF_QIN = 0;        // q tile, 2 TMA boxes of [64 t][64 d] bf
 constexpr uint32_t OFF_KIN = 16384;    // k tile
 constexpr uint32_t OFF_VIN = 32768;    // v tile (MN-major A operand of U^T)
 constexpr uint32_t OFF_LA = 49152;     // log_alpha [64][128] fp32 -> e1 in place
-constexpr uint32_t OFF_OM = 81920;     // omega [64][128] fp32 -> p_hat e2 (diagonal) / e2 (isotropic)
+constexpr uint32_t OFF_OM = 81920;     // omega [64][128] fp32 -> p_hat in place (diagonal)
 constexpr uint32_t OFF_KQ = 114688;    // [K_bar; Q_bar] 128 rows x 128, two 16 KB K-atoms
 constexpr uint32_t OFF_KT = 147456;    // K_til' [64 s][128 i], two 8 KB K-atoms
 constexpr uint32_t OFF_AQ = 163840;    // A [64 t][64 s] bf16
-constexpr uint32_t OFF_LF = 172032;    // L fp32 [64][kLDF]; before that (step 1) the o tile of the
-                                       //   previous chunk, two [64 t][64 j] bf16 tiles for TMA stores
+constexpr uint32_t OFF_LF = 172032;    // M fp32 [64][kLDF]
 constexpr uint32_t OFF_TT = 189440;    // T [64 t][64 s] bf16
 constexpr uint32_t OFF_TF = 197632;    // T fp32 [64][kLDF]
 constexpr uint32_t OFF_XT = 215040;    // merge temporaries fp32 [32][kLDX]
@@ -108,7 +108,7 @@ static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
 constexpr uint32_t TM_S = 0, TM_ZD = 128, TM_O = 192, TM_G = 256, TM_SMB = 320, TM_DB = 384, TM_COLS = 512;
 
 struct TcParams {
-    CUtensorMap tq, tk, tv, tla, tom, to;
+    CUtensorMap tq, tk, tv, tla, tom;
     const float* r;
     const float* om_iso;
     const float* S0;
@@ -236,8 +236,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     const uint32_t sb = smem_addr(base);
     float* sm = reinterpret_cast<float*>(base + OFF_SMALL);
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SM_FLAG);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + OFF_BAR + 32);
-    const uint32_t bar_in = sb + OFF_BAR, bar_v = bar_in + 8, bar_mma = bar_in + 16, bar_o = bar_in + 24;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + OFF_BAR + 48);
+    const uint32_t bar_in = sb + OFF_BAR, bar_v = bar_in + 8, bar_mma = bar_in + 16, bar_o = bar_in + 24,
+                   bar_oj = bar_in + 32, bar_ops = bar_in + 40;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool wg0 = tid < 128, wg1 = tid >= 128 && tid < 256, wg2 = tid >= 256;
@@ -249,6 +250,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         mbar_init(bar_v, 1);
         mbar_init(bar_mma, 1);
         mbar_init(bar_o, 1);
+        mbar_init(bar_oj, 1);
+        mbar_init(bar_ops, 1);
         mbar_fence_init();
         *s_abort = 0;
     }
@@ -273,13 +276,14 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         tma_load_4d(sb + OFF_VIN + 8192, &P.tv, 64, h, n * kC, b, bar_v);
     };
     __syncthreads();
-    // copies and MMAs issued so far (thread 0: v, MMAs; thread 128: q, k, log_alpha, omega)
-    int n_in_issued = 0, n_v_issued = 0, n_mma_issued = 0, n_o_issued = 0;
+    // copies and MMA commits issued so far (thread 0: v, MMAs; thread 128: the Gram MMAs;
+    // thread 160: q, k, log_alpha, omega)
+    int n_in_issued = 0, n_v_issued = 0, n_mma_issued = 0, n_o_issued = 0, n_oj_issued = 0, n_gram_issued = 0;
     if (tid == 0 && nchunks > 0) {
         issue_v(0);
         n_v_issued = 1;
     }
-    if (tid == 128 && nchunks > 0) {
+    if (tid == 160 && nchunks > 0) {
         issue_inputs(0);
         n_in_issued = 1;
     }
@@ -319,9 +323,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     tc_fence_after();
 
     uint32_t ph_in = 0, ph_v = 0;
-    // bar_mma completes three phases per chunk n: Gram (parity n & 1), innovations
-    // ((n + 1) & 1), update (n & 1).  bar_o completes once per chunk (query and
-    // prediction MMA), parity n & 1.
+    // bar_mma completes three phases per chunk n: Gram (parity n & 1, committed by
+    // thread 128), innovations ((n + 1) & 1), state update (n & 1).  bar_o (prediction
+    // and query MMA), bar_oj (output update) and bar_ops (operands built, an arrive by
+    // thread 128) complete once per chunk, parity n & 1.
     auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
         if (*s_abort) return;
         if (!mbar_wait(bar, parity, kWaitLimit)) {
@@ -346,7 +351,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     // uncertainty recurrence and the decay factors, written over the inputs in place.
     // Runs one chunk ahead of the memory pass.  Rows past the end of the sequence
     // arrive as zeros (TMA fill): log_alpha = omega = k = 0 leaves the variance and
-    // the decay factors unchanged and zeroes those rows' operands.
+    // the decay factor unchanged and zeroes those rows' operands.
     auto prep_gains = [&](int c) {
         const int t0c = c * kC, nvc = min(kC, T - t0c);
         if (tid < 128 + kC) {
@@ -380,13 +385,15 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         sm[SM_CF + (c & 1) * 128 + i] = ex2(pend2 + R2);
         pend2 = kLog2e * GC - R2;
         sm[SM_FOUT + i] = ex2(pend2);
-        float e1 = ex2(-R2), e2 = ex2(R2);
+        float e1 = ex2(-R2);
         const unsigned char* kin = base + OFF_KIN + (i >> 6) * 8192 + (i & 7) * 2;
         const int kch = (i & 63) >> 3;
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
             float w[32], w2[32];
-#pragma unroll
+            // (one 16-token body for the diagonal variant keeps the code small; the
+            //  isotropic variant keeps both bodies for its per-half reductions)
+#pragma unroll (ISO ? 2 : 1)
             for (int qt = 0; qt < 2; ++qt) {
                 const int tb = hf * 32 + qt * 16;
                 // loads first (independent of the carry) ...
@@ -414,15 +421,14 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 for (int u = 0; u < 16; ++u) {
                     const int t = tb + u;
                     const float l2 = la[u] * kLog2e;
-                    const float al = ex2(l2), ial = ex2(-l2), a2 = al * al, k2 = kv[u] * kv[u];
+                    const float al = ex2(l2), a2 = al * al, k2 = kv[u] * kv[u];
                     e1 *= al;
-                    e2 *= ial;
                     LA[t * kD + i] = e1;
                     if (!ISO) {
                         const float c = mr[u] * k2, rd = rcp_approx(pd);
                         const float n1 = fmaf(a2, pn, om[u] * pd);
                         const float d1 = fmaf(c * a2, pn, fmaf(c, om[u], 1.0f) * pd);
-                        OM[t * kD + i] = (n1 * rd) * e2;
+                        OM[t * kD + i] = n1 * rd;   // p_hat_t
                         pn = n1;
                         pd = d1;
                         if ((u & 3) == 3) {   // exact rescale: pd back to [1, 2)
@@ -432,7 +438,6 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                             pd *= sc;
                         }
                     } else {
-                        OM[t * kD + i] = e2;
                         w[qt * 16 + u] = k2;
                         w2[qt * 16 + u] = t < nvc ? a2 : 0.0f;
                     }
@@ -500,23 +505,23 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     };
 
     // ------------------------------------------------------------------ warps 0-3
-    // Outputs of a finished chunk: O^T rows out of TMEM, staged as two [64 t][64 j]
-    // tiles over the L region (free until the Gram readout), two TMA stores (rows
-    // past T are clipped).
+    // Outputs of a finished chunk: thread j holds column j of the [64 t][128 j] tile
+    // (its O^T row in TMEM) and stores it directly; a warp writes 64 contiguous bytes
+    // per token.  Rows past T are skipped.
     auto emit_outputs = [&](int c) {
         uint32_t v0[32], v1[32];
         tc_fence_after();
         tmem_ld64(TM_O, v0, v1);
-        __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(base + OFF_LF + (tid >> 6) * 8192) + (tid & 63);
+        const int t0c = c * kC, nvc = min(kC, T - t0c);
+        __nv_bfloat16* og = P.o + (static_cast<size_t>(b) * T + t0c) * H * kD + static_cast<size_t>(h) * kD + tid;
+        const size_t ts = static_cast<size_t>(H) * kD;
+        if (nvc == kC) {
 #pragma unroll
-        for (int t = 0; t < kC; ++t)
-            ost[t * 64] = __float2bfloat16_rn(__uint_as_float(t < 32 ? v0[t] : v1[t - 32]));
-        fence_proxy_async();
-        named_bar(kBarWG0, 128);
-        if (tid == 0 && !*s_abort) {
-            tma_store_4d(&P.to, sb + OFF_LF, 0, h, c * kC, b);
-            tma_store_4d(&P.to, sb + OFF_LF + 8192, 64, h, c * kC, b);
-            bulk_commit();
+            for (int t = 0; t < kC; ++t) og[t * ts] = __float2bfloat16_rn(__uint_as_float(t < 32 ? v0[t] : v1[t - 32]));
+        } else {
+#pragma unroll
+            for (int t = 0; t < kC; ++t)
+                if (t < nvc) og[t * ts] = __float2bfloat16_rn(__uint_as_float(t < 32 ? v0[t] : v1[t - 32]));
         }
     };
     // State of chunk c into its reference frame: S_m^T = S^T diag(cf) in TMEM, and
@@ -561,16 +566,33 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     for (int n = 0; n < nchunks; ++n) {
         const int t0 = n * kC, nv = min(kC, T - t0);
         const uint32_t pb = static_cast<uint32_t>(n) & 1u;
-        // ================= step 1: outputs of chunk n-1, state frame || operands
-        if (n > 0) wait_or_abort(bar_mma, pb ^ 1u);   // update of chunk n-1 has landed
+        // ================= step 1: state frame, outputs of chunk n-1, prediction/query MMA
+        //                   || operands, Gram MMA, prefetch of chunk n+1
         if (wg0) {
-            if (n > 0) emit_outputs(n - 1);
             scale_state(n);
-            if (tid == 0) bulk_wait_read();   // the o tile has left the L region
+            if (n > 0) {
+                wait_or_abort(bar_oj, pb ^ 1u);   // output update of chunk n-1 has landed
+                emit_outputs(n - 1);
+            }
+            tc_fence_before();
+            named_bar(kBarWG0, 128);
+            // [Z^T | O^T] = S_m^T [K_bar; Q_bar]^T  (N = 128: prediction and query together)
+            if (tid == 0 && !*s_abort) {
+                wait_or_abort(bar_ops, pb);   // operands built (warps 4-11)
+                tc_fence_after();
+                const uint32_t id_zo = idesc_bf16(128, 128, 0, 0, 0);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_tmem_a(tmem + TM_ZD, tmem + TM_SMB + 8 * ks,
+                                    sw128_desc(sb + OFF_KQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_zo,
+                                    ks > 0);
+                mma_commit(bar_o);
+                ++n_o_issued;
+            }
         } else {
             // decayed bf16 operands (warps 4-11): thread -> 4 channels in each K-atom
             // (8-byte pieces of the swizzled rows), 16 threads (half a warp) per token row.
-            // K_til' = p_hat k e2 (isotropic: b_hat k e2); the gain denominator enters
+            // K_til' = p_hat k / e1 (isotropic: b_hat k / e1); the gain denominator enters
             // through the diagonal of the triangular system.
             const int u = tid - 128, g = u & 15, tr = u >> 4;
 #pragma unroll 2
@@ -584,7 +606,12 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     const uint2 kr = *reinterpret_cast<const uint2*>(base + OFF_KIN + a * 8192 + sw);
                     const uint2 qr = *reinterpret_cast<const uint2*>(base + OFF_QIN + a * 8192 + sw);
                     const float4 e = *reinterpret_cast<const float4*>(LA + t * kD + 64 * a + 4 * g);
-                    const float4 kp = *reinterpret_cast<const float4*>(OM + t * kD + 64 * a + 4 * g);
+                    float4 kp = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+                    if (!ISO) kp = *reinterpret_cast<const float4*>(OM + t * kD + 64 * a + 4 * g);
+                    kp.x *= rcp_approx(e.x);
+                    kp.y *= rcp_approx(e.y);
+                    kp.z *= rcp_approx(e.z);
+                    kp.w *= rcp_approx(e.w);
                     const float k0 = bf_lo(kr.x), k1 = bf_hi(kr.x), k2 = bf_lo(kr.y), k3 = bf_hi(kr.y);
                     kb[4 * a + 0] = k0 * e.x;
                     kb[4 * a + 1] = k1 * e.y;
@@ -610,36 +637,27 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                                    pack_bf16(kt[4 * a + 2] * sc, kt[4 * a + 3] * sc));
                 }
             }
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        if (*s_abort) break;
-        // ================= step 2: Gram and prediction/query MMAs (thread 0), prefetch of the next inputs (thread 128)
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
+            fence_proxy_async();
+            tc_fence_before();
+            named_bar(kBarOps, 256);
+            // Gram MMA (thread 128) and the next inputs (thread 160)
+            if (tid == 128 && !*s_abort) {
+                tc_fence_after();
+                const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t ad = sw128_desc(sb + OFF_KQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                const uint64_t bd = sw128_desc(sb + OFF_KT + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-                mma_bf16(tmem + TM_G, ad, bd, id, ks > 0);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t ad = sw128_desc(sb + OFF_KQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                    const uint64_t bd = sw128_desc(sb + OFF_KT + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+                    mma_bf16(tmem + TM_G, ad, bd, id, ks > 0);
+                }
+                mma_commit(bar_mma);
+                ++n_gram_issued;
+                mbar_arrive(bar_ops);
             }
-            mma_commit(bar_mma);
-            ++n_mma_issued;
-            // [Z^T | O^T] = S_m^T [K_bar; Q_bar]^T  (N = 128: prediction and query together)
-            const uint32_t id_zo = idesc_bf16(128, 128, 0, 0, 0);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                mma_bf16_tmem_a(tmem + TM_ZD, tmem + TM_SMB + 8 * ks,
-                                sw128_desc(sb + OFF_KQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_zo,
-                                ks > 0);
-            mma_commit(bar_o);
-            ++n_o_issued;
-        }
-        if (tid == 128 && n + 1 < nchunks) {   // the operand pass has consumed the inputs
-            issue_inputs(n + 1);
-            ++n_in_issued;
+            if (tid == 160 && !*s_abort && n + 1 < nchunks) {   // the operand pass has consumed the inputs
+                issue_inputs(n + 1);
+                ++n_in_issued;
+            }
         }
         // ================= step 3
         if (wg2) {
@@ -647,6 +665,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             const int lt = tid - 256, lw = warp - 8;
             {
                 wait_or_abort(bar_mma, pb);
+                if (n > 0) wait_or_abort(bar_oj, pb ^ 1u);   // A' of chunk n-1 has been read
                 tc_fence_after();
                 uint32_t v0[32], v1[32];
                 tmem_ld64(TM_G, v0, v1);
@@ -711,11 +730,23 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 #pragma unroll
                 for (int r = 0; r < 16; ++r) acc[r] = (r == c) ? 1.0f : 0.0f;
 #pragma unroll
-                for (int s = 0; s < 16; ++s) {
-                    const float xs = acc[s] * inv[s];
-                    acc[s] = xs;
+                for (int s4 = 0; s4 < 16; s4 += 4) {
+                    // columns s4..s4+3 of the rows below, one 16-byte load per row
+                    float4 lq[16];
 #pragma unroll
-                    for (int r = s + 1; r < 16; ++r) acc[r] = fmaf(-LF[(o + r) * kLDF + o + s], xs, acc[r]);
+                    for (int r = s4 + 1; r < 16; ++r)
+                        lq[r] = *reinterpret_cast<const float4*>(LF + (o + r) * kLDF + o + s4);
+#pragma unroll
+                    for (int s = s4; s < s4 + 4; ++s) {
+                        const float xs = acc[s] * inv[s];
+                        acc[s] = xs;
+#pragma unroll
+                        for (int r = s + 1; r < 16; ++r) {
+                            const float4 q = lq[r];
+                            const float l = (s & 3) == 0 ? q.x : (s & 3) == 1 ? q.y : (s & 3) == 2 ? q.z : q.w;
+                            acc[r] = fmaf(-l, xs, acc[r]);
+                        }
+                    }
                 }
                 __nv_bfloat16* tcol = reinterpret_cast<__nv_bfloat16*>(tt + ((o + c) & 7) * 2);
 #pragma unroll
@@ -753,47 +784,52 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             fence_proxy_async();
             named_bar(kBarTReady, 256);   // -> warps 0-3 issue the innovation MMAs
         } else if (wg0) {
-            // ---- -Z^T (the prediction S_m^T K_bar^T, negated) -> bf16 A operand in TMEM
+            // ---- Y^T = V^T - Z^T (innovation before the triangular solve; Z^T = S_m^T K_bar^T
+            //      is the prediction) -> bf16 A operand in TMEM
             {
                 wait_or_abort(bar_o, pb);
+                wait_or_abort(bar_v, ph_v);
                 tc_fence_after();
                 uint32_t v0[32], v1[32], pk[32];
                 tmem_ld64(TM_ZD, v0, v1);
+                // column j = tid of the v tile (two [64 t][64 j] swizzled boxes)
+                const unsigned char* vcol = base + OFF_VIN + (tid >> 6) * 8192 + (tid & 7) * 2;
+                const int jc = (tid & 63) >> 3;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    pk[e] = pack_bf16(-__uint_as_float(v0[2 * e]), -__uint_as_float(v0[2 * e + 1]));
-                    pk[16 + e] = pack_bf16(-__uint_as_float(v1[2 * e]), -__uint_as_float(v1[2 * e + 1]));
+                for (int e = 0; e < 32; ++e) {
+                    const int t = 2 * e;
+                    const float va = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + sw128_off(t, jc)));
+                    const float vb = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + sw128_off(t + 1, jc)));
+                    const float za = __uint_as_float(t < 32 ? v0[t] : v1[t - 32]);
+                    const float zb = __uint_as_float(t + 1 < 32 ? v0[t + 1] : v1[t + 1 - 32]);
+                    pk[e] = pack_bf16(va - za, vb - zb);
                 }
                 tmem_st32(lane_base + TM_DB, pk);
                 tmem_wait_st();
             }
+            ph_v ^= 1u;
+            fence_proxy_async();   // v has been read: the next chunk's copy may overwrite it
             tc_fence_before();
-            // ---- Delta'^T = (V^T - Z^T) T^T = V^T T^T + (-Z^T) T^T
+            // ---- Delta'^T = Y^T T^T
             named_bar(kBarTReady, 256);
             if (tid == 0 && !*s_abort) {
-                wait_or_abort(bar_v, ph_v);
                 tc_fence_after();
-                const uint32_t id_v = idesc_bf16(128, 64, 1, 0, 0), id_z = idesc_bf16(128, 64, 0, 0, 0);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + TM_ZD, sw128_desc(sb + OFF_VIN + ks * 2048, 8192, 1024),
-                             sw128_desc(sb + OFF_TT + ks * 32, 16, 1024), id_v, ks > 0);
+                const uint32_t id_y = idesc_bf16(128, 64, 0, 0, 0);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16_tmem_a(tmem + TM_ZD, tmem + TM_DB + 8 * ks, sw128_desc(sb + OFF_TT + ks * 32, 16, 1024),
-                                    id_z, 1u);
+                                    id_y, ks > 0);
                 mma_commit(bar_mma);
                 ++n_mma_issued;
+                if (n + 1 < nchunks) {
+                    issue_v(n + 1);
+                    ++n_v_issued;
+                }
             }
-            ph_v ^= 1u;
-            // ---- Delta'^T -> bf16 in TMEM (A operand); prefetch the next v
+            // ---- Delta'^T -> bf16 in TMEM (A operand)
             {
                 wait_or_abort(bar_mma, pb ^ 1u);
                 tc_fence_after();
-                if (tid == 0 && n + 1 < nchunks && !*s_abort) {
-                    issue_v(n + 1);   // the innovation MMAs that read v have completed
-                    ++n_v_issued;
-                }
                 uint32_t v0[32], v1[32], pk[32];
                 tmem_ld64(TM_ZD, v0, v1);
 #pragma unroll
@@ -806,25 +842,32 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             }
             tc_fence_before();
             named_bar(kBarWG0, 128);
-            // ---- O^T += Delta'^T A'^T ; S^T += Delta'^T K_til'
+            // ---- S^T += Delta'^T K_til' (committed first: the next chunk starts from it);
+            //      O^T += Delta'^T A'^T
             if (tid == 0 && !*s_abort) {
                 tc_fence_after();
                 const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
                 const uint32_t id_s = idesc_bf16(128, 128, 0, 1, 0);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t a = tmem + TM_DB + 8 * ks;
-                    mma_bf16_tmem_a(tmem + TM_O, a, sw128_desc(sb + OFF_AQ + ks * 32, 16, 1024), id_o, 1u);
-                    mma_bf16_tmem_a(tmem + TM_S, a, sw128_desc(sb + OFF_KT + ks * 2048, 8192, 1024), id_s, 1u);
-                }
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16_tmem_a(tmem + TM_S, tmem + TM_DB + 8 * ks, sw128_desc(sb + OFF_KT + ks * 2048, 8192, 1024),
+                                    id_s, 1u);
                 mma_commit(bar_mma);
                 ++n_mma_issued;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16_tmem_a(tmem + TM_O, tmem + TM_DB + 8 * ks, sw128_desc(sb + OFF_AQ + ks * 32, 16, 1024),
+                                    id_o, 1u);
+                mma_commit(bar_oj);
+                ++n_oj_issued;
             }
         } else if (n + 1 < nchunks) {
             // ---- warps 4-7: gains of chunk n + 1
             prep_gains(n + 1);
         }
         if (n + 1 < nchunks) ph_in ^= 1u;
+        // the next chunk starts from the updated state (and overwrites K_til')
+        if (wg0) wait_or_abort(bar_mma, pb);
         tc_fence_before();
         __syncthreads();
         if (*s_abort) break;
@@ -833,9 +876,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     const bool aborted = *s_abort != 0;
     if (!aborted && nchunks > 0) {
         wait_or_abort(bar_mma, static_cast<uint32_t>(nchunks - 1) & 1u);   // update of the last chunk has landed
+        wait_or_abort(bar_oj, static_cast<uint32_t>(nchunks - 1) & 1u);
         if (wg0) emit_outputs(nchunks - 1);
     }
-    if (tid == 0) bulk_wait_all();
     if (!*s_abort) {
         // final state: S_T = (TMEM state) scaled by the last chunk's pending factor
         if (wg0) {
@@ -857,14 +900,21 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             if (!ISO) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = pn / pd;
             else if (tid == 128) P.p_T[bh] = b_iso;
         }
-    } else {
+    }
+    int* s_ngram = reinterpret_cast<int*>(sm + SM_FLAG + 1);
+    if (tid == 128) *s_ngram = n_gram_issued;
+    tc_fence_before();
+    __syncthreads();
+    if (*s_abort) {
         // let copies and MMAs already issued land before the CTA's resources go away
         if (tid == 0) {
-            if (n_mma_issued > 0) mbar_wait(bar_mma, (n_mma_issued - 1) & 1, kWaitLimit);
+            const int nm = n_mma_issued + *s_ngram;
+            if (nm > 0) mbar_wait(bar_mma, (nm - 1) & 1, kWaitLimit);
             if (n_o_issued > 0) mbar_wait(bar_o, (n_o_issued - 1) & 1, kWaitLimit);
+            if (n_oj_issued > 0) mbar_wait(bar_oj, (n_oj_issued - 1) & 1, kWaitLimit);
             if (n_v_issued > 0) mbar_wait(bar_v, (n_v_issued - 1) & 1, kWaitLimit);
         }
-        if (tid == 128 && n_in_issued > 0) mbar_wait(bar_in, (n_in_issued - 1) & 1, kWaitLimit);
+        if (tid == 160 && n_in_issued > 0) mbar_wait(bar_in, (n_in_issued - 1) & 1, kWaitLimit);
     }
     tc_fence_before();
     __syncthreads();
@@ -926,7 +976,6 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t s) {
               encode_4d(&P.tla, a.log_alpha, F32, 4, a.B, a.T, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (ok && a.variant == 0)
         ok = encode_4d(&P.tom, a.omega, F32, 4, a.B, a.T, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (ok) ok = encode_4d(&P.to, a.o, BF, 2, a.B, a.T, a.H, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return cudaErrorInvalidValue;
     P.r = a.r;
     P.om_iso = a.variant == 1 ? a.omega : nullptr;
