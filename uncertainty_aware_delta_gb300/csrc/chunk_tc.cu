@@ -223,6 +223,23 @@ __device__ __forceinline__ float rcp_approx(float x) {   // 1 / x, hardware appr
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// Packed fp32 pair arithmetic (two lanes per instruction).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{ .reg .b64 ra, rb, rc, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5}; mov.b64 rc, {%6, %7};"
+        " fma.rn.f32x2 rd, ra, rb, rc; mov.b64 {%0, %1}, rd; }"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{ .reg .b64 ra, rb, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5}; mul.rn.f32x2 rd, ra, rb;"
+        " mov.b64 {%0, %1}, rd; }"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
 __device__ __forceinline__ float ex2(float x) {   // 2^x, hardware approximation
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -417,27 +434,49 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 // p -> a^2 p + omega -> p_hat / (1 + c p_hat), c = mu k^2 / r, is the
                 // Moebius matrix [[a^2, omega], [c a^2, 1 + c omega]] acting on (pn, pd):
                 // two independent multiply-adds per token, p_hat_t = pn_t / pd_{t-1}.
+                // Token-local factors are formed two tokens at a time (packed fp32 pairs).
+                if (!ISO) {
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int t = tb + u;
-                    const float l2 = la[u] * kLog2e;
-                    const float al = ex2(l2), a2 = al * al, k2 = kv[u] * kv[u];
-                    e1 *= al;
-                    LA[t * kD + i] = e1;
-                    if (!ISO) {
-                        const float c = mr[u] * k2, rd = rcp_approx(pd);
-                        const float n1 = fmaf(a2, pn, om[u] * pd);
-                        const float d1 = fmaf(c * a2, pn, fmaf(c, om[u], 1.0f) * pd);
-                        OM[t * kD + i] = n1 * rd;   // p_hat_t
-                        pn = n1;
-                        pd = d1;
-                        if ((u & 3) == 3) {   // exact rescale: pd back to [1, 2)
+                    for (int u = 0; u < 16; u += 2) {
+                        const int t = tb + u;
+                        const float2 l2 = fmul2(make_float2(la[u], la[u + 1]), make_float2(kLog2e, kLog2e));
+                        const float al0 = ex2(l2.x), al1 = ex2(l2.y);
+                        const float2 a2 = fmul2(make_float2(al0, al1), make_float2(al0, al1));
+                        const float2 kk = make_float2(kv[u], kv[u + 1]);
+                        const float2 cc = fmul2(make_float2(mr[u], mr[u + 1]), fmul2(kk, kk));
+                        const float2 ca2 = fmul2(cc, a2);
+                        const float2 ee = ffma2(cc, make_float2(om[u], om[u + 1]), make_float2(1.0f, 1.0f));
+                        e1 *= al0;
+                        LA[t * kD + i] = e1;
+                        float rd = rcp_approx(pd);
+                        float2 nd = ffma2(make_float2(a2.x, ca2.x), make_float2(pn, pn),
+                                          fmul2(make_float2(om[u], ee.x), make_float2(pd, pd)));
+                        OM[t * kD + i] = nd.x * rd;   // p_hat_t
+                        pn = nd.x;
+                        pd = nd.y;
+                        e1 *= al1;
+                        LA[(t + 1) * kD + i] = e1;
+                        rd = rcp_approx(pd);
+                        nd = ffma2(make_float2(a2.y, ca2.y), make_float2(pn, pn),
+                                   fmul2(make_float2(om[u + 1], ee.y), make_float2(pd, pd)));
+                        OM[(t + 1) * kD + i] = nd.x * rd;
+                        pn = nd.x;
+                        pd = nd.y;
+                        if ((u & 3) == 2) {   // exact rescale: pd back to [1, 2)
                             const int ex = min((__float_as_int(pd) >> 23) & 0xff, 253);
                             const float sc = __int_as_float((254 - ex) << 23);
                             pn *= sc;
                             pd *= sc;
                         }
-                    } else {
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int t = tb + u;
+                        const float l2 = la[u] * kLog2e;
+                        const float al = ex2(l2), a2 = al * al, k2 = kv[u] * kv[u];
+                        e1 *= al;
+                        LA[t * kD + i] = e1;
                         w[qt * 16 + u] = k2;
                         w2[qt * 16 + u] = t < nvc ? a2 : 0.0f;
                     }
