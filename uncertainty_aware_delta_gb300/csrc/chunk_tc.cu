@@ -35,7 +35,8 @@
 //   K   o = O (bf16) to global memory at the start of the next chunk.
 // Schedule per chunk n: warps 0-3 store the outputs of chunk n-1 and move the
 // state into the chunk's frame while warps 4-11 build the operands; one thread
-// issues the Gram and prediction/query MMAs, another prefetches chunk n+1; then
+// issues the prediction/query MMAs, thread 256 the Gram MMA and thread 160 the
+// prefetch of chunk n+1; then
 // warps 8-11 read out the Gram matrix and invert the triangular system while
 // warps 0-3 convert the prediction and run H-J, and warps 4-7 compute the gains
 // of chunk n+1 (A1).
@@ -143,12 +144,14 @@ __device__ __forceinline__ Mob mob_mul(const Mob& x, const Mob& y) {  // x * y
     return {fmaf(x.a, y.a, x.b * y.c), fmaf(x.a, y.b, x.b * y.d), fmaf(x.c, y.a, x.d * y.c),
             fmaf(x.c, y.b, x.d * y.d)};
 }
-__device__ __forceinline__ void mob_renorm(Mob& m) {  // exact power-of-two rescale
+__device__ __forceinline__ void mob_renorm(Mob& m) {  // exact power-of-two rescale (entries >= 0)
     const float mx = fmaxf(fmaxf(m.a, m.b), fmaxf(m.c, m.d));
-    int e;
-    frexpf(mx, &e);
-    const float s = ldexpf(1.0f, -e);
-    m.a *= s; m.b *= s; m.c *= s; m.d *= s;
+    const int ex = min(max((__float_as_int(mx) >> 23) & 0xff, 1), 253);
+    const float s = __int_as_float((254 - ex) << 23);   // 2^(127 - ex): mx * s in [1, 2)
+    m.a *= s;
+    m.b *= s;
+    m.c *= s;
+    m.d *= s;
 }
 
 // ---- warp-level TF32 MMA helpers for the triangular inverse (fp32 row-major tiles in shared memory)
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         tma_load_4d(sb + OFF_VIN + 8192, &P.tv, 64, h, n * kC, b, bar_v);
     };
     __syncthreads();
-    // copies and MMA commits issued so far (thread 0: v, MMAs; thread 128: the Gram MMAs;
+    // copies and MMA commits issued so far (thread 0: v, MMAs; thread 256: the Gram MMAs;
     // thread 160: q, k, log_alpha, omega)
     int n_in_issued = 0, n_v_issued = 0, n_mma_issued = 0, n_o_issued = 0, n_oj_issued = 0, n_gram_issued = 0;
     if (tid == 0 && nchunks > 0) {
@@ -341,9 +344,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 
     uint32_t ph_in = 0, ph_v = 0;
     // bar_mma completes three phases per chunk n: Gram (parity n & 1, committed by
-    // thread 128), innovations ((n + 1) & 1), state update (n & 1).  bar_o (prediction
+    // thread 256), innovations ((n + 1) & 1), state update (n & 1).  bar_o (prediction
     // and query MMA), bar_oj (output update) and bar_ops (operands built, an arrive by
-    // thread 128) complete once per chunk, parity n & 1.
+    // thread 256) complete once per chunk, parity n & 1.
     auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
         if (*s_abort) return;
         if (!mbar_wait(bar, parity, kWaitLimit)) {
@@ -501,7 +504,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     aa[e] = asum * (1.0f / kD);
                     rr[e] = sm[SM_R + t];
                     oo[e] = sm[SM_OMI + t];
-                    uu[e] = P.mu * kk[e] / (kD * rr[e]);
+                    uu[e] = __fdividef(P.mu * kk[e], kD * rr[e]);
                     if (t < nvc)
                         m[e] = {aa[e], oo[e], uu[e] * aa[e], fmaf(uu[e], oo[e], 1.0f)};
                     else
@@ -527,14 +530,14 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 ex.c = __shfl_up_sync(0xffffffffu, pr.c, 1);
                 ex.d = __shfl_up_sync(0xffffffffu, pr.d, 1);
                 if (lane == 0) ex = {1.0f, 0.0f, 0.0f, 1.0f};
-                float bb = (ex.a * b_iso + ex.b) / (ex.c * b_iso + ex.d);
+                float bb = __fdividef(fmaf(ex.a, b_iso, ex.b), fmaf(ex.c, b_iso, ex.d));
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int t = 2 * lane + e;
                     float bhat = 0.0f;
                     if (t < nvc) {
                         bhat = fmaf(aa[e], bb, oo[e]);
-                        bb = bhat / fmaf(uu[e], bhat, 1.0f);
+                        bb = __fdividef(bhat, fmaf(uu[e], bhat, 1.0f));
                     }
                     sm[SM_BHAT + t] = bhat;
                 }
@@ -679,8 +682,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             fence_proxy_async();
             tc_fence_before();
             named_bar(kBarOps, 256);
-            // Gram MMA (thread 128) and the next inputs (thread 160)
-            if (tid == 128 && !*s_abort) {
+            // Gram MMA (thread 256, whose warps read it out next) and the next inputs (thread 160)
+            if (tid == 256 && !*s_abort) {
                 tc_fence_after();
                 const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
 #pragma unroll
@@ -941,7 +944,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         }
     }
     int* s_ngram = reinterpret_cast<int*>(sm + SM_FLAG + 1);
-    if (tid == 128) *s_ngram = n_gram_issued;
+    if (tid == 256) *s_ngram = n_gram_issued;
     tc_fence_before();
     __syncthreads();
     if (*s_abort) {
