@@ -29,9 +29,10 @@
 //       that is the A operand of the prediction/query MMA.
 //   H   Delta'^T = (V^T - Z^T) T^T = V^T T^T + (-Z^T) T^T (-Z^T in bf16 in TMEM
 //       as an A operand).
-//   J   O^T += Delta'^T A'^T ; S^T += Delta'^T K_til'  (Delta'^T in bf16 in TMEM
-//       as the A operand; the state stays in TMEM, the pending factor
-//       e^{G_C - G_ref} is folded into the next chunk's scaling).
+//   J   S^T += Delta'^T K_til' ; O^T += Delta'^T A'^T (issued at the start of
+//       the next chunk)  (Delta'^T in bf16 in TMEM as the A operand; the state
+//       stays in TMEM, the pending factor e^{G_C - G_ref} is folded into the next
+//       chunk's scaling).
 //   K   o = O (bf16) to global memory at the start of the next chunk.
 // Schedule per chunk n: warps 0-3 store the outputs of chunk n-1 and move the
 // state into the chunk's frame while warps 4-11 build the operands; one thread
@@ -95,7 +96,7 @@ constexpr int SM_R = 0, SM_MUR = 64, SM_BHAT = 128, SM_ZP = 192, SM_AP = 448, SM
               SM_FOUT = 832, SM_OMI = 960, SM_FLAG = 1024, SM_CF = 1032 /* [2][128] by chunk parity */,
               SM_INVD = 1288, SM_FLOATS = 1352;
 constexpr uint32_t OFF_BAR = OFF_SMALL + SM_FLOATS * 4;
-constexpr uint32_t kSmemBytes = OFF_BAR + 64;
+constexpr uint32_t kSmemBytes = OFF_BAR + 80;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 static_assert(OFF_TF + 64 * kLDF * 4 <= OFF_XT, "T fp32 before the merge scratch");
 static_assert(OFF_XT + 32 * kLDX * 4 <= OFF_SMALL, "merge scratch before the small region");
@@ -256,9 +257,11 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     const uint32_t sb = smem_addr(base);
     float* sm = reinterpret_cast<float*>(base + OFF_SMALL);
     volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SM_FLAG);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + OFF_BAR + 48);
-    const uint32_t bar_in = sb + OFF_BAR, bar_v = bar_in + 8, bar_mma = bar_in + 16, bar_o = bar_in + 24,
-                   bar_oj = bar_in + 32, bar_ops = bar_in + 40;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + OFF_BAR + 64);
+    // inputs of a chunk arrive on three barriers: log_alpha (bar_la), k and omega
+    // (bar_ko), q (bar_q), in the order the passes need them
+    const uint32_t bar_la = sb + OFF_BAR, bar_v = bar_la + 8, bar_mma = bar_la + 16, bar_o = bar_la + 24,
+                   bar_oj = bar_la + 32, bar_ops = bar_la + 40, bar_ko = bar_la + 48, bar_q = bar_la + 56;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool wg0 = tid < 128, wg1 = tid >= 128 && tid < 256, wg2 = tid >= 256;
@@ -266,7 +269,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     const int nchunks = (T + kC - 1) / kC;
 
     if (tid == 0) {
-        mbar_init(bar_in, 1);
+        mbar_init(bar_la, 1);
+        mbar_init(bar_ko, 1);
+        mbar_init(bar_q, 1);
         mbar_init(bar_v, 1);
         mbar_init(bar_mma, 1);
         mbar_init(bar_o, 1);
@@ -282,13 +287,15 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 
     auto issue_inputs = [&](int n) {
         const int t0 = n * kC;
-        mbar_expect_tx(bar_in, ISO ? 65536u : 98304u);
-        tma_load_4d(sb + OFF_QIN, &P.tq, 0, h, t0, b, bar_in);
-        tma_load_4d(sb + OFF_QIN + 8192, &P.tq, 64, h, t0, b, bar_in);
-        tma_load_4d(sb + OFF_KIN, &P.tk, 0, h, t0, b, bar_in);
-        tma_load_4d(sb + OFF_KIN + 8192, &P.tk, 64, h, t0, b, bar_in);
-        tma_load_4d(sb + OFF_LA, &P.tla, 0, h, t0, b, bar_in);
-        if (!ISO) tma_load_4d(sb + OFF_OM, &P.tom, 0, h, t0, b, bar_in);
+        mbar_expect_tx(bar_la, 32768u);
+        tma_load_4d(sb + OFF_LA, &P.tla, 0, h, t0, b, bar_la);
+        mbar_expect_tx(bar_ko, ISO ? 16384u : 49152u);
+        if (!ISO) tma_load_4d(sb + OFF_OM, &P.tom, 0, h, t0, b, bar_ko);
+        tma_load_4d(sb + OFF_KIN, &P.tk, 0, h, t0, b, bar_ko);
+        tma_load_4d(sb + OFF_KIN + 8192, &P.tk, 64, h, t0, b, bar_ko);
+        mbar_expect_tx(bar_q, 16384u);
+        tma_load_4d(sb + OFF_QIN, &P.tq, 0, h, t0, b, bar_q);
+        tma_load_4d(sb + OFF_QIN + 8192, &P.tq, 64, h, t0, b, bar_q);
     };
     auto issue_v = [&](int n) {
         mbar_expect_tx(bar_v, 16384u);
@@ -387,7 +394,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             sm[SM_MUR + t] = P.mu / rr;
             sm[SM_OMI + t] = om;
         }
-        wait_or_abort(bar_in, ph_in);
+        wait_or_abort(bar_la, ph_in);
         named_bar(kBarWG1, 128);
         const int i = tid - 128, w4 = warp - 4;
         // chunk log-decay G_C and the reference G_ref = G_C / 2 (log2 units)
@@ -406,6 +413,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         pend2 = kLog2e * GC - R2;
         sm[SM_FOUT + i] = ex2(pend2);
         float e1 = ex2(-R2);
+        wait_or_abort(bar_ko, ph_in);   // k and omega of chunk c
         const unsigned char* kin = base + OFF_KIN + (i >> 6) * 8192 + (i & 7) * 2;
         const int kch = (i & 63) >> 3;
 #pragma unroll 1
@@ -599,6 +607,18 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         tmem_wait_st();
     };
 
+    // O^T += Delta'^T A'^T of a finished chunk (thread 0; Delta' in TMEM and A' stay
+    // intact until the next chunk's prediction readout and Gram readout)
+    auto issue_output_update = [&]() {
+        tc_fence_after();
+        const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16_tmem_a(tmem + TM_O, tmem + TM_DB + 8 * ks, sw128_desc(sb + OFF_AQ + ks * 32, 16, 1024), id_o, 1u);
+        mma_commit(bar_oj);
+        ++n_oj_issued;
+    };
+
     if (wg1 && nchunks > 0) prep_gains(0);
     ph_in ^= 1u;
     tc_fence_before();
@@ -611,6 +631,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         // ================= step 1: state frame, outputs of chunk n-1, prediction/query MMA
         //                   || operands, Gram MMA, prefetch of chunk n+1
         if (wg0) {
+            if (tid == 0 && n > 0 && !*s_abort) issue_output_update();   // of chunk n-1
             scale_state(n);
             if (n > 0) {
                 wait_or_abort(bar_oj, pb ^ 1u);   // output update of chunk n-1 has landed
@@ -637,6 +658,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             // K_til' = p_hat k / e1 (isotropic: b_hat k / e1); the gain denominator enters
             // through the diagonal of the triangular system.
             const int u = tid - 128, g = u & 15, tr = u >> 4;
+            wait_or_abort(bar_q, pb);   // q of chunk n
 #pragma unroll 2
             for (int m4 = 0; m4 < 4; ++m4) {
                 const int t = tr + 16 * m4;
@@ -884,11 +906,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             }
             tc_fence_before();
             named_bar(kBarWG0, 128);
-            // ---- S^T += Delta'^T K_til' (committed first: the next chunk starts from it);
-            //      O^T += Delta'^T A'^T
+            // ---- S^T += Delta'^T K_til' (the next chunk starts from it); the output part
+            //      O^T += Delta'^T A'^T is issued at the start of the next chunk
             if (tid == 0 && !*s_abort) {
                 tc_fence_after();
-                const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
                 const uint32_t id_s = idesc_bf16(128, 128, 0, 1, 0);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
@@ -896,12 +917,6 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                                     id_s, 1u);
                 mma_commit(bar_mma);
                 ++n_mma_issued;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_tmem_a(tmem + TM_O, tmem + TM_DB + 8 * ks, sw128_desc(sb + OFF_AQ + ks * 32, 16, 1024),
-                                    id_o, 1u);
-                mma_commit(bar_oj);
-                ++n_oj_issued;
             }
         } else if (n + 1 < nchunks) {
             // ---- warps 4-7: gains of chunk n + 1
@@ -915,6 +930,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         if (*s_abort) break;
     }
 
+    if (tid == 0 && nchunks > 0 && !*s_abort) issue_output_update();   // of the last chunk
     const bool aborted = *s_abort != 0;
     if (!aborted && nchunks > 0) {
         wait_or_abort(bar_mma, static_cast<uint32_t>(nchunks - 1) & 1u);   // update of the last chunk has landed
@@ -956,7 +972,11 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             if (n_oj_issued > 0) mbar_wait(bar_oj, (n_oj_issued - 1) & 1, kWaitLimit);
             if (n_v_issued > 0) mbar_wait(bar_v, (n_v_issued - 1) & 1, kWaitLimit);
         }
-        if (tid == 160 && n_in_issued > 0) mbar_wait(bar_in, (n_in_issued - 1) & 1, kWaitLimit);
+        if (tid == 160 && n_in_issued > 0) {
+            mbar_wait(bar_la, (n_in_issued - 1) & 1, kWaitLimit);
+            mbar_wait(bar_ko, (n_in_issued - 1) & 1, kWaitLimit);
+            mbar_wait(bar_q, (n_in_issued - 1) & 1, kWaitLimit);
+        }
     }
     tc_fence_before();
     __syncthreads();
