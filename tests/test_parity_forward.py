@@ -232,3 +232,23 @@ def test_tensor_core_path_matches_oracle_and_portable_path(case):
     simt = _run(kdn, variant, t, S0=S0d, p0=p0d, chunk=64, flags=kdn.KDN_FLAG_PORTABLE)
     for a, b_ in zip(tc, simt):
         assert np.max(np.abs(to_host(a) - to_host(b_))) <= 2e-2 * max(1e-3, np.max(np.abs(to_host(b_)))), e
+
+
+@pytest.mark.parametrize("variant", ["diag", "iso"])
+def test_tensor_core_path_strong_decay(variant):
+    """Chunks whose log-decay exceeds 80 in magnitude (here 64 x 1.5 = 96 on head 0)
+    switch the fused kernel to the mid-chunk decay reference; the result must
+    still match the oracle, and no range error is reported (|G_C| <= 160)."""
+    import torch
+
+    kdn = _kdn()
+    B, T, H = 2, 200, 2
+    x = make_inputs(variant, B, T, H, 128, 128, io="bf16", seed=77)
+    x["log_alpha"][:, :, 0] = -1.5
+    t = to_device(x)
+    ws = torch.empty(kdn.workspace_size(kdn.KDN_DIAG if variant == "diag" else kdn.KDN_ISO, B, T, H, 128, 128,
+                                        64, kdn.KDN_BF16, 0), dtype=torch.uint8, device="cuda")
+    got = _run(kdn, variant, t, chunk=64, workspace=ws)
+    assert kdn.kdn_read_device_status(ws) == 0
+    ref = oracle.forward(variant, x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"])
+    _check(variant, x, got, ref, "bf16", "strong decay")

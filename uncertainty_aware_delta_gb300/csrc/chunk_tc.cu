@@ -9,10 +9,11 @@
 //       per-channel variance as that pair, held in registers).  Isotropic variant (Sec. 4.2 Eq. 40, App. C): the
 //       scalar map is composed as 2x2 Moebius matrices with a warp-shuffle
 //       inclusive scan over the chunk's tokens, then replayed from the carry.
-//       The decay factors relative to the chunk's per-channel reference
-//       G_ref = G_C / 2 (App. D: decay ratios from differences of cumulative
-//       log-decay) are running products e1_t = e^{G_t - G_ref}; their
-//       reciprocals e2 = 1 / e1 are taken in the operand pass.
+//       The decay factors relative to the chunk's per-channel reference G_ref
+//       (App. D: decay ratios from differences of cumulative log-decay) are
+//       running products e1_t = e^{G_t - G_ref}, G_ref = 0 (chunk start) when
+//       |G_C| <= 80 and G_C / 2 otherwise; their reciprocals are taken in the
+//       operand pass.
 //   A2  decayed operands (bf16, 128-byte-swizzled, tensor-core layouts):
 //         K_bar = k e1, Q_bar = q e1, K_til' = p_hat k / e1  (the isotropic
 //       variant uses its scalar b_hat in place of p_hat).
@@ -73,6 +74,10 @@ constexpr int kNT = 384;
 constexpr int kBarWG1 = 1, kBarWG0 = 2, kBarTReady = 3, kBarOps = 5, kBarWG2 = 6;
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr float kLog2e = 1.4426950408889634f;
+// Chunks whose log-decay stays within this bound use the chunk start as the decay
+// reference (every factor e^{G_t} and its reciprocal fit in fp32 and bf16); the
+// rare chunks beyond it switch to the mid-chunk reference G_C / 2.
+constexpr float kStartRefLogDecay = 80.0f;
 
 // Shared memory map (bytes from a 1024-aligned base).  Regions reused within
 // a chunk are noted; every reuse starts after the previous user finished.
@@ -112,6 +117,7 @@ constexpr uint32_t TM_S = 0, TM_ZD = 128, TM_O = 192, TM_G = 256, TM_SMB = 320, 
 struct TcParams {
     CUtensorMap tq, tk, tv, tla, tom;
     const float* r;
+    const float* la;
     const float* om_iso;
     const float* S0;
     const float* p0;
@@ -234,6 +240,14 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
         " fma.rn.f32x2 rd, ra, rb, rc; mov.b64 {%0, %1}, rd; }"
         : "=f"(d.x), "=f"(d.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{ .reg .b64 ra, rb, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5}; add.rn.f32x2 rd, ra, rb;"
+        " mov.b64 {%0, %1}, rd; }"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
 }
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
@@ -397,23 +411,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         wait_or_abort(bar_la, ph_in);
         named_bar(kBarWG1, 128);
         const int i = tid - 128, w4 = warp - 4;
-        // chunk log-decay G_C and the reference G_ref = G_C / 2 (log2 units)
-        float gs0 = 0.0f, gs1 = 0.0f, gs2 = 0.0f, gs3 = 0.0f;
-#pragma unroll
-        for (int t = 0; t < kC; t += 4) {
-            gs0 += LA[t * kD + i];
-            gs1 += LA[(t + 1) * kD + i];
-            gs2 += LA[(t + 2) * kD + i];
-            gs3 += LA[(t + 3) * kD + i];
-        }
-        const float GC = (gs0 + gs1) + (gs2 + gs3);
-        if (!(fabsf(GC) <= kMaxChunkLogDecay)) set_status(P.status, kStatusRange);
-        const float R2 = 0.5f * kLog2e * GC;
-        sm[SM_CF + (c & 1) * 128 + i] = ex2(pend2 + R2);
-        pend2 = kLog2e * GC - R2;
-        sm[SM_FOUT + i] = ex2(pend2);
-        float e1 = ex2(-R2);
         wait_or_abort(bar_ko, ph_in);   // k and omega of chunk c
+        // decay factors relative to the chunk start (reference checked after the chunk)
+        float e1 = 1.0f;
+        float2 g2 = make_float2(0.0f, 0.0f);   // chunk log-decay, log2 units, two partial sums
         const unsigned char* kin = base + OFF_KIN + (i >> 6) * 8192 + (i & 7) * 2;
         const int kch = (i & 63) >> 3;
 #pragma unroll 1
@@ -451,6 +452,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     for (int u = 0; u < 16; u += 2) {
                         const int t = tb + u;
                         const float2 l2 = fmul2(make_float2(la[u], la[u + 1]), make_float2(kLog2e, kLog2e));
+                        g2 = fadd2(g2, l2);
                         const float al0 = ex2(l2.x), al1 = ex2(l2.y);
                         const float2 a2 = fmul2(make_float2(al0, al1), make_float2(al0, al1));
                         const float2 kk = make_float2(kv[u], kv[u + 1]);
@@ -485,6 +487,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     for (int u = 0; u < 16; ++u) {
                         const int t = tb + u;
                         const float l2 = la[u] * kLog2e;
+                        g2.x += l2;
                         const float al = ex2(l2), a2 = al * al, k2 = kv[u] * kv[u];
                         e1 *= al;
                         LA[t * kD + i] = e1;
@@ -497,6 +500,26 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 sm[SM_ZP + w4 * 64 + hf * 32 + lane] = butterfly_sum32(w, lane);
                 sm[SM_AP + w4 * 64 + hf * 32 + lane] = butterfly_sum32(w2, lane);
             }
+        }
+        {
+            const float G2C = g2.x + g2.y;
+            if (!(fabsf(G2C) <= kMaxChunkLogDecay * kLog2e)) set_status(P.status, kStatusRange);
+            float R2 = 0.0f;
+            if (fabsf(G2C) > kStartRefLogDecay * kLog2e) {
+                // rare: strong decay in this channel, recompute its factors with G_ref = G_C / 2
+                // from log_alpha in global memory (the tile now holds the factors)
+                R2 = 0.5f * G2C;
+                float gg = 0.0f;
+                const float* lag = P.la + (static_cast<size_t>(b) * T + t0c) * H * kD + static_cast<size_t>(h) * kD + i;
+#pragma unroll 4
+                for (int t = 0; t < kC; ++t) {
+                    if (t < nvc) gg += lag[static_cast<size_t>(t) * H * kD] * kLog2e;
+                    LA[t * kD + i] = ex2(gg - R2);
+                }
+            }
+            sm[SM_CF + (c & 1) * 128 + i] = ex2(pend2 + R2);
+            pend2 = G2C - R2;
+            sm[SM_FOUT + i] = ex2(pend2);
         }
         if (ISO) {
             named_bar(kBarWG1, 128);
@@ -1040,6 +1063,7 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t s) {
         ok = encode_4d(&P.tom, a.omega, F32, 4, a.B, a.T, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return cudaErrorInvalidValue;
     P.r = a.r;
+    P.la = a.log_alpha;
     P.om_iso = a.variant == 1 ? a.omega : nullptr;
     P.S0 = a.S0;
     P.p0 = a.p0;
