@@ -94,6 +94,36 @@ def device_inputs(torch, w, variant, seed, device, T=None, B=None):
     return {"q": q, "k": k, "v": v, "log_alpha": la, "omega": om, "r": r}
 
 
+def device_pkda_inputs(torch, w, seed, device):
+    """PKDA inputs on the device with the workload recipe (q, k, v and
+    log_alpha as above; beta = sigmoid(N(0,1)), alpha_p = exp(-U(lo, hi)),
+    beta_p = sigmoid(N(0,1)) per token-head; center = exp(N(0, 0.5)) per head)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    B, T, H, d = w.B, w.T, w.H, w.d
+    iot = torch.bfloat16 if w.io == "bf16" else torch.float32
+    f = dict(device=device, generator=g)
+    q = torch.nn.functional.normalize(torch.randn(B, T, H, d, **f), dim=-1).to(iot)
+    k = torch.nn.functional.normalize(torch.randn(B, T, H, d, **f), dim=-1).to(iot)
+    v = torch.randn(B, T, H, d, **f).to(iot)
+    lo, hi = w.log_alpha_range
+    la = -(lo + (hi - lo) * torch.rand(B, T, H, d, **f))
+    beta = torch.sigmoid(torch.randn(B, T, H, **f))
+    alpha_p = torch.exp(-(lo + (hi - lo) * torch.rand(B, T, H, **f)))
+    beta_p = torch.sigmoid(torch.randn(B, T, H, **f))
+    center = torch.exp(0.5 * torch.randn(H, **f))
+    return {"q": q, "k": k, "v": v, "log_alpha": la, "beta": beta, "alpha_p": alpha_p, "beta_p": beta_p,
+            "center": center}
+
+
+def pkda_algorithmic_bytes(B, T, H, dk, dv, io):
+    """PKDA inputs and outputs: q, k, v, log_alpha, beta, alpha_p, beta_p read
+    once, o written once, S_T and A_T written once, the per-head centres read."""
+    e = 2 if io == "bf16" else 4
+    per_tok = e * (2 * dk + dv) + 4 * dk + 3 * 4 + e * dv
+    return B * T * H * per_tok + B * H * (dk * dv + dk) * 4 + H * 4
+
+
 def algorithmic_bytes(B, T, H, dk, dv, io, variant):
     """Method inputs and outputs only: q, k, v, log_alpha, omega, r read once,
     o written once, final S_T and p_T written once (S_0 = 0, p_0 = 1 are not read)."""
@@ -435,6 +465,15 @@ def other_workloads(torch, kdn, WORKLOADS, device, barrier, peaks):
         out[name] = {"tokens_per_s": w.B * w.T / (ms / 1e3), "ms": ms,
                      "hbm_frac": ab / (ms / 1e3) / 1e9 / hbm}
         del x
+    # PKDA (preconditioned delta rule with per-channel decay) on the headline shape
+    w = WORKLOADS["pkda-bf16-b8h16t4096d128"]
+    x = device_pkda_inputs(torch, w, w.seed, device)
+    names = ("q", "k", "v", "log_alpha", "beta", "alpha_p", "beta_p", "center")
+    ms = time_calls(torch, lambda: kdn.kdn_pkda_forward(*(x[n] for n in names), chunk=w.chunk), 5, 2, barrier)
+    ab = pkda_algorithmic_bytes(w.B, w.T, w.H, w.d, w.d, w.io)
+    out[w.name] = {"tokens_per_s": w.B * w.T / (ms / 1e3), "ms": ms, "hbm_frac": ab / (ms / 1e3) / 1e9 / hbm,
+                   "algorithmic_bytes": ab}
+    del x
     # decode: 512-token prefill through the forward path, then 1024 single-token steps
     w = WORKLOADS["diag-decode-f32-s256h16d128"]
     pre = device_inputs(torch, w, "diag", w.seed, device, T=w.prefill)

@@ -22,6 +22,12 @@
  * compact-WY / UT form (App. D).  Results do not depend on the chunk length
  * beyond floating-point rounding.
  *
+ * The same memory machinery also runs the preconditioned delta rule with
+ * per-channel decay (PKDA; "Preconditioned DeltaNet", arXiv:2604.21100v1,
+ * Sec. 2.4 Eq. 9 and Sec. 2.5), whose write key is the read key rescaled per
+ * channel by a bounded function of a decayed key statistic; see
+ * kdn_pkda_forward.
+ *
  * Conventions for every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
  *     never allocates, frees or retains them and keeps no global mutable state
@@ -79,7 +85,7 @@ typedef enum {
 } kdn_status;
 
 typedef enum { KDN_F32 = 0, KDN_BF16 = 1 } kdn_dtype;
-typedef enum { KDN_DIAG = 0, KDN_ISO = 1 } kdn_variant;
+typedef enum { KDN_DIAG = 0, KDN_ISO = 1, KDN_PKDA = 2 } kdn_variant;
 
 /* Flags for the forward calls. */
 #define KDN_FLAG_PORTABLE 0x1u   /* force the CUDA-core (FFMA) chunk path */
@@ -94,7 +100,7 @@ typedef enum { KDN_DIAG = 0, KDN_ISO = 1 } kdn_variant;
 
 /*
  * Bytes of device workspace a forward (T > 0) or step (T == 1) call needs.
- * variant: KDN_DIAG or KDN_ISO.  Returns 0 for unsupported arguments.  The
+ * variant: KDN_DIAG, KDN_ISO or KDN_PKDA.  Returns 0 for unsupported arguments.  The
  * workspace is scratch owned by the caller, at least 256-byte aligned; its
  * first 256 bytes hold the device status word.  Calls that overlap in time
  * must use different workspaces.
@@ -140,6 +146,43 @@ kdn_status kdn_iso_forward(int B, int T, int H, int dk, int dv, int chunk, float
                            void *workspace, size_t workspace_bytes, kdn_stream_t stream);
 
 /*
+ * Preconditioned delta rule with per-channel decay, PKDA ("Preconditioned
+ * DeltaNet", arXiv:2604.21100v1: Sec. 2.4 Eq. 9, the write key; Sec. 2.5, the
+ * decayed state; Sec. 2.6, its chunkwise form).  PGDN is the special case of
+ * a log_alpha equal across channels, PDN the case log_alpha = 0.  Per head,
+ * memory S (d_k x d_v, row = key channel) and key statistic A (d_k), and for
+ * every token t:
+ *
+ *   A      = alpha_p_t A + beta_p_t (k_t * k_t)           (this token included)
+ *   rho    = log(max(A, 1e-20)) - center_h                (centred in log space)
+ *   k_til  = exp(-log(x) rho / (1 + |rho|)) * k_t         (softsign; scale in [1/x, x])
+ *   S_hat  = diag(exp(log_alpha_t)) S
+ *   S      = S_hat + beta_t k_til (v_t - S_hat^T k_t)^T   (residual with the read key)
+ *   o_t    = S^T q_t                                      (after the write)
+ *
+ * Inputs : q, k [B,T,H,dk] io_dtype; v [B,T,H,dv] io_dtype;
+ *          log_alpha [B,T,H,dk] (log of the per-channel state decay);
+ *          beta [B,T,H] write strength; alpha_p [B,T,H] statistic decay in
+ *          [0, 1]; beta_p [B,T,H] statistic weight >= 0; center [H] the
+ *          per-head log-space centre (the pages' mu > 0);
+ *          S0 [B,H,dk,dv] or NULL (zero memory); A0 [B,H,dk] or NULL (zero
+ *          statistic).
+ * Outputs: o [B,T,H,dv] io_dtype; S_T [B,H,dk,dv]; A_T [B,H,dk] (the state
+ *          after token T-1, the resume point of kdn_pkda_step or a later call).
+ * x      : bound of the write scale (the pages use 1.5); x <= 0 selects 1.5.
+ * Sizes, paths, workspace (variant KDN_PKDA), flags, aliasing (S_T == S0 and
+ * A_T == A0 allowed) and errors: as kdn_diag_forward.
+ */
+kdn_status kdn_pkda_forward(int B, int T, int H, int dk, int dv, int chunk, float x,
+                            int io_dtype, uint32_t flags,
+                            const void *q, const void *k, const void *v,
+                            const float *log_alpha, const float *beta, const float *alpha_p,
+                            const float *beta_p, const float *center,
+                            const float *S0, const float *A0,
+                            void *o, float *S_T, float *A_T,
+                            void *workspace, size_t workspace_bytes, kdn_stream_t stream);
+
+/*
  * Single-token decode for B independent sequences (the recurrent form of
  * the same recurrence; KDN paper Sec. 5.1 and App. C): one token per
  * (sequence, head), state updated IN PLACE.
@@ -158,6 +201,22 @@ kdn_status kdn_step(int variant, int B, int H, int dk, int dv, float mu, int io_
                     void *workspace, size_t workspace_bytes, kdn_stream_t stream);
 
 /*
+ * Single-token PKDA decode (one token of kdn_pkda_forward per sequence and
+ * head), state updated IN PLACE.
+ * Inputs : q, k [B,H,dk] io_dtype; v [B,H,dv] io_dtype; log_alpha [B,H,dk];
+ *          beta, alpha_p, beta_p [B,H]; center [H].
+ * In/out : S [B,H,dk,dv], A [B,H,dk] (fp32).
+ * Output : o [B,H,dv] io_dtype.
+ * Workspace: kdn_workspace_size(KDN_PKDA, B, 1, H, dk, dv, 0, io_dtype, 0) bytes.
+ */
+kdn_status kdn_pkda_step(int B, int H, int dk, int dv, float x, int io_dtype,
+                         const void *q, const void *k, const void *v,
+                         const float *log_alpha, const float *beta, const float *alpha_p,
+                         const float *beta_p, const float *center,
+                         float *S, float *A, void *o,
+                         void *workspace, size_t workspace_bytes, kdn_stream_t stream);
+
+/*
  * Forward without a caller workspace.  The paper has no counterpart: this is
  * a convenience of the library for callers that cannot allocate device
  * memory at the point where they run the mixer -- for example code inside a
@@ -171,8 +230,8 @@ kdn_status kdn_step(int variant, int B, int H, int dk, int dv, float mu, int io_
  * until the process exits.  This entry point calls no cudaMalloc, cudaFree
  * or other allocating routine.
  *
- * variant: KDN_DIAG or KDN_ISO.  Every other argument means what it means
- * for kdn_diag_forward / kdn_iso_forward; inputs and outputs are still
+ * variant: KDN_DIAG or KDN_ISO (PKDA has no allocation-free entry point).
+ * Every other argument means what it means for kdn_diag_forward / kdn_iso_forward; inputs and outputs are still
  * caller-owned device buffers.  status_out: NULL, or a caller-owned device
  * uint32_t (4-byte aligned) that receives this call's device status word on
  * `stream` (the codes kdn_read_device_status returns).

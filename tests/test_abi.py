@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("kdn_diag_forward", "kdn_iso_forward", "kdn_step", "kdn_workspace_size",
               "kdn_read_device_status", "kdn_status_string", "kdn_abi_version",
-              "kdn_forward_kernel_count", "kdn_forward_noalloc"):
+              "kdn_forward_kernel_count", "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step"):
         assert n in names
 
 
@@ -46,7 +46,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings_and_version(lib):
     import uncertainty_aware_delta_gb300 as kdn
 
-    assert lib.kdn_abi_version() == 100
+    assert lib.kdn_abi_version() == 101
     for code in range(0, 11):
         s = kdn.status_string(code)
         assert s and s != "unknown status"
@@ -61,7 +61,9 @@ def test_workspace_size_rules(lib):
     assert ws(0, 1, 64, 2, 24, 16, 16, 0, 0) == 0
     assert ws(0, 1, 64, 2, 16, 16, 48, 0, 0) == 0
     assert ws(0, -1, 64, 2, 16, 16, 16, 0, 0) == 0
-    assert ws(2, 1, 64, 2, 16, 16, 16, 0, 0) == 0
+    assert ws(3, 1, 64, 2, 16, 16, 16, 0, 0) == 0
+    # PKDA keeps a per-channel statistic: the same scratch as the diagonal variant
+    assert ws(2, 2, 100, 3, 32, 16, 16, 0, 1) == ws(0, 2, 100, 3, 32, 16, 16, 0, 1)
     assert ws(0, 1, 64, 2, 16, 16, 16, 5, 0) == 0
     # the portable path stores gains [B,T,H,dk] fp32 plus the scan summaries
     n = ws(0, 2, 100, 3, 32, 16, 16, 0, 1)
@@ -79,6 +81,8 @@ def test_forward_kernel_count(lib):
     assert kdn.forward_kernel_count(0, 1, 0, 2, 16, 16, 0, 0, 0) == 1     # state copy
     assert kdn.forward_kernel_count(0, 0, 64, 2, 16, 16, 0, 0, 0) == 0
     assert kdn.forward_kernel_count(0, 1, 64, 2, 24, 16, 0, 0, 0) == 0
+    assert kdn.forward_kernel_count(2, 1, 64, 2, 16, 16, 16, 0, 0) == 4   # PKDA: statistic scan + chunk pass
+    assert kdn.forward_kernel_count(2, 1, 64, 2, 128, 128, 64, 1, 0) == 1  # fused tensor-core kernel
 
 
 def _fwd_args(**over):
@@ -130,3 +134,43 @@ def test_step_validation_rejects_before_launch(lib):
     p3 = list(ptrs)
     p3[8] = vp((1 << 20) + 64)                               # o overlaps S
     assert lib.kdn_step(*base, *p3, *ws) == 10
+
+
+def _pkda_call(lib, **over):
+    a = dict(B=1, T=64, H=2, dk=16, dv=16, chunk=16, x=1.5, io=0, flags=0,
+             q=64, k=64, v=64, la=64, beta=64, ap=64, bp=64, ce=64, S0=None, A0=None,
+             o=1 << 20, S_T=2 << 20, A_T=3 << 20, ws=4 << 20, wsb=1 << 20)
+    a.update(over)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.kdn_pkda_forward(a["B"], a["T"], a["H"], a["dk"], a["dv"], a["chunk"], a["x"], a["io"],
+                                a["flags"], vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["la"]), vp(a["beta"]),
+                                vp(a["ap"]), vp(a["bp"]), vp(a["ce"]), vp(a["S0"]), vp(a["A0"]), vp(a["o"]),
+                                vp(a["S_T"]), vp(a["A_T"]), vp(a["ws"]), a["wsb"], None)
+
+
+def test_pkda_validation_rejects_before_launch(lib):
+    assert _pkda_call(lib, dk=24) == 6
+    assert _pkda_call(lib, io=3) == 3
+    assert _pkda_call(lib, beta=None) == 1
+    assert _pkda_call(lib, ce=None) == 1
+    assert _pkda_call(lib, A_T=None) == 1
+    assert _pkda_call(lib, bp=72) == 4
+    assert _pkda_call(lib, o=64 + 16) == 10
+    assert _pkda_call(lib, ws=None) == 5
+
+
+def test_pkda_step_validation_rejects_before_launch(lib):
+    vp = ctypes.c_void_p
+    base = [4, 2, 16, 16, 1.5, 0]
+    ptrs = [vp(1 << 12), vp(2 << 12), vp(3 << 12), vp(4 << 12), vp(5 << 12), vp(6 << 12), vp(7 << 12),
+            vp(8 << 12), vp(1 << 20), vp(2 << 20), vp(3 << 20)]
+    ws = [vp(4 << 20), 256, None]
+    assert lib.kdn_pkda_step(*base, *ptrs, None, 256, None) == 5
+    p1 = list(ptrs)
+    p1[4] = None                                               # beta
+    assert lib.kdn_pkda_step(*base, *p1, *ws) == 1
+    p2 = list(ptrs)
+    p2[10] = vp((1 << 20) + 64)                                # o overlaps S
+    assert lib.kdn_pkda_step(*base, *p2, *ws) == 10
+    # the KDN step entry point does not take the PKDA variant
+    assert lib.kdn_step(2, 4, 2, 16, 16, -1.0, 0, *ptrs[:6], vp(1 << 20), vp(2 << 20), vp(3 << 20), *ws) == 2

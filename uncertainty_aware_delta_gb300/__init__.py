@@ -12,10 +12,13 @@ from .binding import (  # noqa: F401
     KDN_F32,
     KDN_FLAG_PORTABLE,
     KDN_ISO,
+    KDN_PKDA,
     KDNError,
     kdn_diag_forward,
     kdn_forward_noalloc,
     kdn_iso_forward,
+    kdn_pkda_forward,
+    kdn_pkda_step,
     kdn_read_device_status,
     kdn_step,
     forward_kernel_count,

@@ -18,13 +18,13 @@ _lock = threading.Lock()
 _lib = None
 
 KDN_F32, KDN_BF16 = 0, 1
-KDN_DIAG, KDN_ISO = 0, 1
+KDN_DIAG, KDN_ISO, KDN_PKDA = 0, 1, 2
 KDN_FLAG_PORTABLE = 0x1
 
 EXPORTED = (
     "kdn_workspace_size", "kdn_diag_forward", "kdn_iso_forward", "kdn_step",
     "kdn_read_device_status", "kdn_status_string", "kdn_abi_version", "kdn_forward_kernel_count",
-    "kdn_forward_noalloc",
+    "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step",
 )
 
 
@@ -58,6 +58,12 @@ def library():
                 getattr(lib, name).argtypes = fwd
             lib.kdn_step.restype = i32
             lib.kdn_step.argtypes = [i32] * 5 + [f32, i32] + [vp] * 3 + [fp] * 3 + [fp, fp, vp] + [vp, sz, vp]
+            lib.kdn_pkda_forward.restype = i32
+            lib.kdn_pkda_forward.argtypes = [i32] * 6 + [f32, i32, u32] + [vp] * 3 + [fp] * 5 + \
+                [fp, fp] + [vp, fp, fp] + [vp, sz, vp]
+            lib.kdn_pkda_step.restype = i32
+            lib.kdn_pkda_step.argtypes = [i32] * 4 + [f32, i32] + [vp] * 3 + [fp] * 5 + [fp, fp, vp] + \
+                [vp, sz, vp]
             lib.kdn_read_device_status.restype = i32
             lib.kdn_read_device_status.argtypes = [vp, vp]
             lib.kdn_status_string.restype = ctypes.c_char_p
@@ -207,6 +213,87 @@ def kdn_step(variant, q, k, v, log_alpha, omega, r, S, p, *, mu=None, o=None, wo
                           workspace.numel() * workspace.element_size(), _stream(stream, device))
     if st != 0:
         raise KDNError(st, "kdn_step")
+    return o
+
+
+def kdn_pkda_forward(q, k, v, log_alpha, beta, alpha_p, beta_p, center, S0=None, A0=None, *, x=1.5,
+                     chunk=0, flags=0, out=None, workspace=None, stream=None):
+    """Preconditioned delta rule with per-channel decay (Preconditioned DeltaNet
+    Sec. 2.4 Eq. 9, Sec. 2.5).  Returns (o, S_T, A_T).
+
+    q, k [B,T,H,dk] and v [B,T,H,dv] in fp32 or bf16; log_alpha [B,T,H,dk];
+    beta, alpha_p, beta_p [B,T,H]; center [H]; optional S0 [B,H,dk,dv] and
+    A0 [B,H,dk] (the key statistic; zero when omitted).  ``x`` bounds the
+    write scale to [1/x, x].  ``out=(o, S_T, A_T)`` writes into given tensors.
+    """
+    lib = library()
+    device = q.device
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    io = KDN_BF16 if q.dtype == torch.bfloat16 else KDN_F32
+    iot = torch.bfloat16 if io == KDN_BF16 else torch.float32
+    f32 = torch.float32
+    for t, name, dt, shp in ((q, "q", iot, (B, T, H, dk)), (k, "k", iot, (B, T, H, dk)),
+                             (v, "v", iot, (B, T, H, dv)), (log_alpha, "log_alpha", f32, (B, T, H, dk)),
+                             (beta, "beta", f32, (B, T, H)), (alpha_p, "alpha_p", f32, (B, T, H)),
+                             (beta_p, "beta_p", f32, (B, T, H)), (center, "center", f32, (H,)),
+                             (S0, "S0", f32, (B, H, dk, dv)), (A0, "A0", f32, (B, H, dk))):
+        _check(t, name, dt, shp, device)
+    if out is None:
+        o = torch.empty((B, T, H, dv), dtype=iot, device=device)
+        S_T = torch.empty((B, H, dk, dv), dtype=f32, device=device)
+        A_T = torch.empty((B, H, dk), dtype=f32, device=device)
+    else:
+        o, S_T, A_T = out
+        _check(o, "o", iot, (B, T, H, dv), device)
+        _check(S_T, "S_T", f32, (B, H, dk, dv), device)
+        _check(A_T, "A_T", f32, (B, H, dk), device)
+    need = lib.kdn_workspace_size(KDN_PKDA, B, T, H, dk, dv, chunk, io, flags)
+    if need == 0:
+        raise KDNError(6, "kdn_workspace_size rejected the arguments")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds {workspace.numel()} bytes, {need} needed")
+    with torch.cuda.device(device):
+        st = lib.kdn_pkda_forward(B, T, H, dk, dv, int(chunk), float(x), io, int(flags), _ptr(q), _ptr(k),
+                                  _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(alpha_p), _ptr(beta_p),
+                                  _ptr(center), _ptr(S0), _ptr(A0), _ptr(o), _ptr(S_T), _ptr(A_T),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream, device))
+    if st != 0:
+        raise KDNError(st, "kdn_pkda_forward")
+    return o, S_T, A_T
+
+
+def kdn_pkda_step(q, k, v, log_alpha, beta, alpha_p, beta_p, center, S, A, *, x=1.5, o=None,
+                  workspace=None, stream=None):
+    """One PKDA decode token per sequence; S and A are updated in place.  Returns o [B,H,dv]."""
+    lib = library()
+    device = q.device
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    io = KDN_BF16 if q.dtype == torch.bfloat16 else KDN_F32
+    iot = torch.bfloat16 if io == KDN_BF16 else torch.float32
+    f32 = torch.float32
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=iot, device=device)
+    for t, name, dt, shp in ((q, "q", iot, (B, H, dk)), (k, "k", iot, (B, H, dk)), (v, "v", iot, (B, H, dv)),
+                             (log_alpha, "log_alpha", f32, (B, H, dk)), (beta, "beta", f32, (B, H)),
+                             (alpha_p, "alpha_p", f32, (B, H)), (beta_p, "beta_p", f32, (B, H)),
+                             (center, "center", f32, (H,)), (S, "S", f32, (B, H, dk, dv)),
+                             (A, "A", f32, (B, H, dk)), (o, "o", iot, (B, H, dv))):
+        _check(t, name, dt, shp, device)
+    need = lib.kdn_workspace_size(KDN_PKDA, B, 1, H, dk, dv, 0, io, 0)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    with torch.cuda.device(device):
+        st = lib.kdn_pkda_step(B, H, dk, dv, float(x), io, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                               _ptr(beta), _ptr(alpha_p), _ptr(beta_p), _ptr(center), _ptr(S), _ptr(A),
+                               _ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream, device))
+    if st != 0:
+        raise KDNError(st, "kdn_pkda_step")
     return o
 
 

@@ -2,6 +2,7 @@
 // kernel dispatch.  See include/kdn.h for the contract of every entry point.
 
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -56,7 +57,7 @@ WsLayout ws_layout(int variant, int B, int T, int H, int dk, int dv, int chunk, 
     memset(&w, 0, sizeof(w));
     size_t off = kStatusBytes;
     if (T > 0 && !use_tc_path(io, dk, dv, chunk, flags)) {
-        const int nu = variant == KDN_DIAG ? dk : 1;
+        const int nu = variant == KDN_ISO ? 1 : dk;
         const size_t BH = (size_t)B * H;
         w.nG = (T + kdn::kGainChunk - 1) / kdn::kGainChunk;
         w.kappa_off = off;
@@ -71,7 +72,7 @@ WsLayout ws_layout(int variant, int B, int T, int H, int dk, int dv, int chunk, 
 }
 
 kdn_status validate_common(int variant, int B, int T, int H, int dk, int dv, int chunk, int io) {
-    if (variant != KDN_DIAG && variant != KDN_ISO) return KDN_ERR_SHAPE;
+    if (variant != KDN_DIAG && variant != KDN_ISO && variant != KDN_PKDA) return KDN_ERR_SHAPE;
     if (io != KDN_F32 && io != KDN_BF16) return KDN_ERR_DTYPE;
     if (B < 0 || T < 0 || H < 0) return KDN_ERR_SHAPE;
     if (!supported_dim(dk) || !supported_dim(dv)) return KDN_ERR_UNSUPPORTED;
@@ -82,22 +83,35 @@ kdn_status validate_common(int variant, int B, int T, int H, int dk, int dv, int
     return KDN_OK;
 }
 
+// Inputs of the preconditioned delta rule (PKDA) that KDN does not have.
+struct PkdaInputs {
+    const float *beta, *alpha_p, *beta_p, *center;
+    float x;
+};
+
+float resolve_x(float x) { return x > 0.f ? x : 1.5f; }
+
 kdn_status forward_impl(int variant, int B, int T, int H, int dk, int dv, int chunk, float mu,
                         int io, uint32_t flags, const void* q, const void* k, const void* v,
                         const float* log_alpha, const float* omega, const float* r,
                         const float* S0, const float* p0, void* o, float* S_T, float* p_T,
-                        void* workspace, size_t workspace_bytes, kdn_stream_t stream) {
+                        void* workspace, size_t workspace_bytes, kdn_stream_t stream,
+                        const PkdaInputs& pk) {
     kdn_status st = validate_common(variant, B, T, H, dk, dv, chunk, io);
     if (st != KDN_OK) return st;
     chunk = resolve_chunk(chunk, T);
+    const bool is_pk = variant == KDN_PKDA;
     const size_t BH = (size_t)B * H;
     const size_t esz = io == KDN_BF16 ? 2 : 4;
     const size_t ntok = (size_t)B * T * H;
-    const size_t nu = variant == KDN_DIAG ? (size_t)dk : 1;
+    const size_t nu = variant == KDN_ISO ? 1 : (size_t)dk;
     if (!workspace) return KDN_ERR_WORKSPACE;
     if (BH > 0 && (!S_T || !p_T)) return KDN_ERR_NULL;
-    if (ntok > 0 && (!q || !k || !v || !log_alpha || !omega || !r || !o)) return KDN_ERR_NULL;
-    const void* ptrs[] = {q, k, v, log_alpha, omega, r, S0, p0, o, S_T, p_T, workspace};
+    if (ntok > 0 && (!q || !k || !v || !log_alpha || !o)) return KDN_ERR_NULL;
+    if (ntok > 0 && !is_pk && (!omega || !r)) return KDN_ERR_NULL;
+    if (ntok > 0 && is_pk && (!pk.beta || !pk.alpha_p || !pk.beta_p || !pk.center)) return KDN_ERR_NULL;
+    const void* ptrs[] = {q, k, v, log_alpha, omega, r, S0, p0, o, S_T, p_T, workspace,
+                          pk.beta, pk.alpha_p, pk.beta_p, pk.center};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return KDN_ERR_ALIGN;
     const WsLayout w = ws_layout(variant, B, T, H, dk, dv, chunk, io, flags);
@@ -105,7 +119,9 @@ kdn_status forward_impl(int variant, int B, int T, int H, int dk, int dv, int ch
 
     const Range in[] = {{q, ntok * dk * esz}, {k, ntok * dk * esz}, {v, ntok * dv * esz},
                         {log_alpha, ntok * dk * 4}, {omega, ntok * nu * 4}, {r, ntok * 4},
-                        {S0, BH * dk * dv * 4}, {p0, BH * nu * 4}};
+                        {S0, BH * dk * dv * 4}, {p0, BH * nu * 4},
+                        {pk.beta, ntok * 4}, {pk.alpha_p, ntok * 4}, {pk.beta_p, ntok * 4},
+                        {pk.center, (size_t)H * 4}};
     const Range ro = {o, ntok * dv * esz}, rs = {S_T, BH * dk * dv * 4}, rp = {p_T, BH * nu * 4};
     const Range rw = {workspace, w.total};
     for (const Range& x : in) {
@@ -129,6 +145,8 @@ kdn_status forward_impl(int variant, int B, int T, int H, int dk, int dv, int ch
     a.mu = mu < 0.f ? (float)dk : mu;
     a.io = io; a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.omega = omega; a.r = r;
     a.S0 = S0; a.p0 = p0; a.o = o; a.S_T = S_T; a.p_T = p_T; a.status = status;
+    a.beta = pk.beta; a.alpha_p = pk.alpha_p; a.beta_p = pk.beta_p; a.center = pk.center;
+    a.neg_log2x = -log2f(resolve_x(pk.x));
 
     cudaError_t e;
     if (T == 0) {
@@ -168,7 +186,7 @@ kdn_status kdn_diag_forward(int B, int T, int H, int dk, int dv, int chunk, floa
                             kdn_stream_t stream) {
     return forward_impl(KDN_DIAG, B, T, H, dk, dv, chunk, mu, io_dtype, flags, q, k, v,
                         log_alpha, omega, r, S0, p0, o, S_T, p_T, workspace, workspace_bytes,
-                        stream);
+                        stream, PkdaInputs{});
 }
 
 kdn_status kdn_iso_forward(int B, int T, int H, int dk, int dv, int chunk, float mu,
@@ -178,27 +196,49 @@ kdn_status kdn_iso_forward(int B, int T, int H, int dk, int dv, int chunk, float
                            float* p_T, void* workspace, size_t workspace_bytes,
                            kdn_stream_t stream) {
     return forward_impl(KDN_ISO, B, T, H, dk, dv, chunk, mu, io_dtype, flags, q, k, v, log_alpha,
-                        omega, r, S0, p0, o, S_T, p_T, workspace, workspace_bytes, stream);
+                        omega, r, S0, p0, o, S_T, p_T, workspace, workspace_bytes, stream,
+                        PkdaInputs{});
 }
 
-kdn_status kdn_step(int variant, int B, int H, int dk, int dv, float mu, int io_dtype,
-                    const void* q, const void* k, const void* v, const float* log_alpha,
-                    const float* omega, const float* r, float* S, float* p, void* o,
-                    void* workspace, size_t workspace_bytes, kdn_stream_t stream) {
+kdn_status kdn_pkda_forward(int B, int T, int H, int dk, int dv, int chunk, float x, int io_dtype,
+                            uint32_t flags, const void* q, const void* k, const void* v,
+                            const float* log_alpha, const float* beta, const float* alpha_p,
+                            const float* beta_p, const float* center, const float* S0,
+                            const float* A0, void* o, float* S_T, float* A_T, void* workspace,
+                            size_t workspace_bytes, kdn_stream_t stream) {
+    return forward_impl(KDN_PKDA, B, T, H, dk, dv, chunk, 0.f, io_dtype, flags, q, k, v, log_alpha,
+                        nullptr, nullptr, S0, A0, o, S_T, A_T, workspace, workspace_bytes, stream,
+                        PkdaInputs{beta, alpha_p, beta_p, center, x});
+}
+
+}  // extern "C"
+
+namespace {
+
+kdn_status step_impl(int variant, int B, int H, int dk, int dv, float mu, int io_dtype,
+                     const void* q, const void* k, const void* v, const float* log_alpha,
+                     const float* omega, const float* r, float* S, float* p, void* o,
+                     void* workspace, size_t workspace_bytes, kdn_stream_t stream,
+                     const PkdaInputs& pk) {
     kdn_status st = validate_common(variant, B, 1, H, dk, dv, 0, io_dtype);
     if (st != KDN_OK) return st;
     if (!workspace) return KDN_ERR_WORKSPACE;
     if (workspace_bytes < kStatusBytes) return KDN_ERR_WORKSPACE;
+    const bool is_pk = variant == KDN_PKDA;
     const size_t BH = (size_t)B * H;
-    if (BH > 0 && (!q || !k || !v || !log_alpha || !omega || !r || !S || !p || !o))
-        return KDN_ERR_NULL;
-    const void* ptrs[] = {q, k, v, log_alpha, omega, r, S, p, o, workspace};
+    if (BH > 0 && (!q || !k || !v || !log_alpha || !S || !p || !o)) return KDN_ERR_NULL;
+    if (BH > 0 && !is_pk && (!omega || !r)) return KDN_ERR_NULL;
+    if (BH > 0 && is_pk && (!pk.beta || !pk.alpha_p || !pk.beta_p || !pk.center)) return KDN_ERR_NULL;
+    const void* ptrs[] = {q, k, v, log_alpha, omega, r, S, p, o, workspace,
+                          pk.beta, pk.alpha_p, pk.beta_p, pk.center};
     for (const void* x : ptrs)
         if (x && !aligned16(x)) return KDN_ERR_ALIGN;
     const size_t esz = io_dtype == KDN_BF16 ? 2 : 4;
-    const size_t nu = variant == KDN_DIAG ? (size_t)dk : 1;
+    const size_t nu = variant == KDN_ISO ? 1 : (size_t)dk;
     const Range in[] = {{q, BH * dk * esz}, {k, BH * dk * esz}, {v, BH * dv * esz},
-                        {log_alpha, BH * dk * 4}, {omega, BH * nu * 4}, {r, BH * 4}};
+                        {log_alpha, BH * dk * 4}, {omega, BH * nu * 4}, {r, BH * 4},
+                        {pk.beta, BH * 4}, {pk.alpha_p, BH * 4}, {pk.beta_p, BH * 4},
+                        {pk.center, (size_t)H * 4}};
     const Range rs = {S, BH * dk * dv * 4}, rp = {p, BH * nu * 4}, ro = {o, BH * dv * esz};
     const Range rw = {workspace, kStatusBytes};
     for (const Range& x : in)
@@ -212,12 +252,37 @@ kdn_status kdn_step(int variant, int B, int H, int dk, int dv, float mu, int io_
     a.mu = mu < 0.f ? (float)dk : mu;
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.omega = omega; a.r = r;
     a.S = S; a.p = p; a.o = o; a.status = static_cast<uint32_t*>(workspace);
+    a.beta = pk.beta; a.alpha_p = pk.alpha_p; a.beta_p = pk.beta_p; a.center = pk.center;
+    a.neg_log2x = -log2f(resolve_x(pk.x));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (BH == 0) {
         return cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) == cudaSuccess ? KDN_OK
                                                                                   : KDN_ERR_CUDA;
     }
     return kdn::launch_step(a, s) == cudaSuccess ? KDN_OK : KDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kdn_status kdn_step(int variant, int B, int H, int dk, int dv, float mu, int io_dtype,
+                    const void* q, const void* k, const void* v, const float* log_alpha,
+                    const float* omega, const float* r, float* S, float* p, void* o,
+                    void* workspace, size_t workspace_bytes, kdn_stream_t stream) {
+    if (variant != KDN_DIAG && variant != KDN_ISO) return KDN_ERR_SHAPE;
+    return step_impl(variant, B, H, dk, dv, mu, io_dtype, q, k, v, log_alpha, omega, r, S, p, o,
+                     workspace, workspace_bytes, stream, PkdaInputs{});
+}
+
+kdn_status kdn_pkda_step(int B, int H, int dk, int dv, float x, int io_dtype, const void* q,
+                         const void* k, const void* v, const float* log_alpha, const float* beta,
+                         const float* alpha_p, const float* beta_p, const float* center, float* S,
+                         float* A, void* o, void* workspace, size_t workspace_bytes,
+                         kdn_stream_t stream) {
+    return step_impl(KDN_PKDA, B, H, dk, dv, 0.f, io_dtype, q, k, v, log_alpha, nullptr, nullptr, S,
+                     A, o, workspace, workspace_bytes, stream,
+                     PkdaInputs{beta, alpha_p, beta_p, center, x});
 }
 
 kdn_status kdn_read_device_status(const void* workspace, kdn_stream_t stream) {
@@ -256,6 +321,6 @@ const char* kdn_status_string(int status) {
     }
 }
 
-int kdn_abi_version(void) { return 100; }
+int kdn_abi_version(void) { return 101; }
 
 }  // extern "C"

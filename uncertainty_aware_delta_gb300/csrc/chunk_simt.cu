@@ -188,12 +188,12 @@ cudaError_t launch_chunk_t(const ForwardArgs& a, const float* kappa, cudaStream_
 
 __global__ void state_copy_kernel(const float* __restrict__ S0, const float* __restrict__ p0,
                                   float* __restrict__ S_T, float* __restrict__ p_T, size_t nS,
-                                  size_t np) {
+                                  size_t np, float p_default) {
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < nS; e += stride)
         S_T[e] = S0 ? S0[e] : 0.f;
     for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < np; e += stride)
-        p_T[e] = p0 ? p0[e] : 1.f;
+        p_T[e] = p0 ? p0[e] : p_default;
 }
 
 }  // namespace
@@ -205,11 +205,13 @@ cudaError_t launch_chunk_simt(const ForwardArgs& a, const float* kappa, cudaStre
 
 cudaError_t launch_state_copy(const ForwardArgs& a, cudaStream_t s) {
     const size_t nS = (size_t)a.B * a.H * a.dk * a.dv;
-    const size_t np = (size_t)a.B * a.H * (a.variant == 0 ? a.dk : 1);
+    // per-channel state for the diagonal variant and PKDA, one scalar for isotropic;
+    // defaults: variance 1 (KDN), key statistic 0 (PKDA)
+    const size_t np = (size_t)a.B * a.H * (a.variant == 1 ? 1 : a.dk);
     if (nS == 0) return cudaSuccess;
     int blocks = (int)((nS + 255) / 256);
     if (blocks > 4096) blocks = 4096;
-    state_copy_kernel<<<blocks, 256, 0, s>>>(a.S0, a.p0, a.S_T, a.p_T, nS, np);
+    state_copy_kernel<<<blocks, 256, 0, s>>>(a.S0, a.p0, a.S_T, a.p_T, nS, np, a.variant == 2 ? 0.f : 1.f);
     return cudaGetLastError();
 }
 

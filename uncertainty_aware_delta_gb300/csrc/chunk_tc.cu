@@ -99,7 +99,8 @@ constexpr int kLDX = 36;
 // small region, float offsets
 constexpr int SM_R = 0, SM_MUR = 64, SM_BHAT = 128, SM_ZP = 192, SM_AP = 448, SM_RZ = 704 /* [2][64] */,
               SM_FOUT = 832, SM_OMI = 960, SM_FLAG = 1024, SM_CF = 1032 /* [2][128] by chunk parity */,
-              SM_INVD = 1288, SM_FLOATS = 1352;
+              SM_INVD = 1288, SM_CF2 = 1352 /* [2][128] */, SM_SPLIT = 1608 /* [2][4] per warp of 4-7 */,
+              SM_FLOATS = 1616;
 constexpr uint32_t OFF_BAR = OFF_SMALL + SM_FLOATS * 4;
 constexpr uint32_t kSmemBytes = OFF_BAR + 80;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
@@ -120,14 +121,27 @@ struct TcParams {
     const float* la;
     const float* om_iso;
     const float* S0;
-    const float* p0;
+    const float* p0;      // initial variances (KDN) or key statistic (PKDA)
     __nv_bfloat16* o;
     float* S_T;
-    float* p_T;
+    float* p_T;           // final variances (KDN) or key statistic (PKDA)
     uint32_t* status;
+    // PKDA: write strength, statistic decay and weight per token-head, centre per head
+    const float* beta;
+    const float* alpha_p;
+    const float* beta_p;
+    const float* center;
     int T, H;
     float mu;
+    float neg_log2x;      // PKDA: -log2(x), x the bound of the write scale
 };
+
+// Kernel variants: the two KDN uncertainty models and the preconditioned delta
+// rule with per-channel decay.
+constexpr int kVarDiag = 0, kVarIso = 1, kVarPkda = 2;
+// PKDA: the statistic enters the logarithm no smaller than this.
+constexpr float kStatFloor = 1e-20f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // Lane L of a warp returns sum over lanes of v[L] (transpose-reduce, 31 shuffles).
 __device__ __forceinline__ float butterfly_sum32(float (&v)[32], int lane) {
@@ -264,8 +278,15 @@ __device__ __forceinline__ float ex2(float x) {   // 2^x, hardware approximation
     return y;
 }
 
-template <bool ISO>
+__device__ __forceinline__ float lg2(float x) {   // log2(x), hardware approximation
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int V>
 __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_constant__ TcParams P) {
+    constexpr bool ISO = V == kVarIso, PK = V == kVarPkda;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_addr(base);
@@ -303,8 +324,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         const int t0 = n * kC;
         mbar_expect_tx(bar_la, 32768u);
         tma_load_4d(sb + OFF_LA, &P.tla, 0, h, t0, b, bar_la);
-        mbar_expect_tx(bar_ko, ISO ? 16384u : 49152u);
-        if (!ISO) tma_load_4d(sb + OFF_OM, &P.tom, 0, h, t0, b, bar_ko);
+        mbar_expect_tx(bar_ko, V == kVarDiag ? 49152u : 16384u);
+        if (V == kVarDiag) tma_load_4d(sb + OFF_OM, &P.tom, 0, h, t0, b, bar_ko);
         tma_load_4d(sb + OFF_KIN, &P.tk, 0, h, t0, b, bar_ko);
         tma_load_4d(sb + OFF_KIN + 8192, &P.tk, 64, h, t0, b, bar_ko);
         mbar_expect_tx(bar_q, 16384u);
@@ -338,7 +359,11 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     float pn = 1.0f, pd = 1.0f;
     float pend2 = 0.0f;   // pending log2-factor of the previous chunk, (G_C - G_ref) log2(e) (warps 4-7)
     float b_iso = 1.0f;   // isotropic scalar variance (warp 4)
-    if (wg1 && !ISO && P.p0) pn = P.p0[static_cast<size_t>(bh) * kD + (tid - 128)];
+    // PKDA: key statistic of channel tid - 128 (warps 4-7), and the head's centre
+    float stat = 0.0f;
+    const float center = PK ? P.center[h] : 0.0f;
+    if (wg1 && V == kVarDiag && P.p0) pn = P.p0[static_cast<size_t>(bh) * kD + (tid - 128)];
+    if (wg1 && PK && P.p0) stat = P.p0[static_cast<size_t>(bh) * kD + (tid - 128)];
     if (ISO && warp == 4 && P.p0) b_iso = P.p0[bh];
     // initial state S^T into TMEM: lane j = value column, columns = key channel
     if (wg0) {
@@ -397,16 +422,31 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         const int t0c = c * kC, nvc = min(kC, T - t0c);
         if (tid < 128 + kC) {
             const int t = tid - 128;
-            float rr = 1.0f, om = 0.0f;
-            if (t < nvc) {
-                const size_t th = (static_cast<size_t>(b) * T + t0c + t) * H + h;
-                rr = P.r[th];
-                if (ISO) om = P.om_iso[th];
+            if (PK) {
+                // write strength, statistic weight and decay (rows past T leave the
+                // statistic unchanged and write nothing)
+                float be = 0.0f, bp = 0.0f, ap = 1.0f;
+                if (t < nvc) {
+                    const size_t th = (static_cast<size_t>(b) * T + t0c + t) * H + h;
+                    be = P.beta[th];
+                    bp = P.beta_p[th];
+                    ap = P.alpha_p[th];
+                }
+                sm[SM_R + t] = be;
+                sm[SM_MUR + t] = bp;
+                sm[SM_OMI + t] = ap;
+            } else {
+                float rr = 1.0f, om = 0.0f;
+                if (t < nvc) {
+                    const size_t th = (static_cast<size_t>(b) * T + t0c + t) * H + h;
+                    rr = P.r[th];
+                    if (ISO) om = P.om_iso[th];
+                }
+                sm[SM_R + t] = rr;
+                sm[SM_RZ + (c & 1) * 64 + t] = rr;
+                sm[SM_MUR + t] = P.mu / rr;
+                sm[SM_OMI + t] = om;
             }
-            sm[SM_R + t] = rr;
-            sm[SM_RZ + (c & 1) * 64 + t] = rr;
-            sm[SM_MUR + t] = P.mu / rr;
-            sm[SM_OMI + t] = om;
         }
         wait_or_abort(bar_la, ph_in);
         named_bar(kBarWG1, 128);
@@ -432,7 +472,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     const int t = tb + u;
                     la[u] = LA[t * kD + i];
                     kv[u] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(kin + sw128_off(t, kch)));
-                    om[u] = ISO ? 0.0f : OM[t * kD + i];
+                    om[u] = V == kVarDiag ? OM[t * kD + i] : 0.0f;
                 }
 #pragma unroll
                 for (int u4 = 0; u4 < 4; ++u4) {
@@ -447,7 +487,44 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 // Moebius matrix [[a^2, omega], [c a^2, 1 + c omega]] acting on (pn, pd):
                 // two independent multiply-adds per token, p_hat_t = pn_t / pd_{t-1}.
                 // Token-local factors are formed two tokens at a time (packed fp32 pairs).
-                if (!ISO) {
+                if (PK) {
+                    // key statistic A = alpha_p A + beta_p k^2 (this token included), then
+                    // the write scale exp(-log(x) s), s = softsign(log A - mu), times beta:
+                    // the coefficient of the write key (Preconditioned DeltaNet Eq. 9)
+                    float bp[16], ap[16], be[16];
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4) {
+                        const float4 b4 = *reinterpret_cast<const float4*>(sm + SM_MUR + tb + 4 * u4);
+                        const float4 a4 = *reinterpret_cast<const float4*>(sm + SM_OMI + tb + 4 * u4);
+                        const float4 w4 = *reinterpret_cast<const float4*>(sm + SM_R + tb + 4 * u4);
+                        bp[4 * u4 + 0] = b4.x; bp[4 * u4 + 1] = b4.y; bp[4 * u4 + 2] = b4.z; bp[4 * u4 + 3] = b4.w;
+                        ap[4 * u4 + 0] = a4.x; ap[4 * u4 + 1] = a4.y; ap[4 * u4 + 2] = a4.z; ap[4 * u4 + 3] = a4.w;
+                        be[4 * u4 + 0] = w4.x; be[4 * u4 + 1] = w4.y; be[4 * u4 + 2] = w4.z; be[4 * u4 + 3] = w4.w;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 16; u += 2) {
+                        const int t = tb + u;
+                        const float2 l2 = fmul2(make_float2(la[u], la[u + 1]), make_float2(kLog2e, kLog2e));
+                        g2 = fadd2(g2, l2);
+                        const float al0 = ex2(l2.x), al1 = ex2(l2.y);
+                        e1 *= al0;
+                        LA[t * kD + i] = e1;
+                        e1 *= al1;
+                        LA[(t + 1) * kD + i] = e1;
+                        const float2 kk = make_float2(kv[u], kv[u + 1]);
+                        const float2 bk = fmul2(make_float2(bp[u], bp[u + 1]), fmul2(kk, kk));
+                        const float A0 = fmaf(ap[u], stat, bk.x);
+                        const float A1 = fmaf(ap[u + 1], A0, bk.y);
+                        stat = A1;
+                        const float2 rho = ffma2(make_float2(lg2(fmaxf(A0, kStatFloor)), lg2(fmaxf(A1, kStatFloor))),
+                                                 make_float2(kLn2, kLn2), make_float2(-center, -center));
+                        const float2 sg = fmul2(rho, make_float2(rcp_approx(1.0f + fabsf(rho.x)),
+                                                                 rcp_approx(1.0f + fabsf(rho.y))));
+                        const float2 ex = fmul2(sg, make_float2(P.neg_log2x, P.neg_log2x));
+                        OM[t * kD + i] = be[u] * ex2(ex.x);
+                        OM[(t + 1) * kD + i] = be[u + 1] * ex2(ex.y);
+                    }
+                } else if (!ISO) {
 #pragma unroll
                     for (int u = 0; u < 16; u += 2) {
                         const int t = tb + u;
@@ -517,7 +594,15 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     LA[t * kD + i] = ex2(gg - R2);
                 }
             }
-            sm[SM_CF + (c & 1) * 128 + i] = ex2(pend2 + R2);
+            // The frame factor 2^(pend2 + R2) of the state: each part is at least
+            // 2^-116 (|G_C| <= 160), but after two strongly decaying chunks their sum
+            // can leave the normal range, and ex2.approx.ftz would flush it to zero.
+            // Such chunks keep the two parts apart and the state is scaled twice.
+            const bool split = pend2 + R2 < -120.0f;
+            sm[SM_CF + (c & 1) * 128 + i] = split ? ex2(pend2) : ex2(pend2 + R2);
+            sm[SM_CF2 + (c & 1) * 128 + i] = split ? ex2(R2) : 1.0f;
+            const unsigned any_split = __ballot_sync(0xffffffffu, split);
+            if (lane == 0) reinterpret_cast<int*>(sm)[SM_SPLIT + (c & 1) * 4 + w4] = any_split != 0u;
             pend2 = G2C - R2;
             sm[SM_FOUT + i] = ex2(pend2);
         }
@@ -601,6 +686,21 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     // its bf16 copy (A operand of the query and prediction MMA) in TMEM.
     auto scale_state = [&](int c) {
         tc_fence_after();
+        const int* sp = reinterpret_cast<const int*>(sm) + SM_SPLIT + (c & 1) * 4;
+        if ((sp[0] | sp[1] | sp[2] | sp[3]) != 0) {
+            // rare: a frame factor kept in two parts; apply the first one in its own pass
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + TM_S + 32 * q, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    r[e] = __float_as_uint(__uint_as_float(r[e]) * sm[SM_CF2 + (c & 1) * 128 + 32 * q + e]);
+                tmem_st32(lane_base + TM_S + 32 * q, r);
+            }
+            tmem_wait_st();
+        }
 #pragma unroll 1
         for (int q2 = 0; q2 < 2; ++q2) {
             uint32_t r0[32], r1[32], pk[32];
@@ -757,8 +857,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 uint32_t v0[32], v1[32];
                 tmem_ld64(TM_G, v0, v1);
                 if (lt < 64) {
-                    // M = diag(r) + lower_incl(K_bar K_til'^T): its diagonal is the gain
-                    // denominator z_t = r_t + sum_i p_hat_t,i k_t,i^2 (the decay factors cancel)
+                    // KDN: M = diag(r) + lower_incl(K_bar K_til'^T): its diagonal is the gain
+                    // denominator z_t = r_t + sum_i p_hat_t,i k_t,i^2 (the decay factors cancel).
+                    // PKDA: M = I + strict_lower(K_bar K_til^T) (the write key is not normalised).
                     float* row = LF + lt * kLDF;
 #pragma unroll
                     for (int c4 = 0; c4 < 16; ++c4) {
@@ -769,19 +870,24 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                                         __uint_as_float(s + 2 < 32 ? v0[s + 2] : v1[s + 2 - 32]),
                                         __uint_as_float(s + 3 < 32 ? v0[s + 3] : v1[s + 3 - 32]));
                     }
-                    // column lt of row lt: a 5-level select tree on the lane bits
-                    uint32_t x[32];
+                    if (PK) {
+                        row[lt] = 1.0f;
+                        sm[SM_INVD + lt] = 1.0f;
+                    } else {
+                        // column lt of row lt: a 5-level select tree on the lane bits
+                        uint32_t x[32];
 #pragma unroll
-                    for (int s = 0; s < 32; ++s) x[s] = lt < 32 ? v0[s] : v1[s];
+                        for (int s = 0; s < 32; ++s) x[s] = lt < 32 ? v0[s] : v1[s];
 #pragma unroll
-                    for (int lv = 0; lv < 5; ++lv) {
-                        const bool hi = (lane >> lv) & 1;
+                        for (int lv = 0; lv < 5; ++lv) {
+                            const bool hi = (lane >> lv) & 1;
 #pragma unroll
-                        for (int j = 0; j < (16 >> lv); ++j) x[j] = hi ? x[2 * j + 1] : x[2 * j];
+                            for (int j = 0; j < (16 >> lv); ++j) x[j] = hi ? x[2 * j + 1] : x[2 * j];
+                        }
+                        const float z = sm[SM_RZ + pb * 64 + lt] + __uint_as_float(x[0]);
+                        row[lt] = z;
+                        sm[SM_INVD + lt] = 1.0f / z;
                     }
-                    const float z = sm[SM_RZ + pb * 64 + lt] + __uint_as_float(x[0]);
-                    row[lt] = z;
-                    sm[SM_INVD + lt] = 1.0f / z;
                 } else {
                     const int t = lt - 64;
 #pragma unroll
@@ -978,7 +1084,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 }
             }
         } else if (wg1) {
-            if (!ISO) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = pn / pd;
+            if (V == kVarDiag) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = pn / pd;
+            else if (PK) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = stat;
             else if (tid == 128) P.p_T[bh] = b_iso;
         }
     }
@@ -1059,12 +1166,17 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t s) {
               encode_4d(&P.tk, a.k, BF, 2, a.B, a.T, a.H, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
               encode_4d(&P.tv, a.v, BF, 2, a.B, a.T, a.H, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
               encode_4d(&P.tla, a.log_alpha, F32, 4, a.B, a.T, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (ok && a.variant == 0)
+    if (ok && a.variant == kVarDiag)
         ok = encode_4d(&P.tom, a.omega, F32, 4, a.B, a.T, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return cudaErrorInvalidValue;
     P.r = a.r;
     P.la = a.log_alpha;
-    P.om_iso = a.variant == 1 ? a.omega : nullptr;
+    P.om_iso = a.variant == kVarIso ? a.omega : nullptr;
+    P.beta = a.beta;
+    P.alpha_p = a.alpha_p;
+    P.beta_p = a.beta_p;
+    P.center = a.center;
+    P.neg_log2x = a.neg_log2x;
     P.S0 = a.S0;
     P.p0 = a.p0;
     P.o = static_cast<__nv_bfloat16*>(a.o);
@@ -1075,17 +1187,15 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t s) {
     P.H = a.H;
     P.mu = a.mu;
     const int grid = a.B * a.H;
-    cudaError_t e;
-    if (a.variant == 0) {
-        e = cudaFuncSetAttribute(kdn_fused_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    auto launch = [&](auto kernel) {
+        const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
         if (e != cudaSuccess) return e;
-        kdn_fused_tc_kernel<false><<<grid, kNT, kSmemAlloc, s>>>(P);
-    } else {
-        e = cudaFuncSetAttribute(kdn_fused_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-        if (e != cudaSuccess) return e;
-        kdn_fused_tc_kernel<true><<<grid, kNT, kSmemAlloc, s>>>(P);
-    }
-    return cudaGetLastError();
+        kernel<<<grid, kNT, kSmemAlloc, s>>>(P);
+        return cudaGetLastError();
+    };
+    if (a.variant == kVarDiag) return launch(kdn_fused_tc_kernel<kVarDiag>);
+    if (a.variant == kVarIso) return launch(kdn_fused_tc_kernel<kVarIso>);
+    return launch(kdn_fused_tc_kernel<kVarPkda>);
 }
 
 }  // namespace kdn

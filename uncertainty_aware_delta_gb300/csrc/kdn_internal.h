@@ -8,15 +8,18 @@
 namespace kdn {
 
 struct ForwardArgs {
-    int variant;  // 0 diagonal, 1 isotropic
+    int variant;  // 0 diagonal, 1 isotropic, 2 PKDA (preconditioned delta rule)
     int B, T, H, dk, dv, chunk;
     float mu;
     int io;       // 0 fp32, 1 bf16
     const void *q, *k, *v;
-    const float *log_alpha, *omega, *r, *S0, *p0;
+    const float *log_alpha, *omega, *r, *S0, *p0;   // PKDA: p0 is the initial key statistic
     void* o;
-    float *S_T, *p_T;
+    float *S_T, *p_T;                               // PKDA: p_T is the final key statistic
     uint32_t* status;  // device status word
+    // PKDA only: beta, alpha_p, beta_p [B,T,H], center [H], -log2(x)
+    const float *beta, *alpha_p, *beta_p, *center;
+    float neg_log2x;
 };
 
 // Gain-scan workspace (CUDA-core path): gains and Moebius chunk summaries.
@@ -30,7 +33,8 @@ struct ScanWorkspace {
 
 constexpr int kGainChunk = 256;
 
-// Moebius 2x2 gain scan: writes kappa [B,T,H,dk] and p_T.  scan.cu
+// Moebius 2x2 gain scan (KDN), or the key-statistic scan and write keys
+// (PKDA): writes kappa [B,T,H,dk] and p_T.  scan.cu
 cudaError_t launch_gain_scan(const ForwardArgs& a, const ScanWorkspace& w, cudaStream_t s);
 
 // CUDA-core chunkwise memory pass (compact-WY/UT form, fp32 FFMA).  chunk_simt.cu
@@ -42,9 +46,11 @@ struct StepArgs {
     float mu;
     const void *q, *k, *v;
     const float *log_alpha, *omega, *r;
-    float *S, *p;
+    float *S, *p;       // PKDA: p is the key statistic
     void* o;
     uint32_t* status;
+    const float *beta, *alpha_p, *beta_p, *center;   // PKDA only
+    float neg_log2x;
 };
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 

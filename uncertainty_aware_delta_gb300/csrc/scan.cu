@@ -63,11 +63,11 @@ __global__ void mobius_summary_diag(const TIO* __restrict__ k, const float* __re
 }
 
 __global__ void mobius_carry(const float* __restrict__ summary, const float* __restrict__ p0,
-                             int BH, int nu, int nG, float* __restrict__ carry) {
+                             float p_default, int BH, int nu, int nG, float* __restrict__ carry) {
     const int e = blockIdx.x * blockDim.x + threadIdx.x;  // (bh, channel)
     if (e >= BH * nu) return;
     const int bh = e / nu, i = e % nu;
-    float p = p0 ? p0[e] : 1.0f;
+    float p = p0 ? p0[e] : p_default;
     for (int c = 0; c < nG; ++c) {
         const size_t idx = ((size_t)bh * nG + c) * nu + i;
         carry[idx] = p;
@@ -213,23 +213,81 @@ __global__ void gain_replay_iso(const TIO* __restrict__ k, const float* __restri
     }
 }
 
+// ---------------------------------------------------------------- PKDA
+// Preconditioned DeltaNet (Sec. 2.4 Eq. 9, Sec. 2.6): the per-channel key
+// statistic A_t = alpha_p_t A_{t-1} + beta_p_t k_t^2 is affine, i.e. the
+// Moebius matrix [[alpha_p, beta_p k^2], [0, 1]], so it rides the same three
+// phases; its chunk summary is (prod alpha_p, the chunk's decayed sum), the
+// pages' chunk formula for the statistic.  The replay emits the write keys
+//     kappa_t = beta_t exp(-log(x) softsign(log max(A_t, floor) - mu_h)) k_t.
+constexpr float kStatFloor = 1e-20f;
+
+template <typename TIO>
+__global__ void stat_summary_pkda(const TIO* __restrict__ k, const float* __restrict__ alpha_p,
+                                  const float* __restrict__ beta_p, int Tn, int H, int dk, int Cg,
+                                  int nG, float* __restrict__ summary) {
+    const int bh = blockIdx.x, c = blockIdx.y, b = bh / H, h = bh % H;
+    const int i = threadIdx.x;
+    if (i >= dk) return;
+    const int t0 = c * Cg, t1 = min(Tn, t0 + Cg);
+    float prod = 1.0f, acc = 0.0f;
+    for (int t = t0; t < t1; ++t) {
+        const size_t th = ((size_t)b * Tn + t) * H + h;
+        const float kv = IO<TIO>::load(k, th * dk + i);
+        const float ap = alpha_p[th];
+        acc = fmaf(ap, acc, beta_p[th] * kv * kv);
+        prod *= ap;
+    }
+    reinterpret_cast<float4*>(summary)[((size_t)bh * nG + c) * dk + i] = make_float4(prod, acc, 0.0f, 1.0f);
+}
+
+template <typename TIO>
+__global__ void gain_replay_pkda(const TIO* __restrict__ k, const float* __restrict__ beta,
+                                 const float* __restrict__ alpha_p, const float* __restrict__ beta_p,
+                                 const float* __restrict__ center, float neg_log2x,
+                                 const float* __restrict__ carry, int Tn, int H, int dk, int Cg,
+                                 int nG, float* __restrict__ kappa, float* __restrict__ A_T) {
+    const int bh = blockIdx.x, c = blockIdx.y, b = bh / H, h = bh % H;
+    const int i = threadIdx.x;
+    if (i >= dk) return;
+    float A = carry[((size_t)bh * nG + c) * dk + i];
+    const float mu = center[h];
+    const int t0 = c * Cg, t1 = min(Tn, t0 + Cg);
+    for (int t = t0; t < t1; ++t) {
+        const size_t th = ((size_t)b * Tn + t) * H + h;
+        const float kv = IO<TIO>::load(k, th * dk + i);
+        A = fmaf(alpha_p[th], A, beta_p[th] * kv * kv);
+        const float rho = logf(fmaxf(A, kStatFloor)) - mu;
+        const float sg = rho / (1.0f + fabsf(rho));
+        kappa[th * dk + i] = beta[th] * exp2f(neg_log2x * sg) * kv;
+    }
+    if (c == nG - 1) A_T[(size_t)bh * dk + i] = A;
+}
+
 template <typename TIO>
 cudaError_t launch_scan_t(const ForwardArgs& a, const ScanWorkspace& w, cudaStream_t s) {
     const TIO* k = static_cast<const TIO*>(a.k);
     const int BH = a.B * a.H, Cg = w.chunk_g, nG = w.n_chunks_g;
     const dim3 grid(BH, nG);
-    if (a.variant == 0) {
+    if (a.variant == 2) {
+        const int nt = ((a.dk + 31) / 32) * 32;
+        stat_summary_pkda<TIO><<<grid, nt, 0, s>>>(k, a.alpha_p, a.beta_p, a.T, a.H, a.dk, Cg, nG, w.summary);
+        const int tot = BH * a.dk;
+        mobius_carry<<<(tot + 127) / 128, 128, 0, s>>>(w.summary, a.p0, 0.0f, BH, a.dk, nG, w.carry);
+        gain_replay_pkda<TIO><<<grid, nt, 0, s>>>(k, a.beta, a.alpha_p, a.beta_p, a.center, a.neg_log2x,
+                                                  w.carry, a.T, a.H, a.dk, Cg, nG, w.kappa, a.p_T);
+    } else if (a.variant == 0) {
         const int nt = ((a.dk + 31) / 32) * 32;
         mobius_summary_diag<TIO><<<grid, nt, 0, s>>>(k, a.log_alpha, a.omega, a.r, a.T, a.H, a.dk,
                                                      a.mu, Cg, nG, w.summary);
         const int tot = BH * a.dk;
-        mobius_carry<<<(tot + 127) / 128, 128, 0, s>>>(w.summary, a.p0, BH, a.dk, nG, w.carry);
+        mobius_carry<<<(tot + 127) / 128, 128, 0, s>>>(w.summary, a.p0, 1.0f, BH, a.dk, nG, w.carry);
         gain_replay_diag<TIO><<<grid, nt, 0, s>>>(k, a.log_alpha, a.omega, a.r, w.carry, a.T, a.H,
                                                   a.dk, a.mu, Cg, nG, w.kappa, a.p_T);
     } else {
         mobius_summary_iso<TIO><<<grid, 128, 2 * Cg * sizeof(float), s>>>(
             k, a.log_alpha, a.omega, a.r, a.T, a.H, a.dk, a.mu, Cg, nG, w.summary);
-        mobius_carry<<<(BH + 127) / 128, 128, 0, s>>>(w.summary, a.p0, BH, 1, nG, w.carry);
+        mobius_carry<<<(BH + 127) / 128, 128, 0, s>>>(w.summary, a.p0, 1.0f, BH, 1, nG, w.carry);
         gain_replay_iso<TIO><<<grid, 128, 3 * Cg * sizeof(float), s>>>(
             k, a.log_alpha, a.omega, a.r, w.carry, a.T, a.H, a.dk, a.mu, Cg, nG, w.kappa, a.p_T);
     }

@@ -9,6 +9,9 @@
 //   S     = diag(a) S + kappa delta^T                         (Eq. 16)
 //   o     = S^T q = (diag(a) S)^T q + delta (kappa . q)       (Eq. 17, read after the write)
 //   p     = p_hat / (1 + (mu / r) k^2 p_hat)   (Isotropic: u = mu ||k||^2 / (d_k r))   (Eq. 60-65)
+// PKDA (Preconditioned DeltaNet Sec. 2.4 Eq. 9, Sec. 2.5) replaces the gain by
+// the write key of the preconditioned delta rule and p by the key statistic A:
+//   A = alpha_p A + beta_p k^2;  kappa = beta exp(-log(x) softsign(log A - mu_h)) k.
 // The two reductions over the key channel (with a*k and a*q) share one read
 // of S; the write pass reuses the values held in registers, so S crosses
 // HBM exactly once in each direction, with 128-bit accesses.
@@ -21,13 +24,16 @@ namespace {
 
 constexpr int kStepNT = 256;
 constexpr int kMaxRegF4 = 16;  // float4 of S per thread for d_k = d_v = 128
+constexpr float kStatFloor = 1e-20f;  // PKDA: the key statistic enters the logarithm no smaller
 
 template <typename TIO>
 __global__ void __launch_bounds__(kStepNT, 2)
 step_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TIO* __restrict__ v,
             const float* __restrict__ la, const float* __restrict__ om, const float* __restrict__ r,
             float* __restrict__ S, float* __restrict__ p, TIO* __restrict__ o, int variant, int DK,
-            int DV, float mu, uint32_t* status) {
+            int DV, float mu, uint32_t* status, const float* __restrict__ beta,
+            const float* __restrict__ alpha_p, const float* __restrict__ beta_p,
+            const float* __restrict__ center, float neg_log2x, int H) {
     __shared__ float s_a[128], s_ak[128], s_aq[128], s_kap[128];
     __shared__ float s_red[kStepNT / 32][4];
     // per-thread partial column sums: row groups x DV = (256 / (DV / 4)) * DV = 1024
@@ -49,7 +55,7 @@ step_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TIO* __r
         if (i < DK) reg[m] = S4[(size_t)i * NC4 + c4];
     }
     const size_t vec = (size_t)bh * DK;
-    const float rt = r[bh];
+    const float rt = variant == 2 ? 1.0f : r[bh];
 
     // -- gain (uses the predictive variance, before the mu-scaled update)
     float kv = 0.f, qv = 0.f, a = 0.f, a2 = 0.f, ph = 0.f;
@@ -63,7 +69,11 @@ step_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TIO* __r
         s_aq[tid] = a * qv;
     }
     float x0, x1, x2;
-    if (variant == 0) {
+    if (variant == 2) {
+        x0 = 0.f;            // no reductions: the write key is per channel
+        x1 = 0.f;
+        x2 = 0.f;
+    } else if (variant == 0) {
         if (tid < DK) ph = a2 * p[vec + tid] + om[vec + tid];
         x0 = ph * kv * kv;   // z
         x1 = 0.f;
@@ -83,7 +93,14 @@ step_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TIO* __r
     }
     __syncthreads();
     float kap = 0.f;
-    if (variant == 0) {
+    if (variant == 2) {
+        if (tid < DK) {
+            const float A = fmaf(alpha_p[bh], p[vec + tid], beta_p[bh] * kv * kv);
+            const float rho = logf(fmaxf(A, kStatFloor)) - center[bh % H];
+            kap = beta[bh] * exp2f(neg_log2x * (rho / (1.0f + fabsf(rho)))) * kv;
+            p[vec + tid] = A;
+        }
+    } else if (variant == 0) {
         const float z = s_scal[0];
         if (tid < DK) {
             kap = ph * kv / (rt + z);
@@ -93,8 +110,8 @@ step_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TIO* __r
     } else {
         const float abar = s_scal[0] / (float)DK, kn2 = s_scal[1];
         const float bhat = abar * p[bh] + om[bh];
-        const float beta = bhat / (rt + bhat * kn2);
-        if (tid < DK) kap = beta * kv;
+        const float gain = bhat / (rt + bhat * kn2);
+        if (tid < DK) kap = gain * kv;
         __syncthreads();  // every thread has read p[bh] before it is replaced
         if (tid == 0) {
             const float u = mu * kn2 / ((float)DK * rt);
@@ -164,16 +181,19 @@ step_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TIO* __r
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s) {
     const int BH = a.B * a.H;
     if (BH == 0) return cudaSuccess;
+    const int grid = BH;
     if (a.io == 1)
-        step_kernel<__nv_bfloat16><<<BH, kStepNT, 0, s>>>(
+        step_kernel<__nv_bfloat16><<<grid, kStepNT, 0, s>>>(
             static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
             static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.omega, a.r, a.S, a.p,
-            static_cast<__nv_bfloat16*>(a.o), a.variant, a.dk, a.dv, a.mu, a.status);
+            static_cast<__nv_bfloat16*>(a.o), a.variant, a.dk, a.dv, a.mu, a.status, a.beta,
+            a.alpha_p, a.beta_p, a.center, a.neg_log2x, a.H);
     else
-        step_kernel<float><<<BH, kStepNT, 0, s>>>(
+        step_kernel<float><<<grid, kStepNT, 0, s>>>(
             static_cast<const float*>(a.q), static_cast<const float*>(a.k),
             static_cast<const float*>(a.v), a.log_alpha, a.omega, a.r, a.S, a.p,
-            static_cast<float*>(a.o), a.variant, a.dk, a.dv, a.mu, a.status);
+            static_cast<float*>(a.o), a.variant, a.dk, a.dv, a.mu, a.status, a.beta, a.alpha_p,
+            a.beta_p, a.center, a.neg_log2x, a.H);
     return cudaGetLastError();
 }
 

@@ -17,6 +17,15 @@ then rounded fp32 -> bf16 (round to nearest even).  Every consumer, the oracle
 included, sees the rounded values.  The initial state is S_0 = 0, p_0 = 1
 unless a test passes one.
 
+PKDA (preconditioned delta rule, Preconditioned DeltaNet Sec. 2.4-2.5) draws
+q, k, v and log_alpha as above, then per (b, t, h)
+  beta       = sigmoid(N(0, 1))            write strength in (0, 1);
+  alpha_p    = exp(-U(lo, hi))             statistic decay (same range as log_alpha);
+  beta_p     = sigmoid(N(0, 1)) * scale    statistic weight (scale 1 unless a test
+                                           widens it to push log A above the centre);
+and per head center = exp(N(0, 0.5)) (the pages' positive log-space centre).
+The pages' models L2-normalise q and k (their architecture table), as here.
+
 The shapes follow the KDN paper's 750M/1.3B mixer layers (16 heads of width
 128, 4K training length; Sec. 5.1 and the Fig. 4 throughput setup); the pages
 measure mixer speed on such layers, not on a dataset, so no dataset is
@@ -32,7 +41,7 @@ import numpy as np
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    variant: str          # "diag" or "iso"
+    variant: str          # "diag", "iso" or "pkda"
     B: int
     H: int
     T: int
@@ -54,6 +63,7 @@ WORKLOADS = {
         Workload("diag-bf16-b1h16t65536d128", "diag", 1, 16, 65536, 128, 64, "bf16", (1e-4, 1e-2), 20260910),
         Workload("diag-decode-f32-s256h16d128", "diag", 256, 16, 512 + 1024, 128, 64, "f32", (1e-3, 0.1),
                  20260911, prefill=512, steps=1024),
+        Workload("pkda-bf16-b8h16t4096d128", "pkda", 8, 16, 4096, 128, 64, "bf16", (1e-3, 0.1), 20260912),
     ]
 }
 
@@ -103,12 +113,48 @@ def make_inputs(variant: str, B: int, T: int, H: int, dk: int, dv: int, io: str 
     return out
 
 
+def _sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def make_pkda_inputs(B: int, T: int, H: int, dk: int, dv: int, io: str = "f32", seed: int = 0,
+                     log_alpha_range=(1e-3, 0.1), beta_p_scale: float = 1.0):
+    """Draw one PKDA batch (recipe above); returns a dict of fp32 numpy arrays.
+
+    Keys: q, k [B,T,H,dk]; v [B,T,H,dv]; log_alpha [B,T,H,dk]; beta, alpha_p,
+    beta_p [B,T,H]; center [H]; plus "io".
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = {"io": io}
+
+    def store(x64):
+        x32 = x64.astype(np.float32)
+        return round_bf16(x32) if io == "bf16" else x32
+
+    for name in ("q", "k"):
+        x = rng.standard_normal((B, T, H, dk))
+        if dk > 0 and x.size:
+            x /= np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+        out[name] = store(x)
+        del x
+    out["v"] = store(rng.standard_normal((B, T, H, dv)))
+    lo, hi = log_alpha_range
+    out["log_alpha"] = (-rng.uniform(lo, hi, size=(B, T, H, dk))).astype(np.float32)
+    out["beta"] = _sigmoid(rng.standard_normal((B, T, H))).astype(np.float32)
+    out["alpha_p"] = np.exp(-rng.uniform(lo, hi, size=(B, T, H))).astype(np.float32)
+    out["beta_p"] = (_sigmoid(rng.standard_normal((B, T, H))) * beta_p_scale).astype(np.float32)
+    out["center"] = np.exp(0.5 * rng.standard_normal(H)).astype(np.float32)
+    return out
+
+
 def workload_inputs(w: Workload, variant: str | None = None):
     """Inputs of a named workload.  ``variant`` overrides the workload's own
     (the isotropic variant is also run on the diagonal workloads' shapes, with
     its own per-(b,t,h) omega drawn from the same seed).  For a decode
     workload this returns the prefill tokens only; see :func:`decode_step_inputs`."""
     T = w.prefill if w.steps else w.T
+    if (variant or w.variant) == "pkda":
+        return make_pkda_inputs(w.B, T, w.H, w.d, w.d, w.io, w.seed, w.log_alpha_range)
     return make_inputs(variant or w.variant, w.B, T, w.H, w.d, w.d, w.io, w.seed, w.log_alpha_range)
 
 
@@ -116,5 +162,7 @@ def decode_step_inputs(w: Workload, step: int, variant: str | None = None):
     """Inputs of decode step ``step`` (0-based) of a decode workload: one token
     per (sequence, head), drawn with the recipe above from seed
     ``w.seed * 4096 + 1 + step`` so any step can be regenerated on its own."""
+    if (variant or w.variant) == "pkda":
+        return make_pkda_inputs(w.B, 1, w.H, w.d, w.d, w.io, w.seed * 4096 + 1 + step, w.log_alpha_range)
     return make_inputs(variant or w.variant, w.B, 1, w.H, w.d, w.d, w.io, w.seed * 4096 + 1 + step,
                        w.log_alpha_range)
