@@ -27,7 +27,12 @@
 //       so z comes out of the Gram MMA.  T = M^{-1}: 16x16 diagonal blocks by
 //       forward substitution, merged 16 -> 32 -> 64 (tf32 mma.sync).
 //   G   state: S_m^T = S_in^T diag(e^{G_ref}) in TMEM, plus a bf16 copy in TMEM
-//       that is the A operand of the prediction/query MMA.
+//       that is the A operand of the prediction/query MMA.  The state is kept with
+//       the previous chunk's factor e^{G_C - G_ref} pending, so one factor
+//       e^{pending + G_ref} moves it into the frame; after two strongly decaying
+//       chunks that product can fall below fp32's normal range, and it is then
+//       applied in two parts (warps 4-7 apply e^{G_ref} once the state update of
+//       the previous chunk has landed).
 //   H   Delta'^T = (V^T - Z^T) T^T = V^T T^T + (-Z^T) T^T (-Z^T in bf16 in TMEM
 //       as an A operand).
 //   J   S^T += Delta'^T K_til' ; O^T += Delta'^T A'^T (issued at the start of
@@ -99,8 +104,7 @@ constexpr int kLDX = 36;
 // small region, float offsets
 constexpr int SM_R = 0, SM_MUR = 64, SM_BHAT = 128, SM_ZP = 192, SM_AP = 448, SM_RZ = 704 /* [2][64] */,
               SM_FOUT = 832, SM_OMI = 960, SM_FLAG = 1024, SM_CF = 1032 /* [2][128] by chunk parity */,
-              SM_INVD = 1288, SM_CF2 = 1352 /* [2][128] */, SM_SPLIT = 1608 /* [2][4] per warp of 4-7 */,
-              SM_FLOATS = 1616;
+              SM_INVD = 1288, SM_CF2 = 1352 /* [128] */, SM_FLOATS = 1480;
 constexpr uint32_t OFF_BAR = OFF_SMALL + SM_FLOATS * 4;
 constexpr uint32_t kSmemBytes = OFF_BAR + 80;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
@@ -284,6 +288,31 @@ __device__ __forceinline__ float lg2(float x) {   // log2(x), hardware approxima
     return y;
 }
 
+// Rare path, kept out of line: multiply this thread's TMEM row of the fp32 state
+// by per-channel factors f[0..127].
+__device__ __noinline__ void rescale_state_rows(uint32_t lane_base, const float* f) {
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + TM_S + 32 * q, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f[32 * q + e]);
+        tmem_st32(lane_base + TM_S + 32 * q, r);
+    }
+}
+
+// Named barrier over `nthreads` threads that also returns the OR of `pred` over them.
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, %2, %3, p; selp.u32 %0, 1, 0, q; }"
+        : "=r"(out)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return out != 0;
+}
+
 template <int V>
 __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_constant__ TcParams P) {
     constexpr bool ISO = V == kVarIso, PK = V == kVarPkda;
@@ -296,7 +325,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     // inputs of a chunk arrive on three barriers: log_alpha (bar_la), k and omega
     // (bar_ko), q (bar_q), in the order the passes need them
     const uint32_t bar_la = sb + OFF_BAR, bar_v = bar_la + 8, bar_mma = bar_la + 16, bar_o = bar_la + 24,
-                   bar_oj = bar_la + 32, bar_ops = bar_la + 40, bar_ko = bar_la + 48, bar_q = bar_la + 56;
+                   bar_oj = bar_la + 32, bar_ops = bar_la + 40, bar_ko = bar_la + 48, bar_q = bar_la + 56,
+                   bar_js = bar_la + 72;   // state update of a chunk (once per chunk, parity n & 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool wg0 = tid < 128, wg1 = tid >= 128 && tid < 256, wg2 = tid >= 256;
@@ -312,6 +342,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         mbar_init(bar_o, 1);
         mbar_init(bar_oj, 1);
         mbar_init(bar_ops, 1);
+        mbar_init(bar_js, 1);
         mbar_fence_init();
         *s_abort = 0;
     }
@@ -340,7 +371,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     __syncthreads();
     // copies and MMA commits issued so far (thread 0: v, MMAs; thread 256: the Gram MMAs;
     // thread 160: q, k, log_alpha, omega)
-    int n_in_issued = 0, n_v_issued = 0, n_mma_issued = 0, n_o_issued = 0, n_oj_issued = 0, n_gram_issued = 0;
+    int n_in_issued = 0, n_v_issued = 0, n_mma_issued = 0, n_o_issued = 0, n_oj_issued = 0, n_gram_issued = 0,
+        n_js_issued = 0;
     if (tid == 0 && nchunks > 0) {
         issue_v(0);
         n_v_issued = 1;
@@ -418,7 +450,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     // Runs one chunk ahead of the memory pass.  Rows past the end of the sequence
     // arrive as zeros (TMA fill): log_alpha = omega = k = 0 leaves the variance and
     // the decay factor unchanged and zeroes those rows' operands.
-    auto prep_gains = [&](int c) {
+    // Returns true when this channel's frame factor for chunk c is kept in two parts.
+    auto prep_gains = [&](int c) -> bool {
+        bool split = false;
         const int t0c = c * kC, nvc = min(kC, T - t0c);
         if (tid < 128 + kC) {
             const int t = tid - 128;
@@ -597,12 +631,11 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             // The frame factor 2^(pend2 + R2) of the state: each part is at least
             // 2^-116 (|G_C| <= 160), but after two strongly decaying chunks their sum
             // can leave the normal range, and ex2.approx.ftz would flush it to zero.
-            // Such chunks keep the two parts apart and the state is scaled twice.
-            const bool split = pend2 + R2 < -120.0f;
+            // Such chunks keep the two parts apart and the state is scaled twice
+            // (2^pend2 brings it to its true scale, 2^R2 into the chunk's frame).
+            split = pend2 + R2 < -120.0f;
             sm[SM_CF + (c & 1) * 128 + i] = split ? ex2(pend2) : ex2(pend2 + R2);
-            sm[SM_CF2 + (c & 1) * 128 + i] = split ? ex2(R2) : 1.0f;
-            const unsigned any_split = __ballot_sync(0xffffffffu, split);
-            if (lane == 0) reinterpret_cast<int*>(sm)[SM_SPLIT + (c & 1) * 4 + w4] = any_split != 0u;
+            sm[SM_CF2 + i] = ex2(R2);
             pend2 = G2C - R2;
             sm[SM_FOUT + i] = ex2(pend2);
         }
@@ -660,6 +693,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 b_iso = __shfl_sync(0xffffffffu, bb, 31);
             }
         }
+        return split;
     };
 
     // ------------------------------------------------------------------ warps 0-3
@@ -686,21 +720,6 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     // its bf16 copy (A operand of the query and prediction MMA) in TMEM.
     auto scale_state = [&](int c) {
         tc_fence_after();
-        const int* sp = reinterpret_cast<const int*>(sm) + SM_SPLIT + (c & 1) * 4;
-        if ((sp[0] | sp[1] | sp[2] | sp[3]) != 0) {
-            // rare: a frame factor kept in two parts; apply the first one in its own pass
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + TM_S + 32 * q, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    r[e] = __float_as_uint(__uint_as_float(r[e]) * sm[SM_CF2 + (c & 1) * 128 + 32 * q + e]);
-                tmem_st32(lane_base + TM_S + 32 * q, r);
-            }
-            tmem_wait_st();
-        }
 #pragma unroll 1
         for (int q2 = 0; q2 < 2; ++q2) {
             uint32_t r0[32], r1[32], pk[32];
@@ -742,7 +761,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         ++n_oj_issued;
     };
 
-    if (wg1 && nchunks > 0) prep_gains(0);
+    if (wg1 && nchunks > 0) prep_gains(0);   // chunk 0 never splits: pend2 = 0
     ph_in ^= 1u;
     tc_fence_before();
     __syncthreads();
@@ -1045,11 +1064,24 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     mma_bf16_tmem_a(tmem + TM_S, tmem + TM_DB + 8 * ks, sw128_desc(sb + OFF_KT + ks * 2048, 8192, 1024),
                                     id_s, 1u);
                 mma_commit(bar_mma);
+                mma_commit(bar_js);
                 ++n_mma_issued;
+                ++n_js_issued;
             }
         } else if (n + 1 < nchunks) {
             // ---- warps 4-7: gains of chunk n + 1
-            prep_gains(n + 1);
+            const bool split = prep_gains(n + 1);
+            if (bar_red_or(kBarWG1, 128, split)) {
+                // rare: some channel's frame factor for chunk n + 1 is kept in two parts;
+                // once this chunk's state update has landed, these warps (the same TMEM
+                // lanes) apply the second part; the first comes with the next chunk's
+                // scaling, after the barrier that ends this chunk
+                wait_or_abort(bar_js, pb);
+                tc_fence_after();
+                rescale_state_rows(lane_base, sm + SM_CF2);
+                tmem_wait_st();
+                tc_fence_before();
+            }
         }
         if (n + 1 < nchunks) ph_in ^= 1u;
         // the next chunk starts from the updated state (and overwrites K_til')
@@ -1101,6 +1133,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             if (n_o_issued > 0) mbar_wait(bar_o, (n_o_issued - 1) & 1, kWaitLimit);
             if (n_oj_issued > 0) mbar_wait(bar_oj, (n_oj_issued - 1) & 1, kWaitLimit);
             if (n_v_issued > 0) mbar_wait(bar_v, (n_v_issued - 1) & 1, kWaitLimit);
+            if (n_js_issued > 0) mbar_wait(bar_js, (n_js_issued - 1) & 1, kWaitLimit);
         }
         if (tid == 160 && n_in_issued > 0) {
             mbar_wait(bar_la, (n_in_issued - 1) & 1, kWaitLimit);
