@@ -234,34 +234,44 @@ def traffic_for(kernel, workload):
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f).get(kernel)
-    except (OSError, ValueError):
+            recs = json.load(f).get("records", [])
+    except (OSError, ValueError, AttributeError):
         return None
-    if not rec or rec.get("workload") != workload:
-        return None
-    src = os.path.join(ROOT, rec["source"])
-    try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    except OSError:
-        return None
-    return rec["bytes_per_launch"] if sha == rec.get("source_sha256") else None
+    for rec in recs:
+        if rec.get("kernel") != kernel or rec.get("workload") != workload:
+            continue
+        src = os.path.join(ROOT, rec["source"])
+        try:
+            sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        except OSError:
+            return None
+        return rec["bytes_per_launch"] if sha == rec.get("source_sha256") else None
+    return None
 
 
 # ----------------------------------------------------------------- CPU oracle
+PKDA_NAMES = ("q", "k", "v", "log_alpha", "beta", "alpha_p", "beta_p", "center")
+
+
 def oracle_tokens_per_s(x_host, variant, tokens, nthreads=0):
     import oracle
 
-    sl = {n: np.ascontiguousarray(v[:, :tokens]) for n, v in x_host.items()}
+    sl = {n: np.ascontiguousarray(v[:, :tokens] if v.ndim > 1 else v) for n, v in x_host.items()}
     t0 = time.perf_counter()
-    oracle.forward(variant, sl["q"], sl["k"], sl["v"], sl["log_alpha"], sl["omega"], sl["r"],
-                   nthreads=nthreads)
+    if variant == "pkda":
+        oracle.recurrence.pkda_forward(*(sl[n] for n in PKDA_NAMES[:5]), alpha_p=sl["alpha_p"],
+                                       beta_p=sl["beta_p"], center=sl["center"], nthreads=nthreads)
+    else:
+        oracle.forward(variant, sl["q"], sl["k"], sl["v"], sl["log_alpha"], sl["omega"], sl["r"],
+                       nthreads=nthreads)
     dt = time.perf_counter() - t0
     B = sl["q"].shape[0]
     return B * tokens / dt, dt
 
 
 def host_sample(torch, x, tokens):
-    return {n: v[:, :tokens].float().cpu().numpy().astype(np.float64) for n, v in x.items()}
+    return {n: (v[:, :tokens] if v.dim() > 1 else v).float().cpu().numpy().astype(np.float64)
+            for n, v in x.items()}
 
 
 def run_reference(args):
@@ -276,7 +286,11 @@ def run_reference(args):
     oracle.build_oracle()
     w = WORKLOADS[args.workload]
     tokens = min(w.T, 256)
-    x = device_inputs(torch, w, w.variant, w.seed, "cpu", T=tokens)
+    if w.variant == "pkda":
+        x = device_pkda_inputs(torch, w, w.seed, "cpu")
+        x = {n: (v[:, :tokens] if v.dim() > 1 else v) for n, v in x.items()}
+    else:
+        x = device_inputs(torch, w, w.variant, w.seed, "cpu", T=tokens)
     xh = {n: v.float().numpy().astype(np.float64) for n, v in x.items()}
     cores = oracle.recurrence.default_threads()
     for _ in range(args.warmup):
@@ -334,22 +348,31 @@ def main():
     peaks, peak_src = load_peaks()
     w = WORKLOADS[args.workload]
     variant = w.variant
-    fwd = kdn.kdn_diag_forward if variant == "diag" else kdn.kdn_iso_forward
-    vcode = kdn.KDN_DIAG if variant == "diag" else kdn.KDN_ISO
+    vcode = {"diag": kdn.KDN_DIAG, "iso": kdn.KDN_ISO, "pkda": kdn.KDN_PKDA}[variant]
     io = kdn.KDN_BF16 if w.io == "bf16" else kdn.KDN_F32
-    x = device_inputs(torch, w, variant, w.seed + 7919 * rank, device)
+    if variant == "pkda":
+        x = device_pkda_inputs(torch, w, w.seed + 7919 * rank, device)
+
+        def fwd(xx, out, ws):
+            return kdn.kdn_pkda_forward(*(xx[n] for n in PKDA_NAMES), chunk=w.chunk, out=out, workspace=ws)
+    else:
+        x = device_inputs(torch, w, variant, w.seed + 7919 * rank, device)
+        fwd_kdn = kdn.kdn_diag_forward if variant == "diag" else kdn.kdn_iso_forward
+
+        def fwd(xx, out, ws):
+            return fwd_kdn(xx["q"], xx["k"], xx["v"], xx["log_alpha"], xx["omega"], xx["r"], chunk=w.chunk,
+                           out=out, workspace=ws)
     nkern = kdn.forward_kernel_count(vcode, w.B, w.T, w.H, w.d, w.d, w.chunk, io, 0)
     tc_path = nkern == 1
     ws = torch.empty(kdn.workspace_size(vcode, w.B, w.T, w.H, w.d, w.d, w.chunk, io, 0),
                      dtype=torch.uint8, device=device)
     o = torch.empty(w.B, w.T, w.H, w.d, dtype=x["q"].dtype, device=device)
     S_T = torch.empty(w.B, w.H, w.d, w.d, dtype=torch.float32, device=device)
-    p_T = torch.empty((w.B, w.H, w.d) if variant == "diag" else (w.B, w.H), dtype=torch.float32,
+    p_T = torch.empty((w.B, w.H) if variant == "iso" else (w.B, w.H, w.d), dtype=torch.float32,
                       device=device)
 
     def step():
-        fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"], chunk=w.chunk,
-            out=(o, S_T, p_T), workspace=ws)
+        fwd(x, (o, S_T, p_T), ws)
 
     if args.profile:
         time_calls(torch, step, args.steps, args.warmup, barrier)
@@ -367,7 +390,10 @@ def main():
     value = aggregate_tokens_per_s(tokens, ms, world)
 
     # ---- roofline of the dominant kernel (whole step when it is one kernel)
-    abytes = algorithmic_bytes(w.B, w.T, w.H, w.d, w.d, w.io, variant)
+    if variant == "pkda":
+        abytes = pkda_algorithmic_bytes(w.B, w.T, w.H, w.d, w.d, w.io)
+    else:
+        abytes = algorithmic_bytes(w.B, w.T, w.H, w.d, w.d, w.io, variant)
     aflops = algorithmic_flops(w.B, w.T, w.H, w.d, w.d, w.chunk)
     hbm = float(peaks["hbm_gbs"])
     achieved = abytes / (ms / 1e3) / 1e9
@@ -392,8 +418,7 @@ def main():
     def e2e_step():
         for n in dx:
             dx[n].copy_(hx[n], non_blocking=True)
-        fwd(dx["q"], dx["k"], dx["v"], dx["log_alpha"], dx["omega"], dx["r"], chunk=w.chunk,
-            out=(o, S_T, p_T), workspace=ws)
+        fwd(dx, (o, S_T, p_T), ws)
         ho.copy_(o, non_blocking=True)
         hS.copy_(S_T, non_blocking=True)
         hp.copy_(p_T, non_blocking=True)
@@ -430,8 +455,10 @@ def main():
         "dtype": "bf16" if tc_path else "f32",
         "data": "synthetic",
         "config": {
-            "workload": w.name, "variant": "diagonal" if variant == "diag" else "isotropic",
-            "B": w.B, "H": w.H, "T": w.T, "d_k": w.d, "d_v": w.d, "chunk": w.chunk, "mu": w.d,
+            "workload": w.name,
+            "variant": {"diag": "diagonal", "iso": "isotropic", "pkda": "pkda (preconditioned delta rule)"}[variant],
+            "B": w.B, "H": w.H, "T": w.T, "d_k": w.d, "d_v": w.d, "chunk": w.chunk,
+            **({"x": 1.5} if variant == "pkda" else {"mu": w.d}),
             "io": w.io, "state": "fp32",
             "path": "tensor-core (tcgen05, fused)" if tc_path else "cuda-core (gain scan + FFMA chunk pass)",
             "l2": f"no flush: the inputs ({abytes / 1e9:.2f} GB per step) are larger than L2 (129 MB)",

@@ -70,3 +70,11 @@ def test_max_over_two_gloo_ranks():
         assert p.exitcode == 0
     assert [r[1] for r in res] == [15.0, 15.0]              # slowest rank's ms on every rank
     assert res[0][2] == pytest.approx(2 * 1000 / 0.015)      # all ranks' tokens / slowest time
+
+
+def test_reference_arm_pkda_workload():
+    r = _bench(["--impl", "reference", "--steps", "1", "--warmup", "0", "--workload", "pkda-bf16-b8h16t4096d128"])
+    assert r.returncode == 0, r.stderr
+    d = json.loads([l for l in r.stdout.splitlines() if l.strip()][0])
+    assert d["impl"] == "reference" and d["value"] > 0
+    assert d["config"]["workload"] == "pkda-bf16-b8h16t4096d128"
