@@ -207,14 +207,17 @@ def test_pkda_full_size_sampled():
         assert e[0] <= tol(w.io) and e[1] <= tol(w.io) and e[2] <= 1e-4, (b, h, e)
 
 
-@pytest.mark.parametrize("case", [(3, 2, 128, 128, "f32"), (2, 3, 16, 64, "f32"), (2, 2, 128, 128, "bf16")],
+@pytest.mark.parametrize("case", [(3, 2, 128, 128, "f32"), (2, 3, 16, 64, "f32"), (2, 2, 128, 128, "bf16"),
+                                  # more (sequence, head) pairs than SMs: each persistent CTA of the
+                                  # 128 x 128 decode walks several heads through its buffer ring
+                                  (100, 4, 128, 128, "f32"), (80, 5, 128, 128, "bf16")],
                          ids=lambda c: "-".join(map(str, c)))
 def test_pkda_steps_after_prefill(case):
     import torch
 
     B, H, dk, dv, io = case
     kdn = _kdn()
-    prefill, steps = 40, 12
+    prefill, steps = (40, 12) if B * H < 100 else (8, 3)
     x = make_pkda_inputs(B, prefill + steps, H, dk, dv, io=io, seed=88 + dk)
     t = _dev(x)
     pre = {n: (v[:, :prefill].contiguous() if n != "center" else v) for n, v in t.items()}

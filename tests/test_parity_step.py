@@ -41,14 +41,18 @@ def _prefill_then_steps(kdn, variant, x, prefill, steps, chunk=64, check_every=1
 
 
 CASES = [("diag", 3, 2, 128, 128, "f32"), ("iso", 3, 2, 128, 128, "f32"), ("diag", 2, 3, 16, 64, "f32"),
-         ("iso", 2, 2, 64, 32, "f32"), ("diag", 2, 2, 128, 128, "bf16"), ("iso", 2, 2, 32, 128, "bf16")]
+         ("iso", 2, 2, 64, 32, "f32"), ("diag", 2, 2, 128, 128, "bf16"), ("iso", 2, 2, 32, 128, "bf16"),
+         # more (sequence, head) pairs than SMs: each persistent CTA of the 128 x 128
+         # decode walks several heads through its buffer ring
+         ("diag", 100, 4, 128, 128, "f32"), ("iso", 100, 4, 128, 128, "f32"),
+         ("diag", 80, 5, 128, 128, "bf16"), ("iso", 80, 5, 128, 128, "bf16")]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
 def test_steps_after_prefill(case):
     variant, B, H, dk, dv, io = case
     kdn = _kdn()
-    prefill, steps = 40, 12
+    prefill, steps = (40, 12) if B * H < 100 else (8, 3)
     x = make_inputs(variant, B, prefill + steps, H, dk, dv, io=io, seed=77 + dk)
     o, S, p = _prefill_then_steps(kdn, variant, x, prefill, steps, chunk=16)
     ref = oracle.forward(variant, x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"])

@@ -123,7 +123,7 @@ struct TcParams {
     CUtensorMap tq, tk, tv, tla, tom;
     const float* r;
     const float* la;
-    const float* om_iso;
+    const float* om;      // omega: per channel (diagonal) or per token-head (isotropic)
     const float* S0;
     const float* p0;      // initial variances (KDN) or key statistic (PKDA)
     __nv_bfloat16* o;
@@ -313,6 +313,59 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
     return out != 0;
 }
 
+// Rare path, kept out of line: a channel whose chunk log-decay exceeds
+// kStartRefLogDecay gets its factors e^{G_t - G_ref} and K_til' scales
+// (p_hat / e1, 1 / e1 or the PKDA write scale / e1) rewritten with the mid-chunk
+// reference G_ref = G_C / 2 (R2 in log2 units), from log_alpha (and omega) in
+// global memory and the chunk-start carries, re-running the chunk's recurrence.
+template <int V>
+__device__ __noinline__ void strong_decay_factors(const TcParams& P, unsigned char* base, int i, int b, int h,
+                                                  int t0c, int nvc, float R2, float pns, float pds, float sts,
+                                                  float center) {
+    constexpr bool ISO = V == kVarIso;
+    const int T = P.T, H = P.H;
+    float* LA = reinterpret_cast<float*>(base + OFF_LA);
+    float* OM = reinterpret_cast<float*>(base + OFF_OM);
+    const float* sm = reinterpret_cast<const float*>(base + OFF_SMALL);
+    float gg = 0.0f;
+    const size_t g0 = (static_cast<size_t>(b) * T + t0c) * H * kD + static_cast<size_t>(h) * kD + i;
+    const unsigned char* kin = base + OFF_KIN + (i >> 6) * 8192 + (i & 7) * 2;
+    const int kch = (i & 63) >> 3;
+#pragma unroll 1
+    for (int t = 0; t < kC; ++t) {
+        const size_t e = g0 + static_cast<size_t>(t) * H * kD;
+        const float l2 = t < nvc ? P.la[e] * kLog2e : 0.0f;
+        gg += l2;
+        const float kx = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(kin + sw128_off(t, kch)));
+        LA[t * kD + i] = ex2(gg - R2);
+        float kp;
+        if (V == kVarDiag) {
+            const float ox = t < nvc ? P.om[e] : 0.0f;
+            const float al = ex2(l2), a2 = al * al, cc = sm[SM_MUR + t] * kx * kx;
+            const float nn = fmaf(a2, pns, ox * pds);
+            const float dd = fmaf(cc * a2, pns, fmaf(cc, ox, 1.0f) * pds);
+            kp = nn * rcp_approx(pds) * ex2(R2 - gg);
+            pns = nn;
+            pds = dd;
+            if ((t & 3) == 3) {
+                const int ex = min((__float_as_int(pds) >> 23) & 0xff, 253);
+                const float sc = __int_as_float((254 - ex) << 23);
+                pns *= sc;
+                pds *= sc;
+            }
+        } else if (ISO) {
+            kp = ex2(R2 - gg);
+        } else {
+            const float A = fmaf(sm[SM_OMI + t], sts, sm[SM_MUR + t] * kx * kx);
+            sts = A;
+            const float rho = fmaf(lg2(fmaxf(A, kStatFloor)), kLn2, -center);
+            const float sg = rho * rcp_approx(1.0f + fabsf(rho));
+            kp = sm[SM_R + t] * ex2(fmaf(sg, P.neg_log2x, R2 - gg));
+        }
+        OM[t * kD + i] = kp;
+    }
+}
+
 template <int V>
 __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_constant__ TcParams P) {
     constexpr bool ISO = V == kVarIso, PK = V == kVarPkda;
@@ -474,7 +527,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 if (t < nvc) {
                     const size_t th = (static_cast<size_t>(b) * T + t0c + t) * H + h;
                     rr = P.r[th];
-                    if (ISO) om = P.om_iso[th];
+                    if (ISO) om = P.om[th];
                 }
                 sm[SM_R + t] = rr;
                 sm[SM_RZ + (c & 1) * 64 + t] = rr;
@@ -487,7 +540,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         const int i = tid - 128, w4 = warp - 4;
         wait_or_abort(bar_ko, ph_in);   // k and omega of chunk c
         // decay factors relative to the chunk start (reference checked after the chunk)
-        float e1 = 1.0f;
+        const float pn0 = pn, pd0 = pd, stat0 = stat;
+        float e1 = 1.0f, gr = 0.0f;   // e^{G_t}, and G_t log2(e) (PKDA)
         float2 g2 = make_float2(0.0f, 0.0f);   // chunk log-decay, log2 units, two partial sums
         const unsigned char* kin = base + OFF_KIN + (i >> 6) * 8192 + (i & 7) * 2;
         const int kch = (i & 63) >> 3;
@@ -539,7 +593,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     for (int u = 0; u < 16; u += 2) {
                         const int t = tb + u;
                         const float2 l2 = fmul2(make_float2(la[u], la[u + 1]), make_float2(kLog2e, kLog2e));
-                        g2 = fadd2(g2, l2);
+                        const float gr0 = gr + l2.x, gr1 = gr0 + l2.y;
+                        gr = gr1;
                         const float al0 = ex2(l2.x), al1 = ex2(l2.y);
                         e1 *= al0;
                         LA[t * kD + i] = e1;
@@ -554,7 +609,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                                                  make_float2(kLn2, kLn2), make_float2(-center, -center));
                         const float2 sg = fmul2(rho, make_float2(rcp_approx(1.0f + fabsf(rho.x)),
                                                                  rcp_approx(1.0f + fabsf(rho.y))));
-                        const float2 ex = fmul2(sg, make_float2(P.neg_log2x, P.neg_log2x));
+                        // divided by the decay factor e1 = 2^{G_t log2 e} (the operand pass
+                        // multiplies k by this directly)
+                        const float2 ex = ffma2(sg, make_float2(P.neg_log2x, P.neg_log2x), make_float2(-gr0, -gr1));
                         OM[t * kD + i] = be[u] * ex2(ex.x);
                         OM[(t + 1) * kD + i] = be[u + 1] * ex2(ex.y);
                     }
@@ -572,15 +629,15 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                         const float2 ee = ffma2(cc, make_float2(om[u], om[u + 1]), make_float2(1.0f, 1.0f));
                         e1 *= al0;
                         LA[t * kD + i] = e1;
-                        float rd = rcp_approx(pd);
+                        float rd = rcp_approx(pd * e1);
                         float2 nd = ffma2(make_float2(a2.x, ca2.x), make_float2(pn, pn),
                                           fmul2(make_float2(om[u], ee.x), make_float2(pd, pd)));
-                        OM[t * kD + i] = nd.x * rd;   // p_hat_t
+                        OM[t * kD + i] = nd.x * rd;   // p_hat_t / e1_t
                         pn = nd.x;
                         pd = nd.y;
                         e1 *= al1;
                         LA[(t + 1) * kD + i] = e1;
-                        rd = rcp_approx(pd);
+                        rd = rcp_approx(pd * e1);
                         nd = ffma2(make_float2(a2.y, ca2.y), make_float2(pn, pn),
                                    fmul2(make_float2(om[u + 1], ee.y), make_float2(pd, pd)));
                         OM[(t + 1) * kD + i] = nd.x * rd;
@@ -613,20 +670,15 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             }
         }
         {
-            const float G2C = g2.x + g2.y;
+            const float G2C = PK ? gr : g2.x + g2.y;
             if (!(fabsf(G2C) <= kMaxChunkLogDecay * kLog2e)) set_status(P.status, kStatusRange);
             float R2 = 0.0f;
             if (fabsf(G2C) > kStartRefLogDecay * kLog2e) {
                 // rare: strong decay in this channel, recompute its factors with G_ref = G_C / 2
-                // from log_alpha in global memory (the tile now holds the factors)
+                // from log_alpha (and omega) in global memory (the tiles now hold the
+                // factors), re-running the variance (statistic) recurrence of the chunk
                 R2 = 0.5f * G2C;
-                float gg = 0.0f;
-                const float* lag = P.la + (static_cast<size_t>(b) * T + t0c) * H * kD + static_cast<size_t>(h) * kD + i;
-#pragma unroll 4
-                for (int t = 0; t < kC; ++t) {
-                    if (t < nvc) gg += lag[static_cast<size_t>(t) * H * kD] * kLog2e;
-                    LA[t * kD + i] = ex2(gg - R2);
-                }
+                strong_decay_factors<V>(P, base, i, b, h, t0c, nvc, R2, pn0, pd0, stat0, center);
             }
             // The frame factor 2^(pend2 + R2) of the state: each part is at least
             // 2^-116 (|G_C| <= 160), but after two strongly decaying chunks their sum
@@ -724,18 +776,19 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         for (int q2 = 0; q2 < 2; ++q2) {
             uint32_t r0[32], r1[32], pk[32];
             tmem_ld64(TM_S + 64 * q2, r0, r1);
+            // (two channels per packed multiply)
+            auto scale4 = [](uint32_t* r, const float4 f) {
+                const float2 a = fmul2(make_float2(__uint_as_float(r[0]), __uint_as_float(r[1])), make_float2(f.x, f.y));
+                const float2 b = fmul2(make_float2(__uint_as_float(r[2]), __uint_as_float(r[3])), make_float2(f.z, f.w));
+                r[0] = __float_as_uint(a.x);
+                r[1] = __float_as_uint(a.y);
+                r[2] = __float_as_uint(b.x);
+                r[3] = __float_as_uint(b.y);
+            };
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
-                const float4 f = *reinterpret_cast<const float4*>(sm + SM_CF + (c & 1) * 128 + 64 * q2 + 4 * c4);
-                r0[4 * c4 + 0] = __float_as_uint(__uint_as_float(r0[4 * c4 + 0]) * f.x);
-                r0[4 * c4 + 1] = __float_as_uint(__uint_as_float(r0[4 * c4 + 1]) * f.y);
-                r0[4 * c4 + 2] = __float_as_uint(__uint_as_float(r0[4 * c4 + 2]) * f.z);
-                r0[4 * c4 + 3] = __float_as_uint(__uint_as_float(r0[4 * c4 + 3]) * f.w);
-                const float4 g = *reinterpret_cast<const float4*>(sm + SM_CF + (c & 1) * 128 + 64 * q2 + 32 + 4 * c4);
-                r1[4 * c4 + 0] = __float_as_uint(__uint_as_float(r1[4 * c4 + 0]) * g.x);
-                r1[4 * c4 + 1] = __float_as_uint(__uint_as_float(r1[4 * c4 + 1]) * g.y);
-                r1[4 * c4 + 2] = __float_as_uint(__uint_as_float(r1[4 * c4 + 2]) * g.z);
-                r1[4 * c4 + 3] = __float_as_uint(__uint_as_float(r1[4 * c4 + 3]) * g.w);
+                scale4(r0 + 4 * c4, *reinterpret_cast<const float4*>(sm + SM_CF + (c & 1) * 128 + 64 * q2 + 4 * c4));
+                scale4(r1 + 4 * c4, *reinterpret_cast<const float4*>(sm + SM_CF + (c & 1) * 128 + 64 * q2 + 32 + 4 * c4));
             }
             tmem_st32(lane_base + TM_S + 64 * q2, r0);
             tmem_st32(lane_base + TM_S + 64 * q2 + 32, r1);
@@ -812,12 +865,13 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     const uint2 kr = *reinterpret_cast<const uint2*>(base + OFF_KIN + a * 8192 + sw);
                     const uint2 qr = *reinterpret_cast<const uint2*>(base + OFF_QIN + a * 8192 + sw);
                     const float4 e = *reinterpret_cast<const float4*>(LA + t * kD + 64 * a + 4 * g);
-                    float4 kp = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
-                    if (!ISO) kp = *reinterpret_cast<const float4*>(OM + t * kD + 64 * a + 4 * g);
-                    kp.x *= rcp_approx(e.x);
-                    kp.y *= rcp_approx(e.y);
-                    kp.z *= rcp_approx(e.z);
-                    kp.w *= rcp_approx(e.w);
+                    // p_hat / e1 (PKDA: write scale / e1), formed by warps 4-7; isotropic: 1 / e1
+                    float4 kp;
+                    if (ISO) {
+                        kp = make_float4(rcp_approx(e.x), rcp_approx(e.y), rcp_approx(e.z), rcp_approx(e.w));
+                    } else {
+                        kp = *reinterpret_cast<const float4*>(OM + t * kD + 64 * a + 4 * g);
+                    }
                     const float k0 = bf_lo(kr.x), k1 = bf_hi(kr.x), k2 = bf_lo(kr.y), k3 = bf_hi(kr.y);
                     kb[4 * a + 0] = k0 * e.x;
                     kb[4 * a + 1] = k1 * e.y;
@@ -1204,7 +1258,7 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t s) {
     if (!ok) return cudaErrorInvalidValue;
     P.r = a.r;
     P.la = a.log_alpha;
-    P.om_iso = a.variant == kVarIso ? a.omega : nullptr;
+    P.om = a.omega;
     P.beta = a.beta;
     P.alpha_p = a.alpha_p;
     P.beta_p = a.beta_p;
