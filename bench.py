@@ -314,6 +314,24 @@ def run_reference(args):
     return 0
 
 
+def profile_decode(torch, kdn, w, device, steps, warmup):
+    """Prefill through the forward path, then warm-up and timed single-token
+    kdn_step calls of a decode workload (one step's inputs, state updated in
+    place): the launch sequence an ncu capture of the decode kernel needs."""
+    pre = device_inputs(torch, w, "diag", w.seed, device, T=w.prefill)
+    _, S, p = kdn.kdn_diag_forward(pre["q"], pre["k"], pre["v"], pre["log_alpha"], pre["omega"],
+                                   pre["r"], chunk=w.chunk)
+    del pre
+    y = {n: t[:, 0] for n, t in device_inputs(torch, w, "diag", w.seed * 4096 + 1, device, T=1).items()}
+    ws = torch.empty(kdn.workspace_size(0, w.B, 1, w.H, w.d, w.d), dtype=torch.uint8, device=device)
+    o = torch.empty(w.B, w.H, w.d, device=device)
+    ms = time_calls(torch, lambda: kdn.kdn_step("diag", y["q"], y["k"], y["v"], y["log_alpha"], y["omega"], y["r"],
+                                                S, p, o=o, workspace=ws), steps, warmup, lambda: None)
+    print(json.dumps({"profile": w.name, "ms_per_step": ms, "device_status": kdn.kdn_read_device_status(ws)}),
+          flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------- main arm
 def main():
     args = parse_args()
@@ -347,6 +365,12 @@ def main():
 
     peaks, peak_src = load_peaks()
     w = WORKLOADS[args.workload]
+    if w.steps > 0:
+        if not args.profile:
+            print("decode workloads are timed inside the default run (see 'workloads'); use --profile",
+                  file=sys.stderr)
+            return 2
+        return profile_decode(torch, kdn, w, device, args.steps, args.warmup)
     variant = w.variant
     vcode = {"diag": kdn.KDN_DIAG, "iso": kdn.KDN_ISO, "pkda": kdn.KDN_PKDA}[variant]
     io = kdn.KDN_BF16 if w.io == "bf16" else kdn.KDN_F32
@@ -543,7 +567,9 @@ def other_workloads(torch, kdn, WORKLOADS, device, barrier, peaks):
                    "timing": "1024 kdn_step calls captured in one CUDA graph, replayed",
                    "eager_tokens_per_s": w.B * w.steps / (ms_eager / 1e3),
                    "hbm_frac": step_bytes / (per_step / 1e3) / 1e9 / hbm,
-                   "algorithmic_bytes_per_step": step_bytes}
+                   "algorithmic_bytes_per_step": step_bytes,
+                   "kernel": "step_stream_kernel",
+                   "traffic": traffic_for("step_stream_kernel", w.name)}
     return out
 
 

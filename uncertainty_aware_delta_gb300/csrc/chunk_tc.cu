@@ -545,25 +545,27 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         float2 g2 = make_float2(0.0f, 0.0f);   // chunk log-decay, log2 units, two partial sums
         const unsigned char* kin = base + OFF_KIN + (i >> 6) * 8192 + (i & 7) * 2;
         const int kch = (i & 63) >> 3;
+        // Tokens per loop body: one short body (8 tokens for KDN, 16 for PKDA, each
+        // measured fastest) keeps the code small; the isotropic variant unrolls the
+        // bodies of a half for its per-half reductions.
+        constexpr int kGB = PK ? 16 : 8, kGQ = 32 / kGB;
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
             float w[32], w2[32];
-            // (one 16-token body for the diagonal variant keeps the code small; the
-            //  isotropic variant keeps both bodies for its per-half reductions)
-#pragma unroll (ISO ? 2 : 1)
-            for (int qt = 0; qt < 2; ++qt) {
-                const int tb = hf * 32 + qt * 16;
+#pragma unroll (ISO ? kGQ : 1)
+            for (int qt = 0; qt < kGQ; ++qt) {
+                const int tb = hf * 32 + qt * kGB;
                 // loads first (independent of the carry) ...
-                float la[16], kv[16], om[16], mr[16];
+                float la[kGB], kv[kGB], om[kGB], mr[kGB];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
+                for (int u = 0; u < kGB; ++u) {
                     const int t = tb + u;
                     la[u] = LA[t * kD + i];
                     kv[u] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(kin + sw128_off(t, kch)));
                     om[u] = V == kVarDiag ? OM[t * kD + i] : 0.0f;
                 }
 #pragma unroll
-                for (int u4 = 0; u4 < 4; ++u4) {
+                for (int u4 = 0; u4 < kGB / 4; ++u4) {
                     const float4 m4 = *reinterpret_cast<const float4*>(sm + SM_MUR + tb + 4 * u4);
                     mr[4 * u4 + 0] = m4.x;
                     mr[4 * u4 + 1] = m4.y;
@@ -579,9 +581,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     // key statistic A = alpha_p A + beta_p k^2 (this token included), then
                     // the write scale exp(-log(x) s), s = softsign(log A - mu), times beta:
                     // the coefficient of the write key (Preconditioned DeltaNet Eq. 9)
-                    float bp[16], ap[16], be[16];
+                    float bp[kGB], ap[kGB], be[kGB];
 #pragma unroll
-                    for (int u4 = 0; u4 < 4; ++u4) {
+                    for (int u4 = 0; u4 < kGB / 4; ++u4) {
                         const float4 b4 = *reinterpret_cast<const float4*>(sm + SM_MUR + tb + 4 * u4);
                         const float4 a4 = *reinterpret_cast<const float4*>(sm + SM_OMI + tb + 4 * u4);
                         const float4 w4 = *reinterpret_cast<const float4*>(sm + SM_R + tb + 4 * u4);
@@ -590,7 +592,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                         be[4 * u4 + 0] = w4.x; be[4 * u4 + 1] = w4.y; be[4 * u4 + 2] = w4.z; be[4 * u4 + 3] = w4.w;
                     }
 #pragma unroll
-                    for (int u = 0; u < 16; u += 2) {
+                    for (int u = 0; u < kGB; u += 2) {
                         const int t = tb + u;
                         const float2 l2 = fmul2(make_float2(la[u], la[u + 1]), make_float2(kLog2e, kLog2e));
                         const float gr0 = gr + l2.x, gr1 = gr0 + l2.y;
@@ -617,7 +619,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     }
                 } else if (!ISO) {
 #pragma unroll
-                    for (int u = 0; u < 16; u += 2) {
+                    for (int u = 0; u < kGB; u += 2) {
                         const int t = tb + u;
                         const float2 l2 = fmul2(make_float2(la[u], la[u + 1]), make_float2(kLog2e, kLog2e));
                         g2 = fadd2(g2, l2);
@@ -652,15 +654,15 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     }
                 } else {
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
+                    for (int u = 0; u < kGB; ++u) {
                         const int t = tb + u;
                         const float l2 = la[u] * kLog2e;
                         g2.x += l2;
                         const float al = ex2(l2), a2 = al * al, k2 = kv[u] * kv[u];
                         e1 *= al;
                         LA[t * kD + i] = e1;
-                        w[qt * 16 + u] = k2;
-                        w2[qt * 16 + u] = t < nvc ? a2 : 0.0f;
+                        w[qt * kGB + u] = k2;
+                        w2[qt * kGB + u] = t < nvc ? a2 : 0.0f;
                     }
                 }
             }
@@ -807,9 +809,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     auto issue_output_update = [&]() {
         tc_fence_after();
         const uint32_t id_o = idesc_bf16(128, 64, 0, 0, 0);
+        const uint64_t d_aq = sw128_desc(sb + OFF_AQ, 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_tmem_a(tmem + TM_O, tmem + TM_DB + 8 * ks, sw128_desc(sb + OFF_AQ + ks * 32, 16, 1024), id_o, 1u);
+            mma_bf16_tmem_a(tmem + TM_O, tmem + TM_DB + 8 * ks, desc_add(d_aq, ks * 32), id_o, 1u);
         mma_commit(bar_oj);
         ++n_oj_issued;
     };
@@ -839,10 +842,11 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 wait_or_abort(bar_ops, pb);   // operands built (warps 4-11)
                 tc_fence_after();
                 const uint32_t id_zo = idesc_bf16(128, 128, 0, 0, 0);
+                const uint64_t d_kq = sw128_desc(sb + OFF_KQ, 16, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16_tmem_a(tmem + TM_ZD, tmem + TM_SMB + 8 * ks,
-                                    sw128_desc(sb + OFF_KQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_zo,
+                                    desc_add(d_kq, (ks >> 2) * 16384 + (ks & 3) * 32), id_zo,
                                     ks > 0);
                 mma_commit(bar_o);
                 ++n_o_issued;
@@ -904,10 +908,11 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             if (tid == 256 && !*s_abort) {
                 tc_fence_after();
                 const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
+                const uint64_t d_kq = sw128_desc(sb + OFF_KQ, 16, 1024), d_kt = sw128_desc(sb + OFF_KT, 16, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t ad = sw128_desc(sb + OFF_KQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                    const uint64_t bd = sw128_desc(sb + OFF_KT + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+                    const uint64_t ad = desc_add(d_kq, (ks >> 2) * 16384 + (ks & 3) * 32);
+                    const uint64_t bd = desc_add(d_kt, (ks >> 2) * 8192 + (ks & 3) * 32);
                     mma_bf16(tmem + TM_G, ad, bd, id, ks > 0);
                 }
                 mma_commit(bar_mma);
@@ -1081,9 +1086,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             if (tid == 0 && !*s_abort) {
                 tc_fence_after();
                 const uint32_t id_y = idesc_bf16(128, 64, 0, 0, 0);
+                const uint64_t d_tt = sw128_desc(sb + OFF_TT, 16, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_tmem_a(tmem + TM_ZD, tmem + TM_DB + 8 * ks, sw128_desc(sb + OFF_TT + ks * 32, 16, 1024),
+                    mma_bf16_tmem_a(tmem + TM_ZD, tmem + TM_DB + 8 * ks, desc_add(d_tt, ks * 32),
                                     id_y, ks > 0);
                 mma_commit(bar_mma);
                 ++n_mma_issued;
@@ -1113,9 +1119,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             if (tid == 0 && !*s_abort) {
                 tc_fence_after();
                 const uint32_t id_s = idesc_bf16(128, 128, 0, 1, 0);
+                const uint64_t d_ktm = sw128_desc(sb + OFF_KT, 8192, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_tmem_a(tmem + TM_S, tmem + TM_DB + 8 * ks, sw128_desc(sb + OFF_KT + ks * 2048, 8192, 1024),
+                    mma_bf16_tmem_a(tmem + TM_S, tmem + TM_DB + 8 * ks, desc_add(d_ktm, ks * 2048),
                                     id_s, 1u);
                 mma_commit(bar_mma);
                 mma_commit(bar_js);

@@ -109,6 +109,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     d |= static_cast<uint64_t>(2) << 61;
     return d;
 }
+// The descriptor of the same tile `byte_off` bytes further on: the start address
+// field (address >> 4, 14 bits) cannot carry into the other fields because shared
+// addresses stay below 256 KB, so the offset is a plain add.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off) {
+    return desc + static_cast<uint64_t>(byte_off >> 4);
+}
 // Instruction descriptor, kind::f16 with bf16 operands and fp32 accumulation.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn, int neg_a) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(neg_a) << 13) |
