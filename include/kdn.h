@@ -89,6 +89,7 @@ typedef enum { KDN_DIAG = 0, KDN_ISO = 1, KDN_PKDA = 2 } kdn_variant;
 
 /* Flags for the forward calls. */
 #define KDN_FLAG_PORTABLE 0x1u   /* force the CUDA-core (FFMA) chunk path */
+#define KDN_FLAG_NO_SPLIT 0x2u   /* tensor-core path: never split sequences into segments */
 
 /*
  * Supported sizes: d_k, d_v in {16, 32, 64, 128}; chunk in {16, 32, 64}

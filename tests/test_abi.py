@@ -85,6 +85,28 @@ def test_forward_kernel_count(lib):
     assert kdn.forward_kernel_count(2, 1, 64, 2, 128, 128, 64, 1, 0) == 1  # fused tensor-core kernel
 
 
+def test_sequence_split_plan(lib):
+    """Few long sequences on the tensor-core path run as segments (scan carries,
+    segment maps, chaining, segments: 6 launches) with their state maps in the
+    workspace; many sequences, short ones or the opt-out flag keep one launch."""
+    import uncertainty_aware_delta_gb300 as kdn
+
+    kc, ws = kdn.forward_kernel_count, kdn.workspace_size
+    NO = kdn.KDN_FLAG_NO_SPLIT
+    for v in (0, 1, 2):
+        # 16 sequences x 65536 tokens: 152 // 16 = 9 segments of 29 x 256 tokens
+        assert kc(v, 1, 65536, 16, 128, 128, 64, 1, 0) == 6
+        assert kc(v, 1, 65536, 16, 128, 128, 64, 1, NO) == 1
+        assert kc(v, 8, 4096, 16, 128, 128, 64, 1, 0) == 1      # 128 sequences fill the GPU
+        assert kc(v, 1, 1500, 2, 128, 128, 64, 1, 0) == 1       # under 2 x 1024 tokens
+        assert kc(v, 1, 2048, 2, 128, 128, 64, 1, 0) == 6
+        nu = 1 if v == 1 else 128
+        n_split, n_whole = ws(v, 1, 65536, 16, 128, 128, 64, 1, 0), ws(v, 1, 65536, 16, 128, 128, 64, 1, NO)
+        # three [16 x 9][128][128] fp32 state arrays and the scan summaries and carries (256 gain chunks)
+        assert n_split - n_whole >= 4 * (3 * 16 * 9 * 128 * 128 + 5 * 16 * 256 * nu)
+        assert ws(v, 8, 4096, 16, 128, 128, 64, 1, 0) == ws(v, 8, 4096, 16, 128, 128, 64, 1, NO)
+
+
 def _fwd_args(**over):
     a = dict(B=1, T=64, H=2, dk=16, dv=16, chunk=16, mu=-1.0, io=0, flags=0,
              q=64, k=64, v=64, la=64, om=64, r=64, S0=None, p0=None, o=1 << 20, S_T=2 << 20,

@@ -256,3 +256,63 @@ def test_tensor_core_path_strong_decay(variant):
     assert kdn.kdn_read_device_status(ws) == 0
     ref = oracle.forward(variant, x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"])
     _check(variant, x, got, ref, "bf16", "strong decay")
+
+
+# ------------------------------------------------------------ sequence split
+SPLIT_CASES = [
+    # variant, B, T, H, with an initial state: few long sequences -> segments on separate SMs
+    ("diag", 1, 4096, 2, False),    # 4 segments of 1024 tokens
+    ("iso", 1, 4096, 2, False),
+    ("diag", 1, 4000, 2, True),     # 3 segments, the last with a ragged tail; resume from a state
+    ("iso", 2, 2600, 1, True),
+]
+
+
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_sequence_split_matches_oracle_and_unsplit_run(case):
+    """The tensor-core forward of few long sequences runs each sequence as
+    segments chained through their affine state maps; it must match the
+    oracle, and the unsplit kernel on the same inputs."""
+    import torch
+
+    variant, B, T, H, with_state = case
+    kdn = _kdn()
+    vcode = kdn.KDN_DIAG if variant == "diag" else kdn.KDN_ISO
+    assert kdn.forward_kernel_count(vcode, B, T, H, 128, 128, 64, kdn.KDN_BF16, 0) == 6
+    assert kdn.forward_kernel_count(vcode, B, T, H, 128, 128, 64, kdn.KDN_BF16, kdn.KDN_FLAG_NO_SPLIT) == 1
+    x = make_inputs(variant, B, T, H, 128, 128, io="bf16", seed=900 + T)
+    t = to_device(x)
+    kw, ref_kw = {}, {}
+    if with_state:
+        rng = np.random.default_rng(T)
+        S0 = (0.2 * rng.standard_normal((B, H, 128, 128))).astype(np.float32)
+        p0 = rng.uniform(0.3, 2.0, size=(B, H, 128) if variant == "diag" else (B, H)).astype(np.float32)
+        kw = {"S0": torch.from_numpy(S0).cuda(), "p0": torch.from_numpy(p0).cuda()}
+        ref_kw = {"S0": S0, "p0": p0}
+    ref = oracle.forward(variant, x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"], **ref_kw)
+    got = _run(kdn, variant, t, chunk=64, **kw)
+    _check(variant, x, got, ref, "bf16", "split")
+    whole = _run(kdn, variant, t, chunk=64, flags=kdn.KDN_FLAG_NO_SPLIT, **kw)
+    for a, b_ in zip(got, whole):
+        a, b_ = to_host(a), to_host(b_)
+        assert np.max(np.abs(a - b_)) <= 2e-2 * max(1e-3, np.max(np.abs(b_)))
+
+
+def test_sequence_split_strong_decay():
+    """Segments whose chunks decay strongly (mid-chunk reference, split frame
+    factor) chain correctly: the transition map of such a segment is tiny."""
+    import torch
+
+    kdn = _kdn()
+    B, T, H = 1, 2048, 2
+    x = make_inputs("diag", B, T, H, 128, 128, io="bf16", seed=78)
+    x["log_alpha"][:, :, 0] = -1.5
+    x["r"][:, :, 0] = 1e-3
+    x["omega"][:, :, 0] = 1.0
+    t = to_device(x)
+    ws = torch.empty(kdn.workspace_size(kdn.KDN_DIAG, B, T, H, 128, 128, 64, kdn.KDN_BF16, 0),
+                     dtype=torch.uint8, device="cuda")
+    got = _run(kdn, "diag", t, chunk=64, workspace=ws)
+    assert kdn.kdn_read_device_status(ws) == 0
+    ref = oracle.forward("diag", x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"])
+    _check("diag", x, got, ref, "bf16", "split, strong decay")

@@ -233,3 +233,20 @@ def test_pkda_steps_after_prefill(case):
     assert err(to_host(torch.stack(outs, 1)), ref["o"][:, prefill:], io) <= tol(io)
     assert err(to_host(S), ref["S_T"], io) <= tol(io)
     assert max_rel(to_host(A), ref["A_T"]) <= 1e-4
+
+
+def test_pkda_sequence_split():
+    """Few long sequences: the PKDA forward runs as chained segments (statistic
+    carries from the scan, affine state maps) and matches the oracle and the
+    unsplit kernel."""
+    kdn = _kdn()
+    B, T, H = 1, 3000, 2
+    assert kdn.forward_kernel_count(kdn.KDN_PKDA, B, T, H, 128, 128, 64, kdn.KDN_BF16, 0) == 6
+    x = make_pkda_inputs(B, T, H, 128, 128, io="bf16", seed=62)
+    t = _dev(x)
+    got = _run(kdn, t, chunk=64)
+    _check(got, _ref(x), "bf16", "split")
+    whole = _run(kdn, t, chunk=64, flags=kdn.KDN_FLAG_NO_SPLIT)
+    for a, b_ in zip(got, whole):
+        a, b_ = to_host(a), to_host(b_)
+        assert np.max(np.abs(a - b_)) <= 2e-2 * max(1e-3, np.max(np.abs(b_)))

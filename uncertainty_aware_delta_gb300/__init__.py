@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     KDN_BF16,
     KDN_DIAG,
     KDN_F32,
+    KDN_FLAG_NO_SPLIT,
     KDN_FLAG_PORTABLE,
     KDN_ISO,
     KDN_PKDA,

@@ -20,6 +20,7 @@ _lib = None
 KDN_F32, KDN_BF16 = 0, 1
 KDN_DIAG, KDN_ISO, KDN_PKDA = 0, 1, 2
 KDN_FLAG_PORTABLE = 0x1
+KDN_FLAG_NO_SPLIT = 0x2
 
 EXPORTED = (
     "kdn_workspace_size", "kdn_diag_forward", "kdn_iso_forward", "kdn_step",

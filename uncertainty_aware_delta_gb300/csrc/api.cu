@@ -49,6 +49,9 @@ struct WsLayout {
     size_t total;
     size_t kappa_off, summary_off, carry_off;
     int nG;
+    // tensor-core sequence split: per-segment state maps and initial states
+    kdn::TcSplit split;
+    size_t sloc_off, phi_off, sin_off;
 };
 
 WsLayout ws_layout(int variant, int B, int T, int H, int dk, int dv, int chunk, int io,
@@ -66,6 +69,23 @@ WsLayout ws_layout(int variant, int B, int T, int H, int dk, int dv, int chunk, 
         off = align_up(off + sizeof(float) * 4 * BH * w.nG * nu);
         w.carry_off = off;
         off = align_up(off + sizeof(float) * BH * w.nG * nu);
+    } else if (T > 0) {
+        w.split = kdn::tc_split_plan(B, T, H, flags);
+        if (w.split.nseg > 1) {
+            const int nu = variant == KDN_ISO ? 1 : dk;
+            const size_t BH = (size_t)B * H, nst = BH * w.split.nseg * dk * dv;
+            w.nG = (T + kdn::kGainChunk - 1) / kdn::kGainChunk;
+            w.summary_off = off;
+            off = align_up(off + sizeof(float) * 4 * BH * w.nG * nu);
+            w.carry_off = off;
+            off = align_up(off + sizeof(float) * BH * w.nG * nu);
+            w.sloc_off = off;
+            off = align_up(off + sizeof(float) * nst);
+            w.phi_off = off;
+            off = align_up(off + sizeof(float) * nst);
+            w.sin_off = off;
+            off = align_up(off + sizeof(float) * nst);
+        }
     }
     w.total = off;
     return w;
@@ -152,7 +172,17 @@ kdn_status forward_impl(int variant, int B, int T, int H, int dk, int dv, int ch
     if (T == 0) {
         e = kdn::launch_state_copy(a, s);
     } else if (use_tc_path(io, dk, dv, chunk, flags)) {
-        e = kdn::launch_forward_tc(a, s);
+        kdn::TcSplit sp = w.split;
+        if (sp.nseg > 1) {
+            char* base = static_cast<char*>(workspace);
+            sp.summary = reinterpret_cast<float*>(base + w.summary_off);
+            sp.carry = reinterpret_cast<float*>(base + w.carry_off);
+            sp.n_chunks_g = w.nG;
+            sp.S_loc = reinterpret_cast<float*>(base + w.sloc_off);
+            sp.Phi = reinterpret_cast<float*>(base + w.phi_off);
+            sp.S_in = reinterpret_cast<float*>(base + w.sin_off);
+        }
+        e = kdn::launch_forward_tc(a, sp, s);
     } else {
         char* base = static_cast<char*>(workspace);
         kdn::ScanWorkspace sw;
@@ -301,7 +331,9 @@ int kdn_forward_kernel_count(int variant, int B, int T, int H, int dk, int dv, i
     if ((size_t)B * H == 0) return 0;
     if (T == 0) return 1;
     chunk = resolve_chunk(chunk, T);
-    return use_tc_path(io_dtype, dk, dv, chunk, flags) ? kdn::tc_kernel_count() : 4;
+    return use_tc_path(io_dtype, dk, dv, chunk, flags)
+               ? kdn::tc_kernel_count(kdn::tc_split_plan(B, T, H, flags).nseg)
+               : 4;
 }
 
 const char* kdn_status_string(int status) {

@@ -60,6 +60,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "kdn.h"
 #include "kdn_internal.h"
 #include "sm100.cuh"
 
@@ -138,6 +139,17 @@ struct TcParams {
     int T, H;
     float mu;
     float neg_log2x;      // PKDA: -log2(x), x the bound of the write scale
+    // Sequence split: CTA blockIdx.x = bh * nseg + seg runs tokens
+    // [seg * seg_len, min(T, (seg + 1) * seg_len)) of sequence bh (nseg = 1: whole
+    // sequences).  seg_len is a multiple of the chunk, so only the last segment has
+    // a ragged tail (past T, where the copies read zeros).
+    int nseg, seg_len;
+    int s0_identity;      // start from S = I (the segment's transition map) instead of S0
+    int no_v;             // values read as zero
+    int no_o;             // outputs not written
+    int last_only;        // final state of the last segment only, to S_T / p_T at bh;
+                          // otherwise every CTA writes its final state to S_T at blockIdx.x
+    long long p0_bh, p0_seg;   // p0 element offset of (bh, seg): bh * p0_bh + seg * p0_seg
 };
 
 // Kernel variants: the two KDN uncertainty models and the preconditioned delta
@@ -383,7 +395,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool wg0 = tid < 128, wg1 = tid >= 128 && tid < 256, wg2 = tid >= 256;
-    const int bh = blockIdx.x, H = P.H, b = bh / H, h = bh % H, T = P.T;
+    const int vs = blockIdx.x, bh = vs / P.nseg, seg = vs % P.nseg, H = P.H, b = bh / H, h = bh % H;
+    const int Tall = P.T, tb = seg * P.seg_len;   // sequence length, first token of the segment
+    const int T = min(P.seg_len, Tall - tb);      // tokens of this CTA's segment
     const int nchunks = (T + kC - 1) / kC;
 
     if (tid == 0) {
@@ -407,26 +421,26 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     auto issue_inputs = [&](int n) {
         const int t0 = n * kC;
         mbar_expect_tx(bar_la, 32768u);
-        tma_load_4d(sb + OFF_LA, &P.tla, 0, h, t0, b, bar_la);
+        tma_load_4d(sb + OFF_LA, &P.tla, 0, h, tb + t0, b, bar_la);
         mbar_expect_tx(bar_ko, V == kVarDiag ? 49152u : 16384u);
-        if (V == kVarDiag) tma_load_4d(sb + OFF_OM, &P.tom, 0, h, t0, b, bar_ko);
-        tma_load_4d(sb + OFF_KIN, &P.tk, 0, h, t0, b, bar_ko);
-        tma_load_4d(sb + OFF_KIN + 8192, &P.tk, 64, h, t0, b, bar_ko);
+        if (V == kVarDiag) tma_load_4d(sb + OFF_OM, &P.tom, 0, h, tb + t0, b, bar_ko);
+        tma_load_4d(sb + OFF_KIN, &P.tk, 0, h, tb + t0, b, bar_ko);
+        tma_load_4d(sb + OFF_KIN + 8192, &P.tk, 64, h, tb + t0, b, bar_ko);
         mbar_expect_tx(bar_q, 16384u);
-        tma_load_4d(sb + OFF_QIN, &P.tq, 0, h, t0, b, bar_q);
-        tma_load_4d(sb + OFF_QIN + 8192, &P.tq, 64, h, t0, b, bar_q);
+        tma_load_4d(sb + OFF_QIN, &P.tq, 0, h, tb + t0, b, bar_q);
+        tma_load_4d(sb + OFF_QIN + 8192, &P.tq, 64, h, tb + t0, b, bar_q);
     };
     auto issue_v = [&](int n) {
         mbar_expect_tx(bar_v, 16384u);
-        tma_load_4d(sb + OFF_VIN, &P.tv, 0, h, n * kC, b, bar_v);
-        tma_load_4d(sb + OFF_VIN + 8192, &P.tv, 64, h, n * kC, b, bar_v);
+        tma_load_4d(sb + OFF_VIN, &P.tv, 0, h, tb + n * kC, b, bar_v);
+        tma_load_4d(sb + OFF_VIN + 8192, &P.tv, 64, h, tb + n * kC, b, bar_v);
     };
     __syncthreads();
     // copies and MMA commits issued so far (thread 0: v, MMAs; thread 256: the Gram MMAs;
     // thread 160: q, k, log_alpha, omega)
     int n_in_issued = 0, n_v_issued = 0, n_mma_issued = 0, n_o_issued = 0, n_oj_issued = 0, n_gram_issued = 0,
         n_js_issued = 0;
-    if (tid == 0 && nchunks > 0) {
+    if (tid == 0 && nchunks > 0 && !P.no_v) {
         issue_v(0);
         n_v_issued = 1;
     }
@@ -447,9 +461,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     // PKDA: key statistic of channel tid - 128 (warps 4-7), and the head's centre
     float stat = 0.0f;
     const float center = PK ? P.center[h] : 0.0f;
-    if (wg1 && V == kVarDiag && P.p0) pn = P.p0[static_cast<size_t>(bh) * kD + (tid - 128)];
-    if (wg1 && PK && P.p0) stat = P.p0[static_cast<size_t>(bh) * kD + (tid - 128)];
-    if (ISO && warp == 4 && P.p0) b_iso = P.p0[bh];
+    const float* p0v = P.p0 ? P.p0 + bh * P.p0_bh + seg * P.p0_seg : nullptr;
+    if (wg1 && V == kVarDiag && p0v) pn = p0v[tid - 128];
+    if (wg1 && PK && p0v) stat = p0v[tid - 128];
+    if (ISO && warp == 4 && p0v) b_iso = p0v[0];
     // initial state S^T into TMEM: lane j = value column, columns = key channel
     if (wg0) {
         const int j = tid;
@@ -459,7 +474,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 const int i = q * 32 + c;
-                r[c] = __float_as_uint(P.S0 ? P.S0[(static_cast<size_t>(bh) * kD + i) * kD + j] : 0.0f);
+                r[c] = __float_as_uint(P.s0_identity ? (i == j ? 1.0f : 0.0f)
+                                       : P.S0 ? P.S0[(static_cast<size_t>(vs) * kD + i) * kD + j] : 0.0f);
             }
             tmem_st32(lane_base + TM_S + q * 32, r);
         }
@@ -514,7 +530,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 // statistic unchanged and write nothing)
                 float be = 0.0f, bp = 0.0f, ap = 1.0f;
                 if (t < nvc) {
-                    const size_t th = (static_cast<size_t>(b) * T + t0c + t) * H + h;
+                    const size_t th = (static_cast<size_t>(b) * Tall + tb + t0c + t) * H + h;
                     be = P.beta[th];
                     bp = P.beta_p[th];
                     ap = P.alpha_p[th];
@@ -525,7 +541,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             } else {
                 float rr = 1.0f, om = 0.0f;
                 if (t < nvc) {
-                    const size_t th = (static_cast<size_t>(b) * T + t0c + t) * H + h;
+                    const size_t th = (static_cast<size_t>(b) * Tall + tb + t0c + t) * H + h;
                     rr = P.r[th];
                     if (ISO) om = P.om[th];
                 }
@@ -680,7 +696,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 // from log_alpha (and omega) in global memory (the tiles now hold the
                 // factors), re-running the variance (statistic) recurrence of the chunk
                 R2 = 0.5f * G2C;
-                strong_decay_factors<V>(P, base, i, b, h, t0c, nvc, R2, pn0, pd0, stat0, center);
+                strong_decay_factors<V>(P, base, i, b, h, tb + t0c, nvc, R2, pn0, pd0, stat0, center);
             }
             // The frame factor 2^(pend2 + R2) of the state: each part is at least
             // 2^-116 (|G_C| <= 160), but after two strongly decaying chunks their sum
@@ -759,7 +775,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         tc_fence_after();
         tmem_ld64(TM_O, v0, v1);
         const int t0c = c * kC, nvc = min(kC, T - t0c);
-        __nv_bfloat16* og = P.o + (static_cast<size_t>(b) * T + t0c) * H * kD + static_cast<size_t>(h) * kD + tid;
+        __nv_bfloat16* og =
+            P.o + (static_cast<size_t>(b) * Tall + tb + t0c) * H * kD + static_cast<size_t>(h) * kD + tid;
         const size_t ts = static_cast<size_t>(H) * kD;
         if (nvc == kC) {
 #pragma unroll
@@ -833,7 +850,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             scale_state(n);
             if (n > 0) {
                 wait_or_abort(bar_oj, pb ^ 1u);   // output update of chunk n-1 has landed
-                emit_outputs(n - 1);
+                if (!P.no_o) emit_outputs(n - 1);
             }
             tc_fence_before();
             named_bar(kBarWG0, 128);
@@ -1059,7 +1076,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             //      is the prediction) -> bf16 A operand in TMEM
             {
                 wait_or_abort(bar_o, pb);
-                wait_or_abort(bar_v, ph_v);
+                if (!P.no_v) wait_or_abort(bar_v, ph_v);
                 tc_fence_after();
                 uint32_t v0[32], v1[32], pk[32];
                 tmem_ld64(TM_ZD, v0, v1);
@@ -1069,8 +1086,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int t = 2 * e;
-                    const float va = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + sw128_off(t, jc)));
-                    const float vb = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + sw128_off(t + 1, jc)));
+                    // (no_v: the segment's transition map, values zero)
+                    const float va = P.no_v ? 0.0f : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + sw128_off(t, jc)));
+                    const float vb = P.no_v ? 0.0f : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + sw128_off(t + 1, jc)));
                     const float za = __uint_as_float(t < 32 ? v0[t] : v1[t - 32]);
                     const float zb = __uint_as_float(t + 1 < 32 ? v0[t + 1] : v1[t + 1 - 32]);
                     pk[e] = pack_bf16(va - za, vb - zb);
@@ -1093,7 +1111,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                                     id_y, ks > 0);
                 mma_commit(bar_mma);
                 ++n_mma_issued;
-                if (n + 1 < nchunks) {
+                if (n + 1 < nchunks && !P.no_v) {
                     issue_v(n + 1);
                     ++n_v_issued;
                 }
@@ -1157,11 +1175,15 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     if (!aborted && nchunks > 0) {
         wait_or_abort(bar_mma, static_cast<uint32_t>(nchunks - 1) & 1u);   // update of the last chunk has landed
         wait_or_abort(bar_oj, static_cast<uint32_t>(nchunks - 1) & 1u);
-        if (wg0) emit_outputs(nchunks - 1);
+        if (wg0 && !P.no_o) emit_outputs(nchunks - 1);
     }
     if (!*s_abort) {
         // final state: S_T = (TMEM state) scaled by the last chunk's pending factor
-        if (wg0) {
+        // (sequence split: only the last segment writes the sequence's final state,
+        //  unless every segment's final state is wanted, at its CTA index)
+        const bool last = seg == P.nseg - 1;
+        const size_t st_idx = P.last_only ? static_cast<size_t>(bh) : static_cast<size_t>(vs);
+        if (wg0 && (last || !P.last_only)) {
             tc_fence_after();
             const int j = tid;
 #pragma unroll 1
@@ -1173,10 +1195,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 for (int c = 0; c < 32; ++c) {
                     const int i = q * 32 + c;
                     const float f = nchunks > 0 ? sm[SM_FOUT + i] : 1.0f;
-                    P.S_T[(static_cast<size_t>(bh) * kD + i) * kD + j] = __uint_as_float(r[c]) * f;
+                    P.S_T[(st_idx * kD + i) * kD + j] = __uint_as_float(r[c]) * f;
                 }
             }
-        } else if (wg1) {
+        } else if (wg1 && last && P.last_only) {
             if (V == kVarDiag) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = pn / pd;
             else if (PK) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = stat;
             else if (tid == 128) P.p_T[bh] = b_iso;
@@ -1207,6 +1229,48 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, TM_COLS);
+    }
+}
+
+// Chain the segment maps of each sequence: S_in(0) = S0 (zero when NULL) and
+// S_in(s + 1) = Phi_s S_in(s) + S_loc(s), all [B*H*nseg][128][128] fp32.  Grid
+// (B*H, 128 / 16), 256 threads: a CTA owns 16 value columns of the state and walks
+// the segments in order; thread (row i, 8 columns) forms its part of each product.
+__global__ void __launch_bounds__(256) segment_states_kernel(const float* __restrict__ S0,
+                                                              const float* __restrict__ Phi,
+                                                              const float* __restrict__ S_loc,
+                                                              float* __restrict__ S_in, int nseg) {
+    __shared__ float cur[kD][17];
+    const int bh = blockIdx.x, cb = blockIdx.y * 16, tid = threadIdx.x;
+    for (int e = tid; e < kD * 16; e += 256) {
+        const int i = e >> 4, j = e & 15;
+        cur[i][j] = S0 ? S0[(static_cast<size_t>(bh) * kD + i) * kD + cb + j] : 0.0f;
+    }
+    __syncthreads();
+    const int i = tid >> 1, j0 = (tid & 1) * 8;
+    for (int sg = 0; sg < nseg; ++sg) {
+        const size_t mb = (static_cast<size_t>(bh) * nseg + sg) * kD * kD;
+        float* out = S_in + mb + static_cast<size_t>(i) * kD + cb + j0;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) out[jj] = cur[i][j0 + jj];
+        if (sg == nseg - 1) break;
+        float acc[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) acc[jj] = S_loc[mb + static_cast<size_t>(i) * kD + cb + j0 + jj];
+        const float4* phi = reinterpret_cast<const float4*>(Phi + mb + static_cast<size_t>(i) * kD);
+#pragma unroll 4
+        for (int k4 = 0; k4 < kD / 4; ++k4) {
+            const float4 f = phi[k4];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+                acc[jj] = fmaf(f.x, cur[4 * k4][j0 + jj],
+                               fmaf(f.y, cur[4 * k4 + 1][j0 + jj],
+                                    fmaf(f.z, cur[4 * k4 + 2][j0 + jj], fmaf(f.w, cur[4 * k4 + 3][j0 + jj], acc[jj]))));
+        }
+        __syncthreads();
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) cur[i][j0 + jj] = acc[jj];
+        __syncthreads();
     }
 }
 
@@ -1250,9 +1314,32 @@ bool tc_path_supported(int io, int dk, int dv, int chunk) {
     return io == 1 && dk == kD && dv == kD && chunk == kC;
 }
 
-int tc_kernel_count() { return 1; }
+// The split runs on one wave of CTAs of the GPU this kernel targets (152 SMs),
+// with segments of at least kMinSegTokens tokens.
+constexpr int kSplitCTAs = 152, kMinSegTokens = 1024;
 
-cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t s) {
+TcSplit tc_split_plan(int B, int T, int H, uint32_t flags) {
+    TcSplit sp;
+    sp.seg_len = T;
+    const long long BH = static_cast<long long>(B) * H;
+    if ((flags & KDN_FLAG_NO_SPLIT) || BH <= 0 || 2 * BH > kSplitCTAs) return sp;
+    long long nseg = kSplitCTAs / BH;
+    if (nseg > T / kMinSegTokens) nseg = T / kMinSegTokens;
+    if (nseg < 2) return sp;
+    const int G = kGainChunk;   // a multiple of the chunk: segments start on gain-chunk carries
+    const long long per = (T + nseg - 1) / nseg;
+    const int seg_len = static_cast<int>((per + G - 1) / G * G);
+    const int n = (T + seg_len - 1) / seg_len;
+    if (n < 2) return sp;
+    sp.nseg = n;
+    sp.seg_len = seg_len;
+    return sp;
+}
+
+// carries (2 launches), segment maps (2), chaining (1), segments (1)
+int tc_kernel_count(int nseg) { return nseg > 1 ? 6 : 1; }
+
+cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStream_t s) {
     TcParams P;
     memset(&P, 0, sizeof(P));
     const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -1280,16 +1367,63 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t s) {
     P.T = a.T;
     P.H = a.H;
     P.mu = a.mu;
-    const int grid = a.B * a.H;
+    const int nu = a.variant == kVarIso ? 1 : kD;
+    P.nseg = 1;
+    P.seg_len = a.T;
+    P.last_only = 1;
+    P.p0_bh = nu;
+    P.p0_seg = 0;
+    int grid = a.B * a.H;
     auto launch = [&](auto kernel) {
         const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
         if (e != cudaSuccess) return e;
         kernel<<<grid, kNT, kSmemAlloc, s>>>(P);
         return cudaGetLastError();
     };
-    if (a.variant == kVarDiag) return launch(kdn_fused_tc_kernel<kVarDiag>);
-    if (a.variant == kVarIso) return launch(kdn_fused_tc_kernel<kVarIso>);
-    return launch(kdn_fused_tc_kernel<kVarPkda>);
+    auto run = [&]() {
+        if (a.variant == kVarDiag) return launch(kdn_fused_tc_kernel<kVarDiag>);
+        if (a.variant == kVarIso) return launch(kdn_fused_tc_kernel<kVarIso>);
+        return launch(kdn_fused_tc_kernel<kVarPkda>);
+    };
+    if (sp.nseg <= 1) return run();
+
+    // ---- sequence split: every segment's initial uncertainty (statistic) from the scan
+    ScanWorkspace w;
+    w.kappa = nullptr;
+    w.summary = sp.summary;
+    w.carry = sp.carry;
+    w.chunk_g = kGainChunk;
+    w.n_chunks_g = sp.n_chunks_g;
+    cudaError_t e = launch_scan_carries(a, w, s);
+    if (e != cudaSuccess) return e;
+    P.nseg = sp.nseg;
+    P.seg_len = sp.seg_len;
+    P.p0 = sp.carry;
+    P.p0_bh = static_cast<long long>(sp.n_chunks_g) * nu;
+    P.p0_seg = static_cast<long long>(sp.seg_len / kGainChunk) * nu;
+    grid = a.B * a.H * sp.nseg;
+    // ---- each segment's affine state map: S_loc from S = 0, Phi from S = I with zero values
+    P.S0 = nullptr;
+    P.no_o = 1;
+    P.last_only = 0;
+    P.S_T = sp.S_loc;
+    P.p_T = nullptr;
+    if ((e = run()) != cudaSuccess) return e;
+    P.s0_identity = 1;
+    P.no_v = 1;
+    P.S_T = sp.Phi;
+    if ((e = run()) != cudaSuccess) return e;
+    // ---- chained initial states, then the segments from their true states
+    segment_states_kernel<<<dim3(a.B * a.H, kD / 16), 256, 0, s>>>(a.S0, sp.Phi, sp.S_loc, sp.S_in, sp.nseg);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    P.S0 = sp.S_in;
+    P.s0_identity = 0;
+    P.no_v = 0;
+    P.no_o = 0;
+    P.last_only = 1;
+    P.S_T = a.S_T;
+    P.p_T = a.p_T;
+    return run();
 }
 
 }  // namespace kdn

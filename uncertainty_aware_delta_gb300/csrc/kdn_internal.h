@@ -54,10 +54,32 @@ struct StepArgs {
 };
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 
+// Chunk summaries and exclusive carries only (no replay) of the gain scan (KDN)
+// or the statistic scan (PKDA): w.carry [B*H, n_chunks_g, nu] holds the
+// recurrence's value at the start of every gain chunk.  scan.cu
+cudaError_t launch_scan_carries(const ForwardArgs& a, const ScanWorkspace& w, cudaStream_t s);
+
 // Fused tensor-core forward (gain scan + compact-WY chunk pass).  chunk_tc.cu
 bool tc_path_supported(int io, int dk, int dv, int chunk);
-cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t s);
-int tc_kernel_count();
+
+// Sequence split of the tensor-core forward for few long sequences: nseg
+// segments of seg_len tokens (a multiple of kGainChunk) per sequence run on
+// separate SMs.  The state map of a segment is affine, S_out = Phi S_in + S_loc;
+// one pass gives every segment's S_loc (from S = 0) and Phi (from S = I, values
+// zero), a short serial pass chains them into each segment's initial state, and
+// a last pass recomputes the segments from their true initial states.
+struct TcSplit {
+    int nseg = 1, seg_len = 0;          // nseg == 1: no split
+    float* summary = nullptr;           // scan workspace (gain chunks of kGainChunk tokens)
+    float* carry = nullptr;
+    int n_chunks_g = 0;
+    float* S_loc = nullptr;             // [B*H*nseg][dk][dv] each
+    float* Phi = nullptr;
+    float* S_in = nullptr;
+};
+TcSplit tc_split_plan(int B, int T, int H, uint32_t flags);   // nseg and seg_len only
+cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStream_t s);
+int tc_kernel_count(int nseg);
 
 // Copy the initial state to the outputs (T == 0).  chunk_simt.cu
 cudaError_t launch_state_copy(const ForwardArgs& a, cudaStream_t s);

@@ -265,7 +265,7 @@ __global__ void gain_replay_pkda(const TIO* __restrict__ k, const float* __restr
 }
 
 template <typename TIO>
-cudaError_t launch_scan_t(const ForwardArgs& a, const ScanWorkspace& w, cudaStream_t s) {
+cudaError_t launch_scan_t(const ForwardArgs& a, const ScanWorkspace& w, bool replay, cudaStream_t s) {
     const TIO* k = static_cast<const TIO*>(a.k);
     const int BH = a.B * a.H, Cg = w.chunk_g, nG = w.n_chunks_g;
     const dim3 grid(BH, nG);
@@ -274,7 +274,8 @@ cudaError_t launch_scan_t(const ForwardArgs& a, const ScanWorkspace& w, cudaStre
         stat_summary_pkda<TIO><<<grid, nt, 0, s>>>(k, a.alpha_p, a.beta_p, a.T, a.H, a.dk, Cg, nG, w.summary);
         const int tot = BH * a.dk;
         mobius_carry<<<(tot + 127) / 128, 128, 0, s>>>(w.summary, a.p0, 0.0f, BH, a.dk, nG, w.carry);
-        gain_replay_pkda<TIO><<<grid, nt, 0, s>>>(k, a.beta, a.alpha_p, a.beta_p, a.center, a.neg_log2x,
+        if (replay)
+            gain_replay_pkda<TIO><<<grid, nt, 0, s>>>(k, a.beta, a.alpha_p, a.beta_p, a.center, a.neg_log2x,
                                                   w.carry, a.T, a.H, a.dk, Cg, nG, w.kappa, a.p_T);
     } else if (a.variant == 0) {
         const int nt = ((a.dk + 31) / 32) * 32;
@@ -282,13 +283,15 @@ cudaError_t launch_scan_t(const ForwardArgs& a, const ScanWorkspace& w, cudaStre
                                                      a.mu, Cg, nG, w.summary);
         const int tot = BH * a.dk;
         mobius_carry<<<(tot + 127) / 128, 128, 0, s>>>(w.summary, a.p0, 1.0f, BH, a.dk, nG, w.carry);
-        gain_replay_diag<TIO><<<grid, nt, 0, s>>>(k, a.log_alpha, a.omega, a.r, w.carry, a.T, a.H,
+        if (replay)
+            gain_replay_diag<TIO><<<grid, nt, 0, s>>>(k, a.log_alpha, a.omega, a.r, w.carry, a.T, a.H,
                                                   a.dk, a.mu, Cg, nG, w.kappa, a.p_T);
     } else {
         mobius_summary_iso<TIO><<<grid, 128, 2 * Cg * sizeof(float), s>>>(
             k, a.log_alpha, a.omega, a.r, a.T, a.H, a.dk, a.mu, Cg, nG, w.summary);
         mobius_carry<<<(BH + 127) / 128, 128, 0, s>>>(w.summary, a.p0, 1.0f, BH, 1, nG, w.carry);
-        gain_replay_iso<TIO><<<grid, 128, 3 * Cg * sizeof(float), s>>>(
+        if (replay)
+            gain_replay_iso<TIO><<<grid, 128, 3 * Cg * sizeof(float), s>>>(
             k, a.log_alpha, a.omega, a.r, w.carry, a.T, a.H, a.dk, a.mu, Cg, nG, w.kappa, a.p_T);
     }
     return cudaGetLastError();
@@ -297,8 +300,13 @@ cudaError_t launch_scan_t(const ForwardArgs& a, const ScanWorkspace& w, cudaStre
 }  // namespace
 
 cudaError_t launch_gain_scan(const ForwardArgs& a, const ScanWorkspace& w, cudaStream_t s) {
-    if (a.io == 1) return launch_scan_t<__nv_bfloat16>(a, w, s);
-    return launch_scan_t<float>(a, w, s);
+    if (a.io == 1) return launch_scan_t<__nv_bfloat16>(a, w, true, s);
+    return launch_scan_t<float>(a, w, true, s);
+}
+
+cudaError_t launch_scan_carries(const ForwardArgs& a, const ScanWorkspace& w, cudaStream_t s) {
+    if (a.io == 1) return launch_scan_t<__nv_bfloat16>(a, w, false, s);
+    return launch_scan_t<float>(a, w, false, s);
 }
 
 }  // namespace kdn
