@@ -92,6 +92,22 @@ typedef enum { KDN_DIAG = 0, KDN_ISO = 1, KDN_PKDA = 2 } kdn_variant;
 #define KDN_FLAG_NO_SPLIT 0x2u   /* tensor-core path: never split sequences into segments */
 
 /*
+ * Sequence split (tensor-core path).  When B*H sequences would leave most of
+ * the GPU idle (2*B*H <= 152) and each is long (T >= 2048), every sequence is
+ * cut into nseg = min(152 / (B*H), T / 1024) segments of a multiple of 256
+ * tokens that run on separate SMs.  The method's state map over a segment is
+ * affine, S_out = Phi S_in + S_loc, for the segment's gains, which depend only
+ * on the uncertainty (statistic) recurrence: a scan over the whole sequence
+ * gives each segment's initial uncertainty, one pass each gives every
+ * segment's S_loc (from S = 0) and Phi (from S = I with zero values), a short
+ * serial pass chains them into each segment's initial state, and a last pass
+ * recomputes the segments from their true states.  The result is the same
+ * recurrence up to rounding; the cost is about three times the arithmetic on
+ * nseg times the SMs.  kdn_workspace_size() includes the per-segment states;
+ * KDN_FLAG_NO_SPLIT keeps one CTA per sequence.
+ */
+
+/*
  * Supported sizes: d_k, d_v in {16, 32, 64, 128}; chunk in {16, 32, 64}
  * (0 selects 64, or T rounded up to 16 when T < 64); any T >= 0 (a ragged
  * tail chunk is masked; T == 0 copies the initial state to the outputs);

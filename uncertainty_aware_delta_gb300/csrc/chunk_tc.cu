@@ -145,7 +145,7 @@ struct TcParams {
     // a ragged tail (past T, where the copies read zeros).
     int nseg, seg_len;
     int s0_identity;      // start from S = I (the segment's transition map) instead of S0
-    int no_v;             // values read as zero
+    int no_v;             // values read as zero (selects the kernel instance)
     int no_o;             // outputs not written
     int last_only;        // final state of the last segment only, to S_T / p_T at bh;
                           // otherwise every CTA writes its final state to S_T at blockIdx.x
@@ -378,8 +378,11 @@ __device__ __noinline__ void strong_decay_factors(const TcParams& P, unsigned ch
     }
 }
 
-template <int V>
+template <int V, int MODE>
 __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_constant__ TcParams P) {
+    // MODE 0: whole sequences; 1: segments of a split sequence; 2: segments with the
+    // values read as zero (a segment's transition map; no v copies)
+    constexpr bool SEG = MODE != 0, NOV = MODE == 2;
     constexpr bool ISO = V == kVarIso, PK = V == kVarPkda;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -395,9 +398,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool wg0 = tid < 128, wg1 = tid >= 128 && tid < 256, wg2 = tid >= 256;
-    const int vs = blockIdx.x, bh = vs / P.nseg, seg = vs % P.nseg, H = P.H, b = bh / H, h = bh % H;
-    const int Tall = P.T, tb = seg * P.seg_len;   // sequence length, first token of the segment
-    const int T = min(P.seg_len, Tall - tb);      // tokens of this CTA's segment
+    const int vs = blockIdx.x, nseg = SEG ? P.nseg : 1;
+    const int bh = SEG ? vs / nseg : vs, seg = SEG ? vs % nseg : 0, H = P.H, b = bh / H, h = bh % H;
+    const int Tall = P.T, tb = SEG ? seg * P.seg_len : 0;   // sequence length, first token of the segment
+    const int T = SEG ? min(P.seg_len, Tall - tb) : Tall;    // tokens of this CTA's segment
     const int nchunks = (T + kC - 1) / kC;
 
     if (tid == 0) {
@@ -440,7 +444,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     // thread 160: q, k, log_alpha, omega)
     int n_in_issued = 0, n_v_issued = 0, n_mma_issued = 0, n_o_issued = 0, n_oj_issued = 0, n_gram_issued = 0,
         n_js_issued = 0;
-    if (tid == 0 && nchunks > 0 && !P.no_v) {
+    if (tid == 0 && nchunks > 0 && !NOV) {
         issue_v(0);
         n_v_issued = 1;
     }
@@ -461,7 +465,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     // PKDA: key statistic of channel tid - 128 (warps 4-7), and the head's centre
     float stat = 0.0f;
     const float center = PK ? P.center[h] : 0.0f;
-    const float* p0v = P.p0 ? P.p0 + bh * P.p0_bh + seg * P.p0_seg : nullptr;
+    const float* p0v = !P.p0 ? nullptr
+                       : SEG ? P.p0 + bh * P.p0_bh + seg * P.p0_seg
+                             : P.p0 + static_cast<size_t>(bh) * (ISO ? 1 : kD);
     if (wg1 && V == kVarDiag && p0v) pn = p0v[tid - 128];
     if (wg1 && PK && p0v) stat = p0v[tid - 128];
     if (ISO && warp == 4 && p0v) b_iso = p0v[0];
@@ -474,7 +480,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 const int i = q * 32 + c;
-                r[c] = __float_as_uint(P.s0_identity ? (i == j ? 1.0f : 0.0f)
+                r[c] = __float_as_uint((SEG && P.s0_identity) ? (i == j ? 1.0f : 0.0f)
                                        : P.S0 ? P.S0[(static_cast<size_t>(vs) * kD + i) * kD + j] : 0.0f);
             }
             tmem_st32(lane_base + TM_S + q * 32, r);
@@ -850,7 +856,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             scale_state(n);
             if (n > 0) {
                 wait_or_abort(bar_oj, pb ^ 1u);   // output update of chunk n-1 has landed
-                if (!P.no_o) emit_outputs(n - 1);
+                if (!(SEG && P.no_o)) emit_outputs(n - 1);
             }
             tc_fence_before();
             named_bar(kBarWG0, 128);
@@ -1076,7 +1082,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             //      is the prediction) -> bf16 A operand in TMEM
             {
                 wait_or_abort(bar_o, pb);
-                if (!P.no_v) wait_or_abort(bar_v, ph_v);
+                if (!NOV) wait_or_abort(bar_v, ph_v);
                 tc_fence_after();
                 uint32_t v0[32], v1[32], pk[32];
                 tmem_ld64(TM_ZD, v0, v1);
@@ -1087,8 +1093,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 for (int e = 0; e < 32; ++e) {
                     const int t = 2 * e;
                     // (no_v: the segment's transition map, values zero)
-                    const float va = P.no_v ? 0.0f : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + sw128_off(t, jc)));
-                    const float vb = P.no_v ? 0.0f : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + sw128_off(t + 1, jc)));
+                    const float va = NOV ? 0.0f : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + sw128_off(t, jc)));
+                    const float vb = NOV ? 0.0f : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + sw128_off(t + 1, jc)));
                     const float za = __uint_as_float(t < 32 ? v0[t] : v1[t - 32]);
                     const float zb = __uint_as_float(t + 1 < 32 ? v0[t + 1] : v1[t + 1 - 32]);
                     pk[e] = pack_bf16(va - za, vb - zb);
@@ -1111,7 +1117,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                                     id_y, ks > 0);
                 mma_commit(bar_mma);
                 ++n_mma_issued;
-                if (n + 1 < nchunks && !P.no_v) {
+                if (n + 1 < nchunks && !NOV) {
                     issue_v(n + 1);
                     ++n_v_issued;
                 }
@@ -1175,15 +1181,15 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     if (!aborted && nchunks > 0) {
         wait_or_abort(bar_mma, static_cast<uint32_t>(nchunks - 1) & 1u);   // update of the last chunk has landed
         wait_or_abort(bar_oj, static_cast<uint32_t>(nchunks - 1) & 1u);
-        if (wg0 && !P.no_o) emit_outputs(nchunks - 1);
+        if (wg0 && !(SEG && P.no_o)) emit_outputs(nchunks - 1);
     }
     if (!*s_abort) {
         // final state: S_T = (TMEM state) scaled by the last chunk's pending factor
         // (sequence split: only the last segment writes the sequence's final state,
         //  unless every segment's final state is wanted, at its CTA index)
-        const bool last = seg == P.nseg - 1;
-        const size_t st_idx = P.last_only ? static_cast<size_t>(bh) : static_cast<size_t>(vs);
-        if (wg0 && (last || !P.last_only)) {
+        const bool last = seg == nseg - 1, last_only = !SEG || P.last_only;
+        const size_t st_idx = last_only ? static_cast<size_t>(bh) : static_cast<size_t>(vs);
+        if (wg0 && (last || !last_only)) {
             tc_fence_after();
             const int j = tid;
 #pragma unroll 1
@@ -1198,7 +1204,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     P.S_T[(st_idx * kD + i) * kD + j] = __uint_as_float(r[c]) * f;
                 }
             }
-        } else if (wg1 && last && P.last_only) {
+        } else if (wg1 && last && last_only) {
             if (V == kVarDiag) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = pn / pd;
             else if (PK) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = stat;
             else if (tid == 128) P.p_T[bh] = b_iso;
@@ -1380,10 +1386,21 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStrea
         kernel<<<grid, kNT, kSmemAlloc, s>>>(P);
         return cudaGetLastError();
     };
+    // kernel instance: whole sequences, segments, or segments without values
     auto run = [&]() {
-        if (a.variant == kVarDiag) return launch(kdn_fused_tc_kernel<kVarDiag>);
-        if (a.variant == kVarIso) return launch(kdn_fused_tc_kernel<kVarIso>);
-        return launch(kdn_fused_tc_kernel<kVarPkda>);
+        if (P.nseg <= 1) {
+            if (a.variant == kVarDiag) return launch(kdn_fused_tc_kernel<kVarDiag, 0>);
+            if (a.variant == kVarIso) return launch(kdn_fused_tc_kernel<kVarIso, 0>);
+            return launch(kdn_fused_tc_kernel<kVarPkda, 0>);
+        }
+        if (P.no_v) {
+            if (a.variant == kVarDiag) return launch(kdn_fused_tc_kernel<kVarDiag, 2>);
+            if (a.variant == kVarIso) return launch(kdn_fused_tc_kernel<kVarIso, 2>);
+            return launch(kdn_fused_tc_kernel<kVarPkda, 2>);
+        }
+        if (a.variant == kVarDiag) return launch(kdn_fused_tc_kernel<kVarDiag, 1>);
+        if (a.variant == kVarIso) return launch(kdn_fused_tc_kernel<kVarIso, 1>);
+        return launch(kdn_fused_tc_kernel<kVarPkda, 1>);
     };
     if (sp.nseg <= 1) return run();
 

@@ -25,11 +25,12 @@
 namespace kdn {
 namespace {
 
+// Exact power-of-two rescale of a matrix with non-negative entries: the largest
+// entry lands in [1, 2) (read from its exponent bits; a zero matrix stays zero).
 __device__ __forceinline__ void renorm4(float& m00, float& m01, float& m10, float& m11) {
     const float mx = fmaxf(fmaxf(m00, m01), fmaxf(m10, m11));
-    int e;
-    frexpf(mx, &e);
-    const float s = ldexpf(1.0f, -e);
+    const int ex = min(max((__float_as_int(mx) >> 23) & 0xff, 1), 253);
+    const float s = __int_as_float((254 - ex) << 23);   // 2^(127 - ex)
     m00 *= s; m01 *= s; m10 *= s; m11 *= s;
 }
 
@@ -44,6 +45,9 @@ __global__ void mobius_summary_diag(const TIO* __restrict__ k, const float* __re
     if (i >= dk) return;
     const int t0 = c * Cg, t1 = min(Tn, t0 + Cg);
     float m00 = 1.f, m01 = 0.f, m10 = 0.f, m11 = 1.f;
+    // (the loads of a few tokens are independent of the product: unrolled, they
+    //  are issued ahead of it)
+#pragma unroll 4
     for (int t = t0; t < t1; ++t) {
         const size_t th = ((size_t)b * Tn + t) * H + h;
         const float kv = IO<TIO>::load(k, th * dk + i);
@@ -68,10 +72,24 @@ __global__ void mobius_carry(const float* __restrict__ summary, const float* __r
     if (e >= BH * nu) return;
     const int bh = e / nu, i = e % nu;
     float p = p0 ? p0[e] : p_default;
-    for (int c = 0; c < nG; ++c) {
+    const float4* sm4 = reinterpret_cast<const float4*>(summary);
+    // the chunk summaries do not depend on the carry: load eight ahead of the chain
+    constexpr int kAhead = 8;
+    int c = 0;
+    for (; c + kAhead <= nG; c += kAhead) {
+        float4 m[kAhead];
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) m[u] = sm4[((size_t)bh * nG + c + u) * nu + i];
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            carry[((size_t)bh * nG + c + u) * nu + i] = p;
+            p = (m[u].x * p + m[u].y) / (m[u].z * p + m[u].w);
+        }
+    }
+    for (; c < nG; ++c) {
         const size_t idx = ((size_t)bh * nG + c) * nu + i;
         carry[idx] = p;
-        const float4 m = reinterpret_cast<const float4*>(summary)[idx];
+        const float4 m = sm4[idx];
         p = (m.x * p + m.y) / (m.z * p + m.w);
     }
 }
@@ -231,6 +249,7 @@ __global__ void stat_summary_pkda(const TIO* __restrict__ k, const float* __rest
     if (i >= dk) return;
     const int t0 = c * Cg, t1 = min(Tn, t0 + Cg);
     float prod = 1.0f, acc = 0.0f;
+#pragma unroll 4
     for (int t = t0; t < t1; ++t) {
         const size_t th = ((size_t)b * Tn + t) * H + h;
         const float kv = IO<TIO>::load(k, th * dk + i);
