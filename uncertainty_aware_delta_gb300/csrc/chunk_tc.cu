@@ -103,9 +103,12 @@ constexpr uint32_t OFF_SMALL = 219648;
 constexpr int kLDF = 68;
 constexpr int kLDX = 36;
 // small region, float offsets
-constexpr int SM_R = 0, SM_MUR = 64, SM_BHAT = 128, SM_ZP = 192, SM_AP = 448, SM_RZ = 704 /* [2][64] */,
-              SM_FOUT = 832, SM_OMI = 960, SM_FLAG = 1024, SM_CF = 1032 /* [2][128] by chunk parity */,
-              SM_INVD = 1288, SM_CF2 = 1352 /* [128] */, SM_FLOATS = 1480;
+// (buffers marked [2] are indexed by chunk parity; ZP and AP hold the isotropic
+//  per-token sums of k^2 and alpha^2 as four per-warp partial sums)
+constexpr int SM_R = 0, SM_MUR = 64, SM_OMB = 128 /* [2][64] */, SM_ZP = 256 /* [2][256] */,
+              SM_AP = 768 /* [2][256] */, SM_RZ = 1280 /* [2][64] */, SM_FOUT = 1408, SM_OMI = 1536,
+              SM_FLAG = 1600, SM_CF = 1608 /* [2][128] */, SM_INVD = 1864, SM_CF2 = 1928 /* [128] */,
+              SM_FLOATS = 2056;
 constexpr uint32_t OFF_BAR = OFF_SMALL + SM_FLOATS * 4;
 constexpr uint32_t kSmemBytes = OFF_BAR + 80;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
@@ -461,7 +464,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     // pd renormalised to [1, 2) by powers of two
     float pn = 1.0f, pd = 1.0f;
     float pend2 = 0.0f;   // pending log2-factor of the previous chunk, (G_C - G_ref) log2(e) (warps 4-7)
-    float b_iso = 1.0f;   // isotropic scalar variance (warp 4)
+    float b_iso = 1.0f;   // isotropic scalar variance (warp 11)
     // PKDA: key statistic of channel tid - 128 (warps 4-7), and the head's centre
     float stat = 0.0f;
     const float center = PK ? P.center[h] : 0.0f;
@@ -470,7 +473,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                              : P.p0 + static_cast<size_t>(bh) * (ISO ? 1 : kD);
     if (wg1 && V == kVarDiag && p0v) pn = p0v[tid - 128];
     if (wg1 && PK && p0v) stat = p0v[tid - 128];
-    if (ISO && warp == 4 && p0v) b_iso = p0v[0];
+    if (ISO && warp == 11 && p0v) b_iso = p0v[0];
     // initial state S^T into TMEM: lane j = value column, columns = key channel
     if (wg0) {
         const int j = tid;
@@ -555,6 +558,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 sm[SM_RZ + (c & 1) * 64 + t] = rr;
                 sm[SM_MUR + t] = P.mu / rr;
                 sm[SM_OMI + t] = om;
+                if (ISO) sm[SM_OMB + (c & 1) * 64 + t] = om;
             }
         }
         wait_or_abort(bar_la, ph_in);
@@ -689,8 +693,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 }
             }
             if (ISO) {
-                sm[SM_ZP + w4 * 64 + hf * 32 + lane] = butterfly_sum32(w, lane);
-                sm[SM_AP + w4 * 64 + hf * 32 + lane] = butterfly_sum32(w2, lane);
+                sm[SM_ZP + (c & 1) * 256 + w4 * 64 + hf * 32 + lane] = butterfly_sum32(w, lane);
+                sm[SM_AP + (c & 1) * 256 + w4 * 64 + hf * 32 + lane] = butterfly_sum32(w2, lane);
             }
         }
         {
@@ -715,61 +719,69 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             pend2 = G2C - R2;
             sm[SM_FOUT + i] = ex2(pend2);
         }
-        if (ISO) {
-            named_bar(kBarWG1, 128);
-            if (w4 == 0) {
-                // Moebius scan of the scalar recurrence over the chunk, 2 tokens per lane
-                float aa[2], uu[2], oo[2], kk[2], rr[2];
-                Mob m[2];
+        return split;
+    };
+
+    // Isotropic: the scalar variance recurrence of chunk c (warp 11, after the operand
+    // pass, beside the Gram MMA).  The write keys K_til' = k / e1 carry no b_hat, so
+    // b_hat_s scales column s of the Gram matrix; dividing row t of the triangular
+    // system by b_hat_t instead gives the diagonal z_t / b_hat_t = r_t / b_hat_t +
+    // ||k_t||^2 (the Gram diagonal is ||k_t||^2) and innovations multiplied by b_hat_t,
+    // which the update and query-write products then take with the unscaled keys.
+    // So b_hat enters only as r_t / b_hat_t in the diagonal, written here.
+    auto iso_scan = [&](int c, int nvc) {
+        const float* zp = sm + SM_ZP + (c & 1) * 256;
+        const float* ap = sm + SM_AP + (c & 1) * 256;
+        float* rz = sm + SM_RZ + (c & 1) * 64;
+        // Moebius scan over the chunk, 2 tokens per lane
+        float aa[2], uu[2], oo[2], rr[2];
+        Mob m[2];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = 2 * lane + e;
-                    const float asum = sm[SM_AP + t] + sm[SM_AP + 64 + t] + sm[SM_AP + 128 + t] + sm[SM_AP + 192 + t];
-                    kk[e] = sm[SM_ZP + t] + sm[SM_ZP + 64 + t] + sm[SM_ZP + 128 + t] + sm[SM_ZP + 192 + t];
-                    aa[e] = asum * (1.0f / kD);
-                    rr[e] = sm[SM_R + t];
-                    oo[e] = sm[SM_OMI + t];
-                    uu[e] = __fdividef(P.mu * kk[e], kD * rr[e]);
-                    if (t < nvc)
-                        m[e] = {aa[e], oo[e], uu[e] * aa[e], fmaf(uu[e], oo[e], 1.0f)};
-                    else
-                        m[e] = {1.0f, 0.0f, 0.0f, 1.0f};
-                }
-                Mob pr = mob_mul(m[1], m[0]);
+        for (int e = 0; e < 2; ++e) {
+            const int t = 2 * lane + e;
+            const float kk = zp[t] + zp[64 + t] + zp[128 + t] + zp[192 + t];
+            aa[e] = (ap[t] + ap[64 + t] + ap[128 + t] + ap[192 + t]) * (1.0f / kD);
+            rr[e] = rz[t];
+            oo[e] = sm[SM_OMB + (c & 1) * 64 + t];
+            uu[e] = __fdividef(P.mu * kk, kD * rr[e]);
+            if (t < nvc)
+                m[e] = {aa[e], oo[e], uu[e] * aa[e], fmaf(uu[e], oo[e], 1.0f)};
+            else
+                m[e] = {1.0f, 0.0f, 0.0f, 1.0f};
+        }
+        Mob pr = mob_mul(m[1], m[0]);
+        mob_renorm(pr);
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            Mob q;
+            q.a = __shfl_up_sync(0xffffffffu, pr.a, d);
+            q.b = __shfl_up_sync(0xffffffffu, pr.b, d);
+            q.c = __shfl_up_sync(0xffffffffu, pr.c, d);
+            q.d = __shfl_up_sync(0xffffffffu, pr.d, d);
+            if (lane >= d) {
+                pr = mob_mul(pr, q);
                 mob_renorm(pr);
-#pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    Mob q;
-                    q.a = __shfl_up_sync(0xffffffffu, pr.a, d);
-                    q.b = __shfl_up_sync(0xffffffffu, pr.b, d);
-                    q.c = __shfl_up_sync(0xffffffffu, pr.c, d);
-                    q.d = __shfl_up_sync(0xffffffffu, pr.d, d);
-                    if (lane >= d) {
-                        pr = mob_mul(pr, q);
-                        mob_renorm(pr);
-                    }
-                }
-                Mob ex;
-                ex.a = __shfl_up_sync(0xffffffffu, pr.a, 1);
-                ex.b = __shfl_up_sync(0xffffffffu, pr.b, 1);
-                ex.c = __shfl_up_sync(0xffffffffu, pr.c, 1);
-                ex.d = __shfl_up_sync(0xffffffffu, pr.d, 1);
-                if (lane == 0) ex = {1.0f, 0.0f, 0.0f, 1.0f};
-                float bb = __fdividef(fmaf(ex.a, b_iso, ex.b), fmaf(ex.c, b_iso, ex.d));
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = 2 * lane + e;
-                    float bhat = 0.0f;
-                    if (t < nvc) {
-                        bhat = fmaf(aa[e], bb, oo[e]);
-                        bb = __fdividef(bhat, fmaf(uu[e], bhat, 1.0f));
-                    }
-                    sm[SM_BHAT + t] = bhat;
-                }
-                b_iso = __shfl_sync(0xffffffffu, bb, 31);
             }
         }
-        return split;
+        Mob ex;
+        ex.a = __shfl_up_sync(0xffffffffu, pr.a, 1);
+        ex.b = __shfl_up_sync(0xffffffffu, pr.b, 1);
+        ex.c = __shfl_up_sync(0xffffffffu, pr.c, 1);
+        ex.d = __shfl_up_sync(0xffffffffu, pr.d, 1);
+        if (lane == 0) ex = {1.0f, 0.0f, 0.0f, 1.0f};
+        float bb = __fdividef(fmaf(ex.a, b_iso, ex.b), fmaf(ex.c, b_iso, ex.d));
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = 2 * lane + e;
+            if (t < nvc) {
+                const float bhat = fmaf(aa[e], bb, oo[e]);
+                bb = __fdividef(bhat, fmaf(uu[e], bhat, 1.0f));
+                // b_hat = 0 (no prior variance, no process noise): a large finite
+                // diagonal gives a zero innovation, the zero gain
+                rz[t] = __fdividef(rr[e], fmaxf(bhat, 1e-30f));
+            }
+        }
+        b_iso = __shfl_sync(0xffffffffu, bb, 31);
     };
 
     // ------------------------------------------------------------------ warps 0-3
@@ -877,7 +889,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         } else {
             // decayed bf16 operands (warps 4-11): thread -> 4 channels in each K-atom
             // (8-byte pieces of the swizzled rows), 16 threads (half a warp) per token row.
-            // K_til' = p_hat k / e1 (isotropic: b_hat k / e1); the gain denominator enters
+            // K_til' = p_hat k / e1 (isotropic: k / e1); the gain denominator enters
             // through the diagonal of the triangular system.
             const int u = tid - 128, g = u & 15, tr = u >> 4;
             wait_or_abort(bar_q, pb);   // q of chunk n
@@ -885,7 +897,6 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             for (int m4 = 0; m4 < 4; ++m4) {
                 const int t = tr + 16 * m4;
                 const uint32_t sw = sw128_off(t, g >> 1) + (g & 1) * 8;
-                const float sc = ISO ? sm[SM_BHAT + t] : 1.0f;
                 float kb[8], qb[8], kt[8];
 #pragma unroll
                 for (int a = 0; a < 2; ++a) {
@@ -920,8 +931,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     *reinterpret_cast<uint2*>(base + OFF_KQ + a * 16384 + 8192 + sw) =
                         make_uint2(pack_bf16(qb[4 * a], qb[4 * a + 1]), pack_bf16(qb[4 * a + 2], qb[4 * a + 3]));
                     *reinterpret_cast<uint2*>(base + OFF_KT + a * 8192 + sw) =
-                        make_uint2(pack_bf16(kt[4 * a] * sc, kt[4 * a + 1] * sc),
-                                   pack_bf16(kt[4 * a + 2] * sc, kt[4 * a + 3] * sc));
+                        make_uint2(pack_bf16(kt[4 * a], kt[4 * a + 1]), pack_bf16(kt[4 * a + 2], kt[4 * a + 3]));
                 }
             }
             fence_proxy_async();
@@ -951,6 +961,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         if (wg2) {
             // ---- Gram rows out of TMEM: M (fp32), query-write matrix A' (bf16)
             const int lt = tid - 256, lw = warp - 8;
+            if (ISO) {   // gain denominators of chunk n, while the Gram MMA runs
+                if (lw == 3) iso_scan(n, nv);
+                named_bar(kBarWG2, 128);
+            }
             {
                 wait_or_abort(bar_mma, pb);
                 if (n > 0) wait_or_abort(bar_oj, pb ^ 1u);   // A' of chunk n-1 has been read
@@ -1207,7 +1221,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         } else if (wg1 && last && last_only) {
             if (V == kVarDiag) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = pn / pd;
             else if (PK) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = stat;
-            else if (tid == 128) P.p_T[bh] = b_iso;
+        } else if (ISO && tid == 352 && last && last_only) {
+            P.p_T[bh] = b_iso;
         }
     }
     int* s_ngram = reinterpret_cast<int*>(sm + SM_FLAG + 1);
