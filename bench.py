@@ -511,19 +511,20 @@ def other_workloads(torch, kdn, WORKLOADS, device, barrier, peaks):
         x = device_inputs(torch, w, variant, w.seed, device)
         fwd = kdn.kdn_diag_forward if variant == "diag" else kdn.kdn_iso_forward
         ms = time_calls(torch, lambda: fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"],
-                                           chunk=w.chunk), 5, 2, barrier)
+                                           chunk=w.chunk), 20, 5, barrier)
         ab = algorithmic_bytes(w.B, w.T, w.H, w.d, w.d, w.io, variant)
         out[name] = {"tokens_per_s": w.B * w.T / (ms / 1e3), "ms": ms,
-                     "hbm_frac": ab / (ms / 1e3) / 1e9 / hbm}
+                     "hbm_frac": ab / (ms / 1e3) / 1e9 / hbm, "algorithmic_bytes": ab,
+                     "traffic": traffic_for("kdn_fused_tc_kernel", name)}
         del x
     # PKDA (preconditioned delta rule with per-channel decay) on the headline shape
     w = WORKLOADS["pkda-bf16-b8h16t4096d128"]
     x = device_pkda_inputs(torch, w, w.seed, device)
     names = ("q", "k", "v", "log_alpha", "beta", "alpha_p", "beta_p", "center")
-    ms = time_calls(torch, lambda: kdn.kdn_pkda_forward(*(x[n] for n in names), chunk=w.chunk), 5, 2, barrier)
+    ms = time_calls(torch, lambda: kdn.kdn_pkda_forward(*(x[n] for n in names), chunk=w.chunk), 20, 5, barrier)
     ab = pkda_algorithmic_bytes(w.B, w.T, w.H, w.d, w.d, w.io)
     out[w.name] = {"tokens_per_s": w.B * w.T / (ms / 1e3), "ms": ms, "hbm_frac": ab / (ms / 1e3) / 1e9 / hbm,
-                   "algorithmic_bytes": ab}
+                   "algorithmic_bytes": ab, "traffic": traffic_for("kdn_fused_tc_kernel", w.name)}
     del x
     # decode: 512-token prefill through the forward path, then 1024 single-token steps
     w = WORKLOADS["diag-decode-f32-s256h16d128"]

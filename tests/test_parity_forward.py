@@ -258,6 +258,30 @@ def test_tensor_core_path_strong_decay(variant):
     _check(variant, x, got, ref, "bf16", "strong decay")
 
 
+@pytest.mark.parametrize("variant", ["diag", "iso"])
+def test_tensor_core_path_zero_prior_variance(variant):
+    """p_0 = 0 with no process noise on head 0: every gain of that head is zero
+    (the isotropic kernel takes its prior variance b_hat into the triangular
+    system as r / b_hat, here with b_hat = 0), so its state only decays and its
+    final variance stays 0; head 1 runs with an ordinary prior beside it."""
+    import torch
+
+    kdn = _kdn()
+    B, T, H = 1, 150, 2
+    x = make_inputs(variant, B, T, H, 128, 128, io="bf16", seed=31)
+    x["omega"][:, :, 0] = 0.0
+    rng = np.random.default_rng(31)
+    S0 = (0.5 * rng.standard_normal((B, H, 128, 128))).astype(np.float32)
+    p0 = np.ones((B, H, 128) if variant == "diag" else (B, H), dtype=np.float32)
+    p0[:, 0] = 0.0
+    t = to_device(x)
+    ref = oracle.forward(variant, x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"], S0=S0, p0=p0)
+    got = _run(kdn, variant, t, S0=torch.from_numpy(S0).cuda(), p0=torch.from_numpy(p0).cuda(), chunk=64)
+    _check(variant, x, got, ref, "bf16", "zero prior variance")
+    assert np.all(to_host(got[2])[:, 0] == 0.0)
+    assert np.all(np.isfinite(to_host(got[0]))) and np.all(np.isfinite(to_host(got[1])))
+
+
 # ------------------------------------------------------------ sequence split
 SPLIT_CASES = [
     # variant, B, T, H, with an initial state: few long sequences -> segments on separate SMs
