@@ -98,13 +98,16 @@ typedef enum { KDN_DIAG = 0, KDN_ISO = 1, KDN_PKDA = 2 } kdn_variant;
  * tokens that run on separate SMs.  The method's state map over a segment is
  * affine, S_out = Phi S_in + S_loc, for the segment's gains, which depend only
  * on the uncertainty (statistic) recurrence: a scan over the whole sequence
- * gives each segment's initial uncertainty, one pass each gives every
- * segment's S_loc (from S = 0) and Phi (from S = I with zero values), a short
- * serial pass chains them into each segment's initial state, and a last pass
- * recomputes the segments from their true states.  The result is the same
- * recurrence up to rounding; the cost is about three times the arithmetic on
- * nseg times the SMs.  kdn_workspace_size() includes the per-segment states;
- * KDN_FLAG_NO_SPLIT keeps one CTA per sequence.
+ * gives each segment's initial uncertainty; one pass from S = 0 gives every
+ * segment's S_loc and its outputs o_loc, one from S = I with zero values gives
+ * Phi and the transformed queries Phi_t^T q_t; a short serial pass chains the
+ * maps into each segment's initial state S_in and the final state, and the
+ * outputs are completed as o_t = o_loc,t + S_in^T (Phi_t^T q_t).  The result is
+ * the same recurrence up to rounding (the correction term is formed with bf16
+ * operands); the cost is about twice the arithmetic on nseg times the SMs.
+ * kdn_workspace_size() includes the per-segment states and the transformed
+ * queries (2 bytes per token-head-channel); KDN_FLAG_NO_SPLIT keeps one CTA per
+ * sequence.
  */
 
 /*

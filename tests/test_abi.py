@@ -87,8 +87,9 @@ def test_forward_kernel_count(lib):
 
 def test_sequence_split_plan(lib):
     """Few long sequences on the tensor-core path run as segments (scan carries,
-    segment maps, chaining, segments: 6 launches) with their state maps in the
-    workspace; many sequences, short ones or the opt-out flag keep one launch."""
+    segment maps, chaining, output correction: 6 launches) with their state maps
+    and transformed queries in the workspace; many sequences, short ones or the
+    opt-out flag keep one launch."""
     import uncertainty_aware_delta_gb300 as kdn
 
     kc, ws = kdn.forward_kernel_count, kdn.workspace_size
@@ -102,8 +103,9 @@ def test_sequence_split_plan(lib):
         assert kc(v, 1, 2048, 2, 128, 128, 64, 1, 0) == 6
         nu = 1 if v == 1 else 128
         n_split, n_whole = ws(v, 1, 65536, 16, 128, 128, 64, 1, 0), ws(v, 1, 65536, 16, 128, 128, 64, 1, NO)
-        # three [16 x 9][128][128] fp32 state arrays and the scan summaries and carries (256 gain chunks)
-        assert n_split - n_whole >= 4 * (3 * 16 * 9 * 128 * 128 + 5 * 16 * 256 * nu)
+        # three [16 x 9][128][128] fp32 state arrays, the scan summaries and carries (256 gain
+        # chunks) and the transformed queries (bf16, one per token-head)
+        assert n_split - n_whole >= 4 * (3 * 16 * 9 * 128 * 128 + 5 * 16 * 256 * nu) + 2 * 65536 * 16 * 128
         assert ws(v, 8, 4096, 16, 128, 128, 64, 1, 0) == ws(v, 8, 4096, 16, 128, 128, 64, 1, NO)
 
 

@@ -51,7 +51,7 @@ struct WsLayout {
     int nG;
     // tensor-core sequence split: per-segment state maps and initial states
     kdn::TcSplit split;
-    size_t sloc_off, phi_off, sin_off;
+    size_t sloc_off, phi_off, sin_off, qt_off;
 };
 
 WsLayout ws_layout(int variant, int B, int T, int H, int dk, int dv, int chunk, int io,
@@ -85,6 +85,8 @@ WsLayout ws_layout(int variant, int B, int T, int H, int dk, int dv, int chunk, 
             off = align_up(off + sizeof(float) * nst);
             w.sin_off = off;
             off = align_up(off + sizeof(float) * nst);
+            w.qt_off = off;   // bf16 [B, T, H, dk]
+            off = align_up(off + 2 * (size_t)B * T * H * dk);
         }
     }
     w.total = off;
@@ -181,6 +183,7 @@ kdn_status forward_impl(int variant, int B, int T, int H, int dk, int dv, int ch
             sp.S_loc = reinterpret_cast<float*>(base + w.sloc_off);
             sp.Phi = reinterpret_cast<float*>(base + w.phi_off);
             sp.S_in = reinterpret_cast<float*>(base + w.sin_off);
+            sp.qt = base + w.qt_off;
         }
         e = kdn::launch_forward_tc(a, sp, s);
     } else {

@@ -1200,7 +1200,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     if (!*s_abort) {
         // final state: S_T = (TMEM state) scaled by the last chunk's pending factor
         // (sequence split: only the last segment writes the sequence's final state,
-        //  unless every segment's final state is wanted, at its CTA index)
+        //  unless every segment's final state is wanted, at its CTA index; the
+        //  final variances come from the last segment when p_T is given)
         const bool last = seg == nseg - 1, last_only = !SEG || P.last_only;
         const size_t st_idx = last_only ? static_cast<size_t>(bh) : static_cast<size_t>(vs);
         if (wg0 && (last || !last_only)) {
@@ -1218,10 +1219,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     P.S_T[(st_idx * kD + i) * kD + j] = __uint_as_float(r[c]) * f;
                 }
             }
-        } else if (wg1 && last && last_only) {
+        } else if (wg1 && last && P.p_T) {
             if (V == kVarDiag) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = pn / pd;
             else if (PK) P.p_T[static_cast<size_t>(bh) * kD + tid - 128] = stat;
-        } else if (ISO && tid == 352 && last && last_only) {
+        } else if (ISO && tid == 352 && last && P.p_T) {
             P.p_T[bh] = b_iso;
         }
     }
@@ -1257,10 +1258,12 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 // S_in(s + 1) = Phi_s S_in(s) + S_loc(s), all [B*H*nseg][128][128] fp32.  Grid
 // (B*H, 128 / 16), 256 threads: a CTA owns 16 value columns of the state and walks
 // the segments in order; thread (row i, 8 columns) forms its part of each product.
-__global__ void __launch_bounds__(256) segment_states_kernel(const float* __restrict__ S0,
+// After the last segment it writes the sequence's final state (S_T may be S0: a CTA
+// reads its columns of S0 before it writes them).
+__global__ void __launch_bounds__(256) segment_states_kernel(const float* S0,
                                                               const float* __restrict__ Phi,
                                                               const float* __restrict__ S_loc,
-                                                              float* __restrict__ S_in, int nseg) {
+                                                              float* __restrict__ S_in, float* S_T, int nseg) {
     __shared__ float cur[kD][17];
     const int bh = blockIdx.x, cb = blockIdx.y * 16, tid = threadIdx.x;
     for (int e = tid; e < kD * 16; e += 256) {
@@ -1274,7 +1277,6 @@ __global__ void __launch_bounds__(256) segment_states_kernel(const float* __rest
         float* out = S_in + mb + static_cast<size_t>(i) * kD + cb + j0;
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) out[jj] = cur[i][j0 + jj];
-        if (sg == nseg - 1) break;
         float acc[8];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) acc[jj] = S_loc[mb + static_cast<size_t>(i) * kD + cb + j0 + jj];
@@ -1288,10 +1290,107 @@ __global__ void __launch_bounds__(256) segment_states_kernel(const float* __rest
                                fmaf(f.y, cur[4 * k4 + 1][j0 + jj],
                                     fmaf(f.z, cur[4 * k4 + 2][j0 + jj], fmaf(f.w, cur[4 * k4 + 3][j0 + jj], acc[jj]))));
         }
+        if (sg == nseg - 1) {
+            float* st = S_T + (static_cast<size_t>(bh) * kD + i) * kD + cb + j0;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) st[jj] = acc[jj];
+            break;
+        }
         __syncthreads();
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) cur[i][j0 + jj] = acc[jj];
         __syncthreads();
+    }
+}
+
+// Output correction of a split sequence.  The outputs of a segment are linear in
+// its initial state: o_t = S_t^T q_t with S_t = Phi_t S_in + S_loc,t, so
+// o_t = o_loc,t + S_in^T (Phi_t^T q_t).  The pass from S = 0 writes o_loc into o;
+// the pass from S = I with zero values writes q~_t = Phi_t^T q_t (its own outputs);
+// this kernel adds S_in^T q~_t once the chained initial states S_in are known.
+// CTA: (group of kCorrTiles 128-token tiles, segment, b*h), 256 threads; warp w owns
+// rows 16w..16w+15 of a tile and all 128 value columns.  bf16 operands (S_in rounded
+// to bf16 as in the state's bf16 copy that the fused kernel multiplies by), fp32
+// accumulation, warp-level m16n8k16 MMAs from shared memory.
+constexpr int kCorrRows = 128, kCorrTiles = 4, kCorrLd = kD + 8;   // +8: conflict-free ldmatrix rows
+constexpr int kCorrSmem = 2 * kCorrRows * kCorrLd * 2;
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const __nv_bfloat16* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(256) segment_output_correction_kernel(const float* __restrict__ S_in,
+                                                                        const __nv_bfloat16* __restrict__ qt,
+                                                                        __nv_bfloat16* __restrict__ o, int T,
+                                                                        int H, int nseg, int seg_len,
+                                                                        int skip_first) {
+    extern __shared__ __align__(16) unsigned char corr_smem[];
+    __nv_bfloat16* As = reinterpret_cast<__nv_bfloat16*>(corr_smem);   // q~ rows [t][i]
+    __nv_bfloat16* Bs = As + kCorrRows * kCorrLd;                       // S_in^T [j][i]
+    const int bh = blockIdx.z, seg = blockIdx.y, b = bh / H, h = bh % H;
+    if (seg == 0 && skip_first) return;   // the first segment starts from S = 0
+    const int tb = seg * seg_len, Ts = min(seg_len, T - tb);
+    const int r0 = blockIdx.x * kCorrTiles * kCorrRows;
+    if (r0 >= Ts) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const float* S = S_in + (static_cast<size_t>(bh) * nseg + seg) * kD * kD;
+    for (int e = tid; e < kD * kD / 4; e += 256) {
+        const int i = e >> 5, j = (e & 31) * 4;
+        const float4 f = *reinterpret_cast<const float4*>(S + i * kD + j);
+        Bs[(j + 0) * kCorrLd + i] = __float2bfloat16_rn(f.x);
+        Bs[(j + 1) * kCorrLd + i] = __float2bfloat16_rn(f.y);
+        Bs[(j + 2) * kCorrLd + i] = __float2bfloat16_rn(f.z);
+        Bs[(j + 3) * kCorrLd + i] = __float2bfloat16_rn(f.w);
+    }
+    const size_t ts = static_cast<size_t>(H) * kD;   // token stride of [B, T, H, d]
+    const size_t row0 = (static_cast<size_t>(b) * T + tb) * ts + static_cast<size_t>(h) * kD;
+    const int g = lane >> 2, q = lane & 3;
+    for (int tile = 0; tile < kCorrTiles; ++tile) {
+        const int rt = r0 + tile * kCorrRows;
+        if (rt >= Ts) break;
+        __syncthreads();   // S_in^T is in place (first tile), the previous tile's rows are read
+        for (int e = tid; e < kCorrRows * (kD / 8); e += 256) {   // 16-byte pieces, 16 per row
+            const int r = e >> 4, c = (e & 15) * 8;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (rt + r < Ts) v = __ldg(reinterpret_cast<const uint4*>(qt + row0 + (rt + r) * ts + c));
+            *reinterpret_cast<uint4*>(As + r * kCorrLd + c) = v;
+        }
+        __syncthreads();
+        float acc[16][4];
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            uint32_t a[4];
+            ldmatrix_x4(a, As + (16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8) * kCorrLd + 16 * ks + (lane >> 4) * 8);
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {   // value columns 16 np .. 16 np + 15
+                uint32_t bb[4];
+                ldmatrix_x4(bb, Bs + (16 * np + (lane & 7) + (lane >> 4) * 8) * kCorrLd + 16 * ks + ((lane >> 3) & 1) * 8);
+                mma_bf16_16816(acc[2 * np], a, bb[0], bb[1]);
+                mma_bf16_16816(acc[2 * np + 1], a, bb[2], bb[3]);
+            }
+        }
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const int r = 16 * warp + g + 8 * hr;
+            if (rt + r >= Ts) continue;
+            __nv_bfloat16* orow = o + row0 + (rt + r) * ts;
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt) {
+                __nv_bfloat162* pp = reinterpret_cast<__nv_bfloat162*>(orow + 8 * nt + 2 * q);
+                const float2 cur = __bfloat1622float2(*pp);
+                *pp = __floats2bfloat162_rn(cur.x + acc[nt][2 * hr], cur.y + acc[nt][2 * hr + 1]);
+            }
+        }
     }
 }
 
@@ -1357,7 +1456,7 @@ TcSplit tc_split_plan(int B, int T, int H, uint32_t flags) {
     return sp;
 }
 
-// carries (2 launches), segment maps (2), chaining (1), segments (1)
+// carries (2 launches), segment maps (2), chaining (1), output correction (1)
 int tc_kernel_count(int nseg) { return nseg > 1 ? 6 : 1; }
 
 cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStream_t s) {
@@ -1434,28 +1533,32 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStrea
     P.p0_bh = static_cast<long long>(sp.n_chunks_g) * nu;
     P.p0_seg = static_cast<long long>(sp.seg_len / kGainChunk) * nu;
     grid = a.B * a.H * sp.nseg;
-    // ---- each segment's affine state map: S_loc from S = 0, Phi from S = I with zero values
+    // ---- each segment's affine state map: S_loc (and the outputs o_loc) from S = 0,
+    //      Phi (and q~_t = Phi_t^T q_t) from S = I with zero values; the last
+    //      segment's pass from S = 0 also gives the final variances
     P.S0 = nullptr;
-    P.no_o = 1;
     P.last_only = 0;
     P.S_T = sp.S_loc;
-    P.p_T = nullptr;
+    P.p_T = a.p_T;
     if ((e = run()) != cudaSuccess) return e;
     P.s0_identity = 1;
     P.no_v = 1;
     P.S_T = sp.Phi;
+    P.p_T = nullptr;
+    P.o = static_cast<__nv_bfloat16*>(sp.qt);
     if ((e = run()) != cudaSuccess) return e;
-    // ---- chained initial states, then the segments from their true states
-    segment_states_kernel<<<dim3(a.B * a.H, kD / 16), 256, 0, s>>>(a.S0, sp.Phi, sp.S_loc, sp.S_in, sp.nseg);
+    // ---- chained initial states and the final state, then o += S_in^T q~
+    segment_states_kernel<<<dim3(a.B * a.H, kD / 16), 256, 0, s>>>(a.S0, sp.Phi, sp.S_loc, sp.S_in, a.S_T,
+                                                                      sp.nseg);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    P.S0 = sp.S_in;
-    P.s0_identity = 0;
-    P.no_v = 0;
-    P.no_o = 0;
-    P.last_only = 1;
-    P.S_T = a.S_T;
-    P.p_T = a.p_T;
-    return run();
+    e = cudaFuncSetAttribute(segment_output_correction_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kCorrSmem);
+    if (e != cudaSuccess) return e;
+    const int groups = (sp.seg_len + kCorrTiles * kCorrRows - 1) / (kCorrTiles * kCorrRows);
+    segment_output_correction_kernel<<<dim3(groups, sp.nseg, a.B * a.H), 256, kCorrSmem, s>>>(
+        sp.S_in, static_cast<const __nv_bfloat16*>(sp.qt), static_cast<__nv_bfloat16*>(a.o), a.T, a.H, sp.nseg,
+        sp.seg_len, a.S0 == nullptr ? 1 : 0);
+    return cudaGetLastError();
 }
 
 }  // namespace kdn

@@ -76,6 +76,7 @@ struct TcSplit {
     float* S_loc = nullptr;             // [B*H*nseg][dk][dv] each
     float* Phi = nullptr;
     float* S_in = nullptr;
+    void* qt = nullptr;                 // [B][T][H][dk] bf16: q~_t = Phi_t^T q_t of each segment
 };
 TcSplit tc_split_plan(int B, int T, int H, uint32_t flags);   // nseg and seg_len only
 cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStream_t s);
