@@ -1258,12 +1258,15 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
 // S_in(s + 1) = Phi_s S_in(s) + S_loc(s), all [B*H*nseg][128][128] fp32.  Grid
 // (B*H, 128 / 16), 256 threads: a CTA owns 16 value columns of the state and walks
 // the segments in order; thread (row i, 8 columns) forms its part of each product.
-// After the last segment it writes the sequence's final state (S_T may be S0: a CTA
-// reads its columns of S0 before it writes them).
+// Each segment's initial state goes out transposed in bf16, S_in^T [j][i] (the B
+// operand of the output correction); after the last segment the CTA writes the
+// sequence's final state (S_T may be S0: a CTA reads its columns of S0 before it
+// writes them).
 __global__ void __launch_bounds__(256) segment_states_kernel(const float* S0,
                                                               const float* __restrict__ Phi,
                                                               const float* __restrict__ S_loc,
-                                                              float* __restrict__ S_in, float* S_T, int nseg) {
+                                                              __nv_bfloat16* __restrict__ S_inT, float* S_T,
+                                                              int nseg) {
     __shared__ float cur[kD][17];
     const int bh = blockIdx.x, cb = blockIdx.y * 16, tid = threadIdx.x;
     for (int e = tid; e < kD * 16; e += 256) {
@@ -1274,9 +1277,12 @@ __global__ void __launch_bounds__(256) segment_states_kernel(const float* S0,
     const int i = tid >> 1, j0 = (tid & 1) * 8;
     for (int sg = 0; sg < nseg; ++sg) {
         const size_t mb = (static_cast<size_t>(bh) * nseg + sg) * kD * kD;
-        float* out = S_in + mb + static_cast<size_t>(i) * kD + cb + j0;
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) out[jj] = cur[i][j0 + jj];
+        {   // thread -> column cb + (tid >> 4), channels 8 (tid & 15) .. + 7: one 16-byte store
+            const int jl = tid >> 4, ic = (tid & 15) * 8;
+            const uint4 pk = make_uint4(pack_bf16(cur[ic][jl], cur[ic + 1][jl]), pack_bf16(cur[ic + 2][jl], cur[ic + 3][jl]),
+                                        pack_bf16(cur[ic + 4][jl], cur[ic + 5][jl]), pack_bf16(cur[ic + 6][jl], cur[ic + 7][jl]));
+            *reinterpret_cast<uint4*>(S_inT + mb + static_cast<size_t>(cb + jl) * kD + ic) = pk;
+        }
         float acc[8];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) acc[jj] = S_loc[mb + static_cast<size_t>(i) * kD + cb + j0 + jj];
@@ -1313,7 +1319,7 @@ __global__ void __launch_bounds__(256) segment_states_kernel(const float* S0,
 // to bf16 as in the state's bf16 copy that the fused kernel multiplies by), fp32
 // accumulation, warp-level m16n8k16 MMAs from shared memory.
 constexpr int kCorrRows = 128, kCorrTiles = 4, kCorrLd = kD + 8;   // +8: conflict-free ldmatrix rows
-constexpr int kCorrSmem = 2 * kCorrRows * kCorrLd * 2;
+constexpr int kCorrSmem = 3 * kCorrRows * kCorrLd * 2;   // S_in^T and two q~ tiles
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const __nv_bfloat16* p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -1327,50 +1333,64 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__global__ void __launch_bounds__(256) segment_output_correction_kernel(const float* __restrict__ S_in,
-                                                                        const __nv_bfloat16* __restrict__ qt,
-                                                                        __nv_bfloat16* __restrict__ o, int T,
-                                                                        int H, int nseg, int seg_len,
-                                                                        int skip_first) {
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(256, 2) segment_output_correction_kernel(const __nv_bfloat16* __restrict__ S_inT,
+                                                                           const __nv_bfloat16* __restrict__ qt,
+                                                                           __nv_bfloat16* __restrict__ o, int T,
+                                                                           int H, int nseg, int seg_len,
+                                                                           int skip_first) {
     extern __shared__ __align__(16) unsigned char corr_smem[];
-    __nv_bfloat16* As = reinterpret_cast<__nv_bfloat16*>(corr_smem);   // q~ rows [t][i]
-    __nv_bfloat16* Bs = As + kCorrRows * kCorrLd;                       // S_in^T [j][i]
+    __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(corr_smem);   // S_in^T [j][i]
+    __nv_bfloat16* As = Bs + kCorrRows * kCorrLd;                       // q~ rows [t][i], two buffers
     const int bh = blockIdx.z, seg = blockIdx.y, b = bh / H, h = bh % H;
     if (seg == 0 && skip_first) return;   // the first segment starts from S = 0
     const int tb = seg * seg_len, Ts = min(seg_len, T - tb);
     const int r0 = blockIdx.x * kCorrTiles * kCorrRows;
     if (r0 >= Ts) return;
+    const int ntiles = min(kCorrTiles, (Ts - r0 + kCorrRows - 1) / kCorrRows);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const float* S = S_in + (static_cast<size_t>(bh) * nseg + seg) * kD * kD;
-    for (int e = tid; e < kD * kD / 4; e += 256) {
-        const int i = e >> 5, j = (e & 31) * 4;
-        const float4 f = *reinterpret_cast<const float4*>(S + i * kD + j);
-        Bs[(j + 0) * kCorrLd + i] = __float2bfloat16_rn(f.x);
-        Bs[(j + 1) * kCorrLd + i] = __float2bfloat16_rn(f.y);
-        Bs[(j + 2) * kCorrLd + i] = __float2bfloat16_rn(f.z);
-        Bs[(j + 3) * kCorrLd + i] = __float2bfloat16_rn(f.w);
-    }
     const size_t ts = static_cast<size_t>(H) * kD;   // token stride of [B, T, H, d]
     const size_t row0 = (static_cast<size_t>(b) * T + tb) * ts + static_cast<size_t>(h) * kD;
-    const int g = lane >> 2, q = lane & 3;
-    for (int tile = 0; tile < kCorrTiles; ++tile) {
-        const int rt = r0 + tile * kCorrRows;
-        if (rt >= Ts) break;
-        __syncthreads();   // S_in^T is in place (first tile), the previous tile's rows are read
+    // q~ rows of tile k into buffer k & 1 (rows past the segment read as zero)
+    auto load_tile = [&](int k) {
+        const int rt = r0 + k * kCorrRows;
+        __nv_bfloat16* dst = As + (k & 1) * kCorrRows * kCorrLd;
         for (int e = tid; e < kCorrRows * (kD / 8); e += 256) {   // 16-byte pieces, 16 per row
             const int r = e >> 4, c = (e & 15) * 8;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (rt + r < Ts) v = __ldg(reinterpret_cast<const uint4*>(qt + row0 + (rt + r) * ts + c));
-            *reinterpret_cast<uint4*>(As + r * kCorrLd + c) = v;
+            if (rt + r < Ts) cp_async16(dst + r * kCorrLd + c, qt + row0 + (rt + r) * ts + c);
+            else *reinterpret_cast<uint4*>(dst + r * kCorrLd + c) = make_uint4(0u, 0u, 0u, 0u);
         }
-        __syncthreads();
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    load_tile(0);
+    const __nv_bfloat16* St = S_inT + (static_cast<size_t>(bh) * nseg + seg) * kD * kD;
+    for (int e = tid; e < kD * (kD / 8); e += 256) {
+        const int j = e >> 4, c = (e & 15) * 8;
+        *reinterpret_cast<uint4*>(Bs + j * kCorrLd + c) = __ldg(reinterpret_cast<const uint4*>(St + j * kD + c));
+    }
+    const int g = lane >> 2, q = lane & 3;
+    for (int tile = 0; tile < ntiles; ++tile) {
+        const int rt = r0 + tile * kCorrRows;
+        if (tile + 1 < ntiles) {   // the next tile's rows land while this one is multiplied
+            load_tile(tile + 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();   // this tile's rows (and S_in^T) are in shared memory for every warp
+        const __nv_bfloat16* A = As + (tile & 1) * kCorrRows * kCorrLd;
         float acc[16][4];
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
             uint32_t a[4];
-            ldmatrix_x4(a, As + (16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8) * kCorrLd + 16 * ks + (lane >> 4) * 8);
+            ldmatrix_x4(a, A + (16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8) * kCorrLd + 16 * ks + (lane >> 4) * 8);
 #pragma unroll
             for (int np = 0; np < 8; ++np) {   // value columns 16 np .. 16 np + 15
                 uint32_t bb[4];
@@ -1391,6 +1411,7 @@ __global__ void __launch_bounds__(256) segment_output_correction_kernel(const fl
                 *pp = __floats2bfloat162_rn(cur.x + acc[nt][2 * hr], cur.y + acc[nt][2 * hr + 1]);
             }
         }
+        __syncthreads();   // every warp has read buffer tile & 1 before it is refilled
     }
 }
 
@@ -1548,7 +1569,8 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStrea
     P.o = static_cast<__nv_bfloat16*>(sp.qt);
     if ((e = run()) != cudaSuccess) return e;
     // ---- chained initial states and the final state, then o += S_in^T q~
-    segment_states_kernel<<<dim3(a.B * a.H, kD / 16), 256, 0, s>>>(a.S0, sp.Phi, sp.S_loc, sp.S_in, a.S_T,
+    __nv_bfloat16* S_inT = reinterpret_cast<__nv_bfloat16*>(sp.S_in);   // bf16 in the fp32 slot
+    segment_states_kernel<<<dim3(a.B * a.H, kD / 16), 256, 0, s>>>(a.S0, sp.Phi, sp.S_loc, S_inT, a.S_T,
                                                                       sp.nseg);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     e = cudaFuncSetAttribute(segment_output_correction_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1556,7 +1578,7 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStrea
     if (e != cudaSuccess) return e;
     const int groups = (sp.seg_len + kCorrTiles * kCorrRows - 1) / (kCorrTiles * kCorrRows);
     segment_output_correction_kernel<<<dim3(groups, sp.nseg, a.B * a.H), 256, kCorrSmem, s>>>(
-        sp.S_in, static_cast<const __nv_bfloat16*>(sp.qt), static_cast<__nv_bfloat16*>(a.o), a.T, a.H, sp.nseg,
+        S_inT, static_cast<const __nv_bfloat16*>(sp.qt), static_cast<__nv_bfloat16*>(a.o), a.T, a.H, sp.nseg,
         sp.seg_len, a.S0 == nullptr ? 1 : 0);
     return cudaGetLastError();
 }

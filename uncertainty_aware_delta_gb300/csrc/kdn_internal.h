@@ -75,7 +75,7 @@ struct TcSplit {
     int n_chunks_g = 0;
     float* S_loc = nullptr;             // [B*H*nseg][dk][dv] each
     float* Phi = nullptr;
-    float* S_in = nullptr;
+    float* S_in = nullptr;              // chained initial states, held as bf16 S_in^T [j][i]
     void* qt = nullptr;                 // [B][T][H][dk] bf16: q~_t = Phi_t^T q_t of each segment
 };
 TcSplit tc_split_plan(int B, int T, int H, uint32_t flags);   // nseg and seg_len only
