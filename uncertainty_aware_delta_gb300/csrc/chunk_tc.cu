@@ -1318,8 +1318,8 @@ __global__ void __launch_bounds__(256) segment_states_kernel(const float* S0,
 // rows 16w..16w+15 of a tile and all 128 value columns.  bf16 operands (S_in rounded
 // to bf16 as in the state's bf16 copy that the fused kernel multiplies by), fp32
 // accumulation, warp-level m16n8k16 MMAs from shared memory.
-constexpr int kCorrRows = 128, kCorrTiles = 4, kCorrLd = kD + 8;   // +8: conflict-free ldmatrix rows
-constexpr int kCorrSmem = 3 * kCorrRows * kCorrLd * 2;   // S_in^T and two q~ tiles
+constexpr int kCorrRows = 128, kCorrTiles = 8, kCorrLd = kD + 8;   // +8: conflict-free ldmatrix rows
+constexpr int kCorrSmem = 5 * kCorrRows * kCorrLd * 2;   // S_in^T, two q~ tiles, two o tiles
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const __nv_bfloat16* p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -1339,7 +1339,7 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
                  : "memory");
 }
 
-__global__ void __launch_bounds__(256, 2) segment_output_correction_kernel(const __nv_bfloat16* __restrict__ S_inT,
+__global__ void __launch_bounds__(256, 1) segment_output_correction_kernel(const __nv_bfloat16* __restrict__ S_inT,
                                                                            const __nv_bfloat16* __restrict__ qt,
                                                                            __nv_bfloat16* __restrict__ o, int T,
                                                                            int H, int nseg, int seg_len,
@@ -1347,6 +1347,7 @@ __global__ void __launch_bounds__(256, 2) segment_output_correction_kernel(const
     extern __shared__ __align__(16) unsigned char corr_smem[];
     __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(corr_smem);   // S_in^T [j][i]
     __nv_bfloat16* As = Bs + kCorrRows * kCorrLd;                       // q~ rows [t][i], two buffers
+    __nv_bfloat16* Os = As + 2 * kCorrRows * kCorrLd;                   // o rows [t][j], two buffers
     const int bh = blockIdx.z, seg = blockIdx.y, b = bh / H, h = bh % H;
     if (seg == 0 && skip_first) return;   // the first segment starts from S = 0
     const int tb = seg * seg_len, Ts = min(seg_len, T - tb);
@@ -1356,14 +1357,19 @@ __global__ void __launch_bounds__(256, 2) segment_output_correction_kernel(const
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t ts = static_cast<size_t>(H) * kD;   // token stride of [B, T, H, d]
     const size_t row0 = (static_cast<size_t>(b) * T + tb) * ts + static_cast<size_t>(h) * kD;
-    // q~ rows of tile k into buffer k & 1 (rows past the segment read as zero)
+    // q~ and o rows of tile k into buffers k & 1 (q~ rows past the segment read as zero)
     auto load_tile = [&](int k) {
         const int rt = r0 + k * kCorrRows;
-        __nv_bfloat16* dst = As + (k & 1) * kCorrRows * kCorrLd;
+        __nv_bfloat16* dq = As + (k & 1) * kCorrRows * kCorrLd;
+        __nv_bfloat16* dout = Os + (k & 1) * kCorrRows * kCorrLd;
         for (int e = tid; e < kCorrRows * (kD / 8); e += 256) {   // 16-byte pieces, 16 per row
             const int r = e >> 4, c = (e & 15) * 8;
-            if (rt + r < Ts) cp_async16(dst + r * kCorrLd + c, qt + row0 + (rt + r) * ts + c);
-            else *reinterpret_cast<uint4*>(dst + r * kCorrLd + c) = make_uint4(0u, 0u, 0u, 0u);
+            if (rt + r < Ts) {
+                cp_async16(dq + r * kCorrLd + c, qt + row0 + (rt + r) * ts + c);
+                cp_async16(dout + r * kCorrLd + c, o + row0 + (rt + r) * ts + c);
+            } else {
+                *reinterpret_cast<uint4*>(dq + r * kCorrLd + c) = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
@@ -1399,19 +1405,27 @@ __global__ void __launch_bounds__(256, 2) segment_output_correction_kernel(const
                 mma_bf16_16816(acc[2 * np + 1], a, bb[2], bb[3]);
             }
         }
+        // o rows += the product, in shared memory (each element has one owner), then
+        // written back row by row in 16-byte pieces
+        __nv_bfloat16* Ot = Os + (tile & 1) * kCorrRows * kCorrLd;
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
             const int r = 16 * warp + g + 8 * hr;
-            if (rt + r >= Ts) continue;
-            __nv_bfloat16* orow = o + row0 + (rt + r) * ts;
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt) {
-                __nv_bfloat162* pp = reinterpret_cast<__nv_bfloat162*>(orow + 8 * nt + 2 * q);
+                __nv_bfloat162* pp = reinterpret_cast<__nv_bfloat162*>(Ot + r * kCorrLd + 8 * nt + 2 * q);
                 const float2 cur = __bfloat1622float2(*pp);
                 *pp = __floats2bfloat162_rn(cur.x + acc[nt][2 * hr], cur.y + acc[nt][2 * hr + 1]);
             }
         }
-        __syncthreads();   // every warp has read buffer tile & 1 before it is refilled
+        __syncthreads();
+        for (int e = tid; e < kCorrRows * (kD / 8); e += 256) {
+            const int r = e >> 4, c = (e & 15) * 8;
+            if (rt + r < Ts)
+                *reinterpret_cast<uint4*>(o + row0 + (rt + r) * ts + c) =
+                    *reinterpret_cast<const uint4*>(Ot + r * kCorrLd + c);
+        }
+        __syncthreads();   // every warp has read buffers tile & 1 before they are refilled
     }
 }
 
