@@ -81,6 +81,10 @@ struct TcSplit {
 TcSplit tc_split_plan(int B, int T, int H, uint32_t flags);   // nseg and seg_len only
 cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStream_t s);
 int tc_kernel_count(int nseg);
+// Sequence split, after the two map passes: chained initial states S_in (as bf16
+// S_in^T) and the final state, then o += S_in^T q~ per segment.  split.cu
+cudaError_t launch_segment_states(const ForwardArgs& a, const TcSplit& sp, cudaStream_t s);
+cudaError_t launch_segment_correction(const ForwardArgs& a, const TcSplit& sp, cudaStream_t s);
 
 // Copy the initial state to the outputs (T == 0).  chunk_simt.cu
 cudaError_t launch_state_copy(const ForwardArgs& a, cudaStream_t s);
