@@ -249,6 +249,19 @@ def traffic_for(kernel, workload):
     return None
 
 
+def dense_algorithmic_flops(B, T, H, d):
+    """Flops of the dense filter per call: 13 d^2 per token-head (D P D: 2 d^2,
+    P_hat k: 2 d^2, P_hat - kappa u^T: 2 d^2, D S: d^2, S_hat^T k: 2 d^2,
+    kappa delta^T: 2 d^2, S^T q: 2 d^2), lower-order terms left out."""
+    return 13 * d * d * B * T * H
+
+
+def dense_alu_peak_tflops(torch, device):
+    """fp32 CUDA-core peak: SMs x 128 fp32 lanes x 2 flop (FMA) x 2070 MHz."""
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    return sms * 128 * 2 * 2.07e9 / 1e12
+
+
 # ----------------------------------------------------------------- CPU oracle
 PKDA_NAMES = ("q", "k", "v", "log_alpha", "beta", "alpha_p", "beta_p", "center")
 
@@ -371,6 +384,16 @@ def main():
                   file=sys.stderr)
             return 2
         return profile_decode(torch, kdn, w, device, args.steps, args.warmup)
+    if w.variant == "dense":
+        if not args.profile:
+            print("the dense workload is timed inside the default run (see 'workloads'); use --profile",
+                  file=sys.stderr)
+            return 2
+        x = device_inputs(torch, w, "diag", w.seed, device)
+        time_calls(torch, lambda: kdn.kdn_dense_forward(x["q"], x["k"], x["v"], x["log_alpha"], x["omega"],
+                                                        x["r"]), args.steps, args.warmup, barrier)
+        print(json.dumps({"profile": w.name, "kernels_per_step": 1}), flush=True)
+        return 0
     variant = w.variant
     vcode = {"diag": kdn.KDN_DIAG, "iso": kdn.KDN_ISO, "pkda": kdn.KDN_PKDA}[variant]
     io = kdn.KDN_BF16 if w.io == "bf16" else kdn.KDN_F32
@@ -525,6 +548,18 @@ def other_workloads(torch, kdn, WORKLOADS, device, barrier, peaks):
     ab = pkda_algorithmic_bytes(w.B, w.T, w.H, w.d, w.d, w.io)
     out[w.name] = {"tokens_per_s": w.B * w.T / (ms / 1e3), "ms": ms, "hbm_frac": ab / (ms / 1e3) / 1e9 / hbm,
                    "algorithmic_bytes": ab, "traffic": traffic_for("kdn_fused_tc_kernel", w.name)}
+    del x
+    # dense-covariance (exact) filter on the headline shape: token-serial, bound by fp32 ALU work
+    w = WORKLOADS["dense-bf16-b8h16t4096d128"]
+    x = device_inputs(torch, w, "diag", w.seed, device)
+    ms = time_calls(torch, lambda: kdn.kdn_dense_forward(x["q"], x["k"], x["v"], x["log_alpha"], x["omega"],
+                                                         x["r"]), 5, 2, barrier)
+    flops = dense_algorithmic_flops(w.B, w.T, w.H, w.d)
+    peak = dense_alu_peak_tflops(torch, device)
+    out[w.name] = {"tokens_per_s": w.B * w.T / (ms / 1e3), "ms": ms, "kernel": "dense_forward_kernel",
+                   "bound": "alu", "algorithmic_flops": flops, "achieved_tflops": flops / (ms / 1e3) / 1e12,
+                   "peak_tflops": peak, "alu_frac": flops / (ms / 1e3) / 1e12 / peak,
+                   "peak_source": "SM count x 128 fp32 lanes x 2 flop x 2070 MHz (maximum SM clock)"}
     del x
     # decode: 512-token prefill through the forward path, then 1024 single-token steps
     w = WORKLOADS["diag-decode-f32-s256h16d128"]

@@ -237,6 +237,32 @@ kdn_status kdn_pkda_step(int B, int H, int dk, int dv, float x, int io_dtype,
                          void *workspace, size_t workspace_bytes, kdn_stream_t stream);
 
 /*
+ * Dense-covariance (exact) Kalman memory forward (KDN paper Sec. 3.2, Eq. 12-17):
+ * the filter that the Diagonal and Isotropic KDN approximate.  Per head a
+ * memory S (d x d) and a full key covariance P (d x d); for every token, with
+ * a_t = exp(log_alpha_t):
+ *
+ *   P_hat = diag(a_t) P diag(a_t) + diag(omega_t),  u = P_hat k_t,
+ *   kappa = u / (r_t + k_t^T u),  P = P_hat - kappa u^T  (= (I - kappa k^T) P_hat),
+ *   S_hat = diag(a_t) S,  S = S_hat + kappa (v_t - S_hat^T k_t)^T,  o_t = S^T q_t.
+ *
+ * Inputs : q, k, v [B,T,H,d] io_dtype; log_alpha, omega [B,T,H,d] fp32;
+ *          r [B,T,H] fp32 > 0; S0 [B,H,d,d] or NULL (zero memory);
+ *          P0 [B,H,d,d] or NULL (identity), symmetric positive semi-definite.
+ * Outputs: o [B,T,H,d] io_dtype; S_T, P_T [B,H,d,d] fp32 (the state after token
+ *          T-1; S_T == S0 and P_T == P0 are allowed).
+ * Sizes  : d in {32, 64, 128} (d_k = d_v = d); any T >= 0; B, H >= 0.
+ * The tokens of a head run in order on one CTA with P and S in registers (O(d^2)
+ * work per token and head, fp32; no workspace, no device status).  Alignment,
+ * aliasing and errors as kdn_diag_forward.
+ */
+kdn_status kdn_dense_forward(int B, int T, int H, int d, int io_dtype,
+                             const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *omega, const float *r,
+                             const float *S0, const float *P0,
+                             void *o, float *S_T, float *P_T, kdn_stream_t stream);
+
+/*
  * Forward without a caller workspace.  The paper has no counterpart: this is
  * a convenience of the library for callers that cannot allocate device
  * memory at the point where they run the mixer -- for example code inside a

@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("kdn_diag_forward", "kdn_iso_forward", "kdn_step", "kdn_workspace_size",
               "kdn_read_device_status", "kdn_status_string", "kdn_abi_version",
-              "kdn_forward_kernel_count", "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step"):
+              "kdn_forward_kernel_count", "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step",
+              "kdn_dense_forward"):
         assert n in names
 
 
@@ -139,6 +140,29 @@ def test_validation_rejects_before_launch(lib, variant):
     assert _call(lib, _fwd_args(k=72), variant) == 4           # KDN_ERR_ALIGN (72 % 16 != 0)
     assert _call(lib, _fwd_args(o=64 + 16), variant) == 10     # KDN_ERR_ALIAS (o overlaps q)
     assert _call(lib, _fwd_args(ws=1 << 20), variant) == 10    # workspace overlaps o
+
+
+def test_dense_validation_rejects_before_launch(lib):
+    # B=1 T=64 H=2 d=32: inputs of 64*2*32 elements; each case fails a host check
+    vp = ctypes.c_void_p
+
+    def call(d=32, io=0, T=64, **ptr):
+        p = dict(q=1 << 16, k=2 << 16, v=3 << 16, la=4 << 16, om=5 << 16, r=6 << 16, S0=None, P0=None,
+                 o=1 << 20, S_T=2 << 20, P_T=3 << 20)
+        p.update(ptr)
+        args = [vp(p[n]) if p[n] is not None else None
+                for n in ("q", "k", "v", "la", "om", "r", "S0", "P0", "o", "S_T", "P_T")]
+        return lib.kdn_dense_forward(1, T, 2, d, io, *args, None)
+
+    assert call(d=16) == 6                     # KDN_ERR_UNSUPPORTED
+    assert call(io=2) == 3                     # KDN_ERR_DTYPE
+    assert call(T=-1) == 2                     # KDN_ERR_SHAPE
+    assert call(q=None) == 1                   # KDN_ERR_NULL
+    assert call(P_T=None) == 1
+    assert call(k=(2 << 16) + 8) == 4          # KDN_ERR_ALIGN
+    assert call(o=(1 << 16) + 64) == 10        # KDN_ERR_ALIAS: o overlaps q
+    assert call(P_T=(2 << 20) + 256) == 10     # P_T overlaps S_T
+    assert call(P0=(2 << 20)) == 10            # P0 overlaps S_T
 
 
 def test_step_validation_rejects_before_launch(lib):

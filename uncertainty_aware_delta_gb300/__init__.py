@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     kdn_diag_forward,
     kdn_forward_noalloc,
     kdn_iso_forward,
+    kdn_dense_forward,
     kdn_pkda_forward,
     kdn_pkda_step,
     kdn_read_device_status,

@@ -74,6 +74,8 @@ def library():
             lib.kdn_forward_noalloc.restype = i32
             lib.kdn_forward_noalloc.argtypes = [i32] * 7 + [f32, i32, u32] + [vp] * 3 + [fp] * 5 + \
                 [vp, fp, fp, vp, vp]
+            lib.kdn_dense_forward.restype = i32
+            lib.kdn_dense_forward.argtypes = [i32] * 5 + [vp] * 3 + [fp] * 5 + [vp, fp, fp, vp]
             lib.kdn_abi_version.restype = i32
             lib.kdn_abi_version.argtypes = []
             _lib = lib
@@ -335,6 +337,41 @@ def kdn_forward_noalloc(variant, q, k, v, log_alpha, omega, r, S0=None, p0=None,
     if st != 0:
         raise KDNError(st, "kdn_forward_noalloc")
     return o, S_T, p_T
+
+
+def kdn_dense_forward(q, k, v, log_alpha, omega, r, S0=None, P0=None, *, out=None, stream=None):
+    """Dense-covariance (exact) Kalman memory forward (KDN paper Sec. 3.2).  Returns (o, S_T, P_T).
+
+    q, k, v [B,T,H,d] in fp32 or bf16 (d in 32, 64, 128); log_alpha, omega [B,T,H,d],
+    r [B,T,H] fp32; optional S0 [B,H,d,d] (zero) and P0 [B,H,d,d] (identity) fp32.
+    ``out=(o, S_T, P_T)`` writes into given tensors.
+    """
+    lib = library()
+    device = q.device
+    B, T, H, d = q.shape
+    io = KDN_BF16 if q.dtype == torch.bfloat16 else KDN_F32
+    iot = torch.bfloat16 if io == KDN_BF16 else torch.float32
+    for t, name, dt, shape in ((q, "q", iot, (B, T, H, d)), (k, "k", iot, (B, T, H, d)),
+                               (v, "v", iot, (B, T, H, d)), (log_alpha, "log_alpha", torch.float32, (B, T, H, d)),
+                               (omega, "omega", torch.float32, (B, T, H, d)), (r, "r", torch.float32, (B, T, H)),
+                               (S0, "S0", torch.float32, (B, H, d, d)), (P0, "P0", torch.float32, (B, H, d, d))):
+        _check(t, name, dt, shape, device)
+    if out is None:
+        o = torch.empty((B, T, H, d), dtype=iot, device=device)
+        S_T = torch.empty((B, H, d, d), dtype=torch.float32, device=device)
+        P_T = torch.empty((B, H, d, d), dtype=torch.float32, device=device)
+    else:
+        o, S_T, P_T = out
+        _check(o, "o", iot, (B, T, H, d), device)
+        _check(S_T, "S_T", torch.float32, (B, H, d, d), device)
+        _check(P_T, "P_T", torch.float32, (B, H, d, d), device)
+    with torch.cuda.device(device):
+        st = lib.kdn_dense_forward(B, T, H, d, io, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(omega),
+                                   _ptr(r), _ptr(S0), _ptr(P0), _ptr(o), _ptr(S_T), _ptr(P_T),
+                                   _stream(stream, device))
+    if st != 0:
+        raise KDNError(st, "kdn_dense_forward")
+    return o, S_T, P_T
 
 
 def kdn_read_device_status(workspace, stream=None) -> int:

@@ -318,6 +318,42 @@ kdn_status kdn_pkda_step(int B, int H, int dk, int dv, float x, int io_dtype, co
                      PkdaInputs{beta, alpha_p, beta_p, center, x});
 }
 
+kdn_status kdn_dense_forward(int B, int T, int H, int d, int io_dtype, const void* q, const void* k,
+                             const void* v, const float* log_alpha, const float* omega, const float* r,
+                             const float* S0, const float* P0, void* o, float* S_T, float* P_T,
+                             kdn_stream_t stream) {
+    if (io_dtype != KDN_F32 && io_dtype != KDN_BF16) return KDN_ERR_DTYPE;
+    if (B < 0 || T < 0 || H < 0) return KDN_ERR_SHAPE;
+    if (d != 32 && d != 64 && d != 128) return KDN_ERR_UNSUPPORTED;
+    if ((double)B * (double)T * (double)H * 128.0 > 1.0e12 || (double)B * (double)H > 2.0e9)
+        return KDN_ERR_SHAPE;
+    const size_t BH = (size_t)B * H, ntok = (size_t)B * T * H, esz = io_dtype == KDN_BF16 ? 2 : 4;
+    if (BH > 0 && (!S_T || !P_T)) return KDN_ERR_NULL;
+    if (ntok > 0 && (!q || !k || !v || !log_alpha || !omega || !r || !o)) return KDN_ERR_NULL;
+    const void* ptrs[] = {q, k, v, log_alpha, omega, r, S0, P0, o, S_T, P_T};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KDN_ERR_ALIGN;
+    const size_t nd = ntok * d, ns = BH * d * d;
+    const Range in[] = {{q, nd * esz}, {k, nd * esz}, {v, nd * esz}, {log_alpha, nd * 4},
+                        {omega, nd * 4}, {r, ntok * 4}, {S0, ns * 4}, {P0, ns * 4}};
+    const Range ro = {o, nd * esz}, rs = {S_T, ns * 4}, rp = {P_T, ns * 4};
+    for (const Range& x : in) {
+        if (overlaps(ro, x)) return KDN_ERR_ALIAS;
+        if (x.p != S0 && overlaps(rs, x)) return KDN_ERR_ALIAS;
+        if (x.p != P0 && overlaps(rp, x)) return KDN_ERR_ALIAS;
+    }
+    if (overlaps(ro, rs) || overlaps(ro, rp) || overlaps(rs, rp)) return KDN_ERR_ALIAS;
+    if (S0 && S0 != (const float*)S_T && overlaps(rs, Range{S0, ns * 4})) return KDN_ERR_ALIAS;
+    if (P0 && P0 != (const float*)P_T && overlaps(rp, Range{P0, ns * 4})) return KDN_ERR_ALIAS;
+    if (BH == 0) return KDN_OK;
+    kdn::DenseArgs a;
+    a.B = B; a.T = T; a.H = H; a.d = d; a.io = io_dtype;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.omega = omega; a.r = r;
+    a.S0 = S0; a.P0 = P0; a.o = o; a.S_T = S_T; a.P_T = P_T;
+    return kdn::launch_dense_forward(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KDN_OK
+                                                                                              : KDN_ERR_CUDA;
+}
+
 kdn_status kdn_read_device_status(const void* workspace, kdn_stream_t stream) {
     if (!workspace) return KDN_ERR_NULL;
     uint32_t word = 0;

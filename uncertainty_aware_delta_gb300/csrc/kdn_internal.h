@@ -86,6 +86,16 @@ int tc_kernel_count(int nseg);
 cudaError_t launch_segment_states(const ForwardArgs& a, const TcSplit& sp, cudaStream_t s);
 cudaError_t launch_segment_correction(const ForwardArgs& a, const TcSplit& sp, cudaStream_t s);
 
+// Dense-covariance (exact) Kalman memory forward, token by token.  dense.cu
+struct DenseArgs {
+    int B, T, H, d, io;
+    const void *q, *k, *v;
+    const float *log_alpha, *omega, *r, *S0, *P0;
+    void* o;
+    float *S_T, *P_T;
+};
+cudaError_t launch_dense_forward(const DenseArgs& a, cudaStream_t s);
+
 // Copy the initial state to the outputs (T == 0).  chunk_simt.cu
 cudaError_t launch_state_copy(const ForwardArgs& a, cudaStream_t s);
 

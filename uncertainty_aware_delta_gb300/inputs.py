@@ -41,7 +41,7 @@ import numpy as np
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    variant: str          # "diag", "iso" or "pkda"
+    variant: str          # "diag", "iso", "pkda" or "dense"
     B: int
     H: int
     T: int
@@ -64,6 +64,8 @@ WORKLOADS = {
         Workload("diag-decode-f32-s256h16d128", "diag", 256, 16, 512 + 1024, 128, 64, "f32", (1e-3, 0.1),
                  20260911, prefill=512, steps=1024),
         Workload("pkda-bf16-b8h16t4096d128", "pkda", 8, 16, 4096, 128, 64, "bf16", (1e-3, 0.1), 20260912),
+        # the dense-covariance (exact) filter on the headline shape; inputs as the diagonal recipe
+        Workload("dense-bf16-b8h16t4096d128", "dense", 8, 16, 4096, 128, 0, "bf16", (1e-3, 0.1), 20260913),
     ]
 }
 
@@ -153,9 +155,12 @@ def workload_inputs(w: Workload, variant: str | None = None):
     its own per-(b,t,h) omega drawn from the same seed).  For a decode
     workload this returns the prefill tokens only; see :func:`decode_step_inputs`."""
     T = w.prefill if w.steps else w.T
-    if (variant or w.variant) == "pkda":
+    variant = variant or w.variant
+    if variant == "dense":   # the dense filter takes the diagonal recipe's inputs
+        variant = "diag"
+    if variant == "pkda":
         return make_pkda_inputs(w.B, T, w.H, w.d, w.d, w.io, w.seed, w.log_alpha_range)
-    return make_inputs(variant or w.variant, w.B, T, w.H, w.d, w.d, w.io, w.seed, w.log_alpha_range)
+    return make_inputs(variant, w.B, T, w.H, w.d, w.d, w.io, w.seed, w.log_alpha_range)
 
 
 def decode_step_inputs(w: Workload, step: int, variant: str | None = None):
