@@ -65,9 +65,10 @@ bool tc_path_supported(int io, int dk, int dv, int chunk);
 // Sequence split of the tensor-core forward for few long sequences: nseg
 // segments of seg_len tokens (a multiple of kGainChunk) per sequence run on
 // separate SMs.  The state map of a segment is affine, S_out = Phi S_in + S_loc;
-// one pass gives every segment's S_loc (from S = 0) and Phi (from S = I, values
-// zero), a short serial pass chains them into each segment's initial state, and
-// a last pass recomputes the segments from their true initial states.
+// one pass gives every segment's S_loc and outputs o_loc (from S = 0), one its
+// Phi and transformed queries Phi_t^T q_t (from S = I, values zero), a short
+// serial pass chains the maps into each segment's initial state and the final
+// state, and o_t = o_loc,t + S_in^T (Phi_t^T q_t) completes the outputs.
 struct TcSplit {
     int nseg = 1, seg_len = 0;          // nseg == 1: no split
     float* summary = nullptr;           // scan workspace (gain chunks of kGainChunk tokens)
