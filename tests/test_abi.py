@@ -47,7 +47,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings_and_version(lib):
     import uncertainty_aware_delta_gb300 as kdn
 
-    assert lib.kdn_abi_version() == 101
+    assert lib.kdn_abi_version() == 102
     for code in range(0, 11):
         s = kdn.status_string(code)
         assert s and s != "unknown status"

@@ -392,6 +392,6 @@ const char* kdn_status_string(int status) {
     }
 }
 
-int kdn_abi_version(void) { return 101; }
+int kdn_abi_version(void) { return 102; }
 
 }  // extern "C"
