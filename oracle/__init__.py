@@ -15,9 +15,14 @@ Contents
                  recurrence (KDN paper Eq. 32-37) and the weighted ridge
                  regression closed form (Preconditioned DeltaNet Eq. 1-5;
                  Gated KalmaNet test-time ridge regression).
+  backward    -- numpy fp64 adjoint of the token recurrence (the gradients of
+                 a weighted sum of o, S_T and p_T with respect to every input),
+                 for tiny inputs; the pages give no backward pass.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-against printed values, closed forms, special-case reductions and brute force.
+against printed values, closed forms, special-case reductions and brute force;
+the backward by ``tests/test_backward_oracle.py`` against central finite
+differences of the forward.
 """
 from .recurrence import build_oracle, forward, step, library_path  # noqa: F401
 from .dense import (  # noqa: F401
