@@ -32,7 +32,9 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
  *     never allocates, frees or retains them and keeps no global mutable state
  *     (re-entrant; concurrent calls on different streams with disjoint buffers
- *     are safe).
+ *     are safe).  The one exception is kdn_forward_noalloc, which uses a
+ *     library-owned static device array and a per-device cache of its address
+ *     (see that entry point for the sharing rules).
  *   - Layouts are dense row-major with the feature dimension innermost:
  *       q, k, log_alpha       [B, T, H, d_k]
  *       v, o                  [B, T, H, d_v]
@@ -87,15 +89,31 @@ typedef enum {
 typedef enum { KDN_F32 = 0, KDN_BF16 = 1 } kdn_dtype;
 typedef enum { KDN_DIAG = 0, KDN_ISO = 1, KDN_PKDA = 2 } kdn_variant;
 
-/* Flags for the forward calls. */
+/* Flags for the forward calls (and kdn_step_ex). */
 #define KDN_FLAG_PORTABLE 0x1u   /* force the CUDA-core (FFMA) chunk path */
 #define KDN_FLAG_NO_SPLIT 0x2u   /* tensor-core path: never split sequences into segments */
+/*
+ * Test facility for the bounded-wait path; never set it in production.  The
+ * kernels that wait on asynchronous copies (the tensor-core forward and the
+ * d_k = d_v = 128 decode kernel) first wait, with a short bound (a few
+ * milliseconds), on a barrier that nothing completes, while their first
+ * copies are in flight.  The wait gives up, the status word records
+ * KDN_ERR_TIMEOUT, and each CTA takes its abort path: it issues no further
+ * work, lets the copies already issued land and exits.  The outputs of such
+ * a call are undefined; the stream and the device stay usable.  Other paths
+ * (CUDA-core forward, other decode shapes, the dense filter) ignore the flag.
+ */
+#define KDN_FLAG_TIMEOUT_PROBE 0x100u
 
 /*
  * Sequence split (tensor-core path).  When B*H sequences would leave most of
- * the GPU idle (2*B*H <= 152) and each is long (T >= 2048), every sequence is
- * cut into nseg = min(152 / (B*H), T / 1024) segments of a multiple of 256
- * tokens that run on separate SMs.  The method's state map over a segment is
+ * the GPU idle (2*B*H <= N_SM, the SM count of the current device: 152 on
+ * GB300, and 152 when no device can be queried) and each is long
+ * (T >= 2048), every sequence is cut into nseg = min(N_SM / (B*H), T / 1024)
+ * segments of a multiple of 256 tokens that run on separate SMs.  The plan,
+ * and therefore kdn_workspace_size() and kdn_forward_kernel_count(), depend on
+ * the device that is current when they are called: query them with the same
+ * device current as the forward call.  The method's state map over a segment is
  * affine, S_out = Phi S_in + S_loc, for the segment's gains, which depend only
  * on the uncertainty (statistic) recurrence: a scan over the whole sequence
  * gives each segment's initial uncertainty; one pass from S = 0 gives every
@@ -221,6 +239,17 @@ kdn_status kdn_step(int variant, int B, int H, int dk, int dv, float mu, int io_
                     void *workspace, size_t workspace_bytes, kdn_stream_t stream);
 
 /*
+ * kdn_step with flags: the same call, arguments and workspace.  flags may be 0
+ * or KDN_FLAG_TIMEOUT_PROBE (see above); other bits return
+ * KDN_ERR_UNSUPPORTED.
+ */
+kdn_status kdn_step_ex(int variant, int B, int H, int dk, int dv, float mu, int io_dtype, uint32_t flags,
+                       const void *q, const void *k, const void *v,
+                       const float *log_alpha, const float *omega, const float *r,
+                       float *S, float *p, void *o,
+                       void *workspace, size_t workspace_bytes, kdn_stream_t stream);
+
+/*
  * Single-token PKDA decode (one token of kdn_pkda_forward per sequence and
  * head), state updated IN PLACE.
  * Inputs : q, k [B,H,dk] io_dtype; v [B,H,dv] io_dtype; log_alpha [B,H,dk];
@@ -284,7 +313,10 @@ kdn_status kdn_dense_forward(int B, int T, int H, int d, int io_dtype,
  *
  * Set-up: the first call on a device looks up the device address of the
  * static array, with that device current; make that first call before any
- * stream capture begins on the device.
+ * stream capture begins on the device.  The address is cached per device for
+ * the life of the process: after cudaDeviceReset (or any teardown of the
+ * device's primary context) the cached address is stale, so do not call this
+ * entry point again in a process that has reset the device.
  *
  * Sharing: all calls in the process share the one array per device and it
  * keeps the last call's contents; each call clears what must start at zero

@@ -38,6 +38,36 @@ def err(x, y, io):
     return max_rel(x, y) if io == "f32" else norm_max_abs(x, y)
 
 
+def rel_floors(x, y):
+    """(rms floor, 1%-of-rms floor, no floor) per-element relative errors: the
+    asserted fp32 metric, the stricter floor a plain fp32 recurrence already
+    fails (see test_fp32_rounding_floor.py), and the pure element-wise value."""
+    x = np.asarray(x, np.float64)
+    y = np.asarray(y, np.float64)
+    if y.size == 0:
+        return (0.0, 0.0, 0.0)
+    rms = np.sqrt(np.mean(y * y))
+    d = np.abs(x - y)
+    ay = np.abs(y)
+    return (float(np.max(d / np.maximum(ay, rms + 1e-300))), float(np.max(d / np.maximum(ay, 1e-2 * rms + 1e-300))),
+            float(np.max(d / np.maximum(ay, 1e-300))))
+
+
+def report(what, got, ref, io):
+    """Print the asserted error and, for fp32, the other two floors beside it
+    (shown with pytest -s, and on failure)."""
+    line = {}
+    for name in got:
+        e = err(got[name], ref[name], io)
+        if io == "f32":
+            a, b, c = rel_floors(got[name], ref[name])
+            line[name] = f"{e:.2e} (1%-rms {b:.2e}, elementwise {c:.2e})"
+        else:
+            line[name] = f"{e:.2e}"
+    print(f"[parity] {what} [{io}]: {line}")
+    return line
+
+
 def tol(io):
     return FP32_TOL if io == "f32" else BF16_TOL
 
@@ -55,4 +85,6 @@ def to_device(x, dev="cuda:0"):
 
 
 def to_host(t):
+    if isinstance(t, np.ndarray):
+        return t
     return t.detach().float().cpu().numpy()

@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     for n in ("kdn_diag_forward", "kdn_iso_forward", "kdn_step", "kdn_workspace_size",
               "kdn_read_device_status", "kdn_status_string", "kdn_abi_version",
               "kdn_forward_kernel_count", "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step",
-              "kdn_dense_forward"):
+              "kdn_dense_forward", "kdn_step_ex"):
         assert n in names
 
 
@@ -47,7 +47,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings_and_version(lib):
     import uncertainty_aware_delta_gb300 as kdn
 
-    assert lib.kdn_abi_version() == 102
+    assert lib.kdn_abi_version() == 103
     for code in range(0, 11):
         s = kdn.status_string(code)
         assert s and s != "unknown status"
@@ -182,6 +182,10 @@ def test_step_validation_rejects_before_launch(lib):
     p3 = list(ptrs)
     p3[8] = vp((1 << 20) + 64)                               # o overlaps S
     assert lib.kdn_step(*base, *p3, *ws) == 10
+    # kdn_step_ex: the same validation; flags other than the timeout probe are refused
+    assert lib.kdn_step_ex(*base, 0, *p3, *ws) == 10
+    assert lib.kdn_step_ex(*base, 0x1, *ptrs, *ws) == 6
+    assert lib.kdn_step_ex(*bad, 0x100, *ptrs, *ws) == 6
 
 
 def _pkda_call(lib, **over):

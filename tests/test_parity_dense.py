@@ -77,6 +77,26 @@ def test_dense_forward_matches_oracle(case):
     _check(got, _reference(x), io, case)
 
 
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_dense_forward_long_sequence_stays_symmetric(io):
+    """A 4096-token sequence (the length of the dense filter's bench workload):
+    the fp32 covariance update P_hat - kappa u^T is not symmetrised, so check
+    that P_T stays symmetric and finite over the whole run, and that o, S_T
+    and P_T still match the fp64 filter."""
+    kdn = _kdn()
+    x = make_inputs("diag", 1, 4096, 1, 128, 128, io=io, seed=3999)
+    t = to_device(x)
+    got = kdn.kdn_dense_forward(t["q"], t["k"], t["v"], t["log_alpha"], t["omega"], t["r"])
+    o, S_T, P_T = (to_host(a) for a in got)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S_T)) and np.all(np.isfinite(P_T))
+    P = P_T[0, 0].astype(np.float64)
+    asym = np.max(np.abs(P - P.T)) / np.max(np.abs(P))
+    assert asym <= 1e-5, asym
+    assert np.min(np.linalg.eigvalsh(0.5 * (P + P.T))) > 0.0
+    e = _check(got, _reference(x), io, f"long {io}")
+    print(f"[parity] dense T=4096 {io}: {e}, P_T asymmetry {asym:.2e}")
+
+
 def test_dense_initial_state_in_place_resume_and_empty_sequence():
     import torch
 

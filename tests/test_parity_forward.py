@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
-from kdn_testutil import err, to_device, to_host, tol
+from kdn_testutil import err, report, to_device, to_host, tol
 from uncertainty_aware_delta_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
 
 pytestmark = pytest.mark.gpu
@@ -32,6 +32,7 @@ def _run(kdn, variant, t, **kw):
 def _check(variant, x, got, ref, io, what=""):
     o, S_T, p_T = (to_host(a) for a in got)
     e = {"o": err(o, ref["o"], io), "S_T": err(S_T, ref["S_T"], io), "p_T": err(p_T, ref["p_T"], io)}
+    report(f"{variant} {what}", {"o": o, "S_T": S_T, "p_T": p_T}, ref, io)
     bound = tol(io)
     assert all(v <= bound for v in e.values()), (variant, what, e)
     return e
@@ -165,43 +166,48 @@ def test_extreme_decay_is_reported_not_faulted():
 
 
 # ------------------------------------------------------------ full-size workloads
-def _sampled_parity(name, variant, seqs):
+def _full_parity(name, variant):
     """Run a full-size workload on the GPU in the benchmark's launch
-    configuration and compare the sampled (b, h) sequences with the oracle."""
+    configuration and compare EVERY (b, h) sequence, element by element,
+    with the oracle on the same inputs (the oracle runs all sequences on the
+    host cores)."""
     kdn = _kdn()
     w = WORKLOADS[name]
     x = workload_inputs(w, variant)
     t = to_device(x)
     got = _run(kdn, variant, t, chunk=w.chunk)
     o, S_T, p_T = (to_host(a) for a in got)
-    errs = []
-    for b, h in seqs:
-        sl = lambda a: a[b:b + 1, :, h:h + 1]
-        ref = oracle.forward(variant, sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["log_alpha"]),
-                             sl(x["omega"]), sl(x["r"]))
-        e = (err(o[b:b + 1, :, h:h + 1], ref["o"], w.io), err(S_T[b:b + 1, h:h + 1], ref["S_T"], w.io),
-             err(p_T[b:b + 1, h:h + 1], ref["p_T"], w.io))
-        errs.append(e)
-        assert max(e) <= tol(w.io), (name, variant, b, h, e)
-    assert np.all(np.isfinite(o))
-    return errs
+    del t, got
+    ref = oracle.forward(variant, x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"])
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S_T)) and np.all(np.isfinite(p_T))
+    e = _check(variant, x, (o, S_T, p_T), ref, w.io, f"{name} all sequences")
+    # per sequence as well: a mistake confined to a few (b, h) pairs would be
+    # diluted by the tensor-wide normalisation above
+    worst = 0.0
+    for b in range(w.B):
+        for h in range(w.H):
+            eo = err(o[b, :, h], ref["o"][b, :, h], w.io)
+            es = err(S_T[b, h], ref["S_T"][b, h], w.io)
+            worst = max(worst, eo, es)
+            assert max(eo, es) <= tol(w.io), (name, variant, b, h, eo, es)
+    print(f"[parity] {name} {variant}: worst per-sequence error {worst:.2e}")
+    return e
 
 
 @pytest.mark.parametrize("variant", ["diag", "iso"])
 def test_full_size_b8h16t4096(variant):
-    _sampled_parity("diag-bf16-b8h16t4096d128" if variant == "diag" else "iso-bf16-b8h16t4096d128",
-                    variant, [(0, 0), (7, 15), (3, 9)])
+    _full_parity("diag-bf16-b8h16t4096d128" if variant == "diag" else "iso-bf16-b8h16t4096d128", variant)
 
 
 @pytest.mark.parametrize("variant", ["diag", "iso"])
 def test_full_size_long_context(variant):
-    _sampled_parity("diag-bf16-b1h16t65536d128", variant, [(0, 5)])
+    _full_parity("diag-bf16-b1h16t65536d128", variant)
 
 
 def test_small_workload_every_output():
     w = WORKLOADS["diag-f32-b1h2t64d16"]
-    _sampled_parity(w.name, "diag", [(0, 0), (0, 1)])
-    _sampled_parity(w.name, "iso", [(0, 0), (0, 1)])
+    _full_parity(w.name, "diag")
+    _full_parity(w.name, "iso")
 
 
 # ------------------------------------------------------------ tensor-core path

@@ -57,6 +57,36 @@ def test_noalloc_matches_workspace_forward_on_two_calls(variant):
             assert max_rel(to_host(o), orc["o"]) <= FP32_TOL
 
 
+@pytest.mark.parametrize("variant", ["diag", "iso"])
+def test_noalloc_tensor_core_split_path_on_two_calls(variant):
+    """The tensor-core path with the sequence split (bf16, d = 128, chunk 64, few
+    long sequences): its scan summaries, carries, segment states and
+    transformed queries are carved from the built-in scratch; two calls in a
+    row must match the workspace-taking entry point."""
+    import torch
+
+    kdn = _kdn()
+    B, T, H, d = 1, 2048, 2, 128
+    vcode = kdn.KDN_DIAG if variant == "diag" else kdn.KDN_ISO
+    assert kdn.forward_kernel_count(vcode, B, T, H, d, d, 64, kdn.KDN_BF16, 0) == 6   # split into segments
+    assert kdn.workspace_size(vcode, B, T, H, d, d, 64, kdn.KDN_BF16, 0) <= 32 * 2 ** 20
+    fwd = kdn.kdn_diag_forward if variant == "diag" else kdn.kdn_iso_forward
+    for call, seed in enumerate((303, 404)):
+        x = make_inputs(variant, B, T, H, d, d, io="bf16", seed=seed)
+        t = to_device(x)
+        args = (t["q"], t["k"], t["v"], t["log_alpha"], t["omega"], t["r"])
+        ref = fwd(*args, chunk=64)
+        outs = tuple(torch.full_like(a, float("nan")) for a in ref)
+        status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        kdn.kdn_forward_noalloc(variant, *args, chunk=64, out=outs, status_out=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, f"call {call}: device status {int(status.item())}"
+        for got, want in zip(outs, ref):
+            g, w = to_host(got), to_host(want)
+            assert np.all(np.isfinite(g))
+            assert np.max(np.abs(g - w)) <= 1e-3 * max(1e-3, np.max(np.abs(w))), f"call {call}"
+
+
 def test_noalloc_refuses_problems_larger_than_its_scratch():
     import torch
 

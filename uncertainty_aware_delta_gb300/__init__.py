@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     KDN_F32,
     KDN_FLAG_NO_SPLIT,
     KDN_FLAG_PORTABLE,
+    KDN_FLAG_TIMEOUT_PROBE,
     KDN_ISO,
     KDN_PKDA,
     KDNError,

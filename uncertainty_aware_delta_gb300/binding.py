@@ -21,11 +21,12 @@ KDN_F32, KDN_BF16 = 0, 1
 KDN_DIAG, KDN_ISO, KDN_PKDA = 0, 1, 2
 KDN_FLAG_PORTABLE = 0x1
 KDN_FLAG_NO_SPLIT = 0x2
+KDN_FLAG_TIMEOUT_PROBE = 0x100   # test facility of the bounded-wait path (include/kdn.h)
 
 EXPORTED = (
     "kdn_workspace_size", "kdn_diag_forward", "kdn_iso_forward", "kdn_step",
     "kdn_read_device_status", "kdn_status_string", "kdn_abi_version", "kdn_forward_kernel_count",
-    "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step",
+    "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step", "kdn_dense_forward", "kdn_step_ex",
 )
 
 
@@ -59,6 +60,9 @@ def library():
                 getattr(lib, name).argtypes = fwd
             lib.kdn_step.restype = i32
             lib.kdn_step.argtypes = [i32] * 5 + [f32, i32] + [vp] * 3 + [fp] * 3 + [fp, fp, vp] + [vp, sz, vp]
+            lib.kdn_step_ex.restype = i32
+            lib.kdn_step_ex.argtypes = [i32] * 5 + [f32, i32, u32] + [vp] * 3 + [fp] * 3 + [fp, fp, vp] + \
+                [vp, sz, vp]
             lib.kdn_pkda_forward.restype = i32
             lib.kdn_pkda_forward.argtypes = [i32] * 6 + [f32, i32, u32] + [vp] * 3 + [fp] * 5 + \
                 [fp, fp] + [vp, fp, fp] + [vp, sz, vp]
@@ -185,8 +189,9 @@ def kdn_iso_forward(q, k, v, log_alpha, omega, r, S0=None, p0=None, *, mu=None, 
 
 
 def kdn_step(variant, q, k, v, log_alpha, omega, r, S, p, *, mu=None, o=None, workspace=None,
-             stream=None):
-    """One decode token per sequence; S and p are updated in place.  Returns o [B,H,dv]."""
+             stream=None, flags=0):
+    """One decode token per sequence; S and p are updated in place.  Returns o [B,H,dv].
+    flags (kdn_step_ex): 0, or KDN_FLAG_TIMEOUT_PROBE in tests of the bounded-wait path."""
     lib = library()
     variant = {"diag": KDN_DIAG, "iso": KDN_ISO}.get(variant, variant)
     device = q.device
@@ -211,9 +216,12 @@ def kdn_step(variant, q, k, v, log_alpha, omega, r, S, p, *, mu=None, o=None, wo
         workspace = torch.empty(need, dtype=torch.uint8, device=device)
     mu = -1.0 if mu is None else float(mu)
     with torch.cuda.device(device):
-        st = lib.kdn_step(variant, B, H, dk, dv, mu, io, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
-                          _ptr(omega), _ptr(r), _ptr(S), _ptr(p), _ptr(o), _ptr(workspace),
-                          workspace.numel() * workspace.element_size(), _stream(stream, device))
+        args = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(omega), _ptr(r), _ptr(S), _ptr(p), _ptr(o),
+                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, device))
+        if flags:
+            st = lib.kdn_step_ex(variant, B, H, dk, dv, mu, io, int(flags), *args)
+        else:
+            st = lib.kdn_step(variant, B, H, dk, dv, mu, io, *args)
     if st != 0:
         raise KDNError(st, "kdn_step")
     return o

@@ -169,6 +169,7 @@ kdn_status forward_impl(int variant, int B, int T, int H, int dk, int dv, int ch
     a.S0 = S0; a.p0 = p0; a.o = o; a.S_T = S_T; a.p_T = p_T; a.status = status;
     a.beta = pk.beta; a.alpha_p = pk.alpha_p; a.beta_p = pk.beta_p; a.center = pk.center;
     a.neg_log2x = -log2f(resolve_x(pk.x));
+    a.flags = flags;
 
     cudaError_t e;
     if (T == 0) {
@@ -252,7 +253,7 @@ kdn_status step_impl(int variant, int B, int H, int dk, int dv, float mu, int io
                      const void* q, const void* k, const void* v, const float* log_alpha,
                      const float* omega, const float* r, float* S, float* p, void* o,
                      void* workspace, size_t workspace_bytes, kdn_stream_t stream,
-                     const PkdaInputs& pk) {
+                     const PkdaInputs& pk, uint32_t flags) {
     kdn_status st = validate_common(variant, B, 1, H, dk, dv, 0, io_dtype);
     if (st != KDN_OK) return st;
     if (!workspace) return KDN_ERR_WORKSPACE;
@@ -287,11 +288,12 @@ kdn_status step_impl(int variant, int B, int H, int dk, int dv, float mu, int io
     a.S = S; a.p = p; a.o = o; a.status = static_cast<uint32_t*>(workspace);
     a.beta = pk.beta; a.alpha_p = pk.alpha_p; a.beta_p = pk.beta_p; a.center = pk.center;
     a.neg_log2x = -log2f(resolve_x(pk.x));
+    a.flags = flags;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (BH == 0) {
-        return cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) == cudaSuccess ? KDN_OK
-                                                                                  : KDN_ERR_CUDA;
-    }
+    // the status word is cleared here, in stream order, so no CTA of the step can
+    // clear a condition another CTA has already recorded
+    if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return KDN_ERR_CUDA;
+    if (BH == 0) return KDN_OK;
     return kdn::launch_step(a, s) == cudaSuccess ? KDN_OK : KDN_ERR_CUDA;
 }
 
@@ -305,7 +307,17 @@ kdn_status kdn_step(int variant, int B, int H, int dk, int dv, float mu, int io_
                     void* workspace, size_t workspace_bytes, kdn_stream_t stream) {
     if (variant != KDN_DIAG && variant != KDN_ISO) return KDN_ERR_SHAPE;
     return step_impl(variant, B, H, dk, dv, mu, io_dtype, q, k, v, log_alpha, omega, r, S, p, o,
-                     workspace, workspace_bytes, stream, PkdaInputs{});
+                     workspace, workspace_bytes, stream, PkdaInputs{}, 0u);
+}
+
+kdn_status kdn_step_ex(int variant, int B, int H, int dk, int dv, float mu, int io_dtype, uint32_t flags,
+                       const void* q, const void* k, const void* v, const float* log_alpha,
+                       const float* omega, const float* r, float* S, float* p, void* o,
+                       void* workspace, size_t workspace_bytes, kdn_stream_t stream) {
+    if (variant != KDN_DIAG && variant != KDN_ISO) return KDN_ERR_SHAPE;
+    if (flags & ~KDN_FLAG_TIMEOUT_PROBE) return KDN_ERR_UNSUPPORTED;
+    return step_impl(variant, B, H, dk, dv, mu, io_dtype, q, k, v, log_alpha, omega, r, S, p, o,
+                     workspace, workspace_bytes, stream, PkdaInputs{}, flags);
 }
 
 kdn_status kdn_pkda_step(int B, int H, int dk, int dv, float x, int io_dtype, const void* q,
@@ -315,7 +327,7 @@ kdn_status kdn_pkda_step(int B, int H, int dk, int dv, float x, int io_dtype, co
                          kdn_stream_t stream) {
     return step_impl(KDN_PKDA, B, H, dk, dv, 0.f, io_dtype, q, k, v, log_alpha, nullptr, nullptr, S,
                      A, o, workspace, workspace_bytes, stream,
-                     PkdaInputs{beta, alpha_p, beta_p, center, x});
+                     PkdaInputs{beta, alpha_p, beta_p, center, x}, 0u);
 }
 
 kdn_status kdn_dense_forward(int B, int T, int H, int d, int io_dtype, const void* q, const void* k,
@@ -392,6 +404,6 @@ const char* kdn_status_string(int status) {
     }
 }
 
-int kdn_abi_version(void) { return 102; }
+int kdn_abi_version(void) { return 103; }
 
 }  // extern "C"

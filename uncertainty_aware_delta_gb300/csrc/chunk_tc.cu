@@ -82,6 +82,8 @@ constexpr int kNT = 384;
 // named barriers
 constexpr int kBarWG1 = 1, kBarWG0 = 2, kBarTReady = 3, kBarOps = 5, kBarWG2 = 6;
 constexpr uint32_t kWaitLimit = 1u << 20;
+// Bound of the timeout probe's wait (KDN_FLAG_TIMEOUT_PROBE): a few milliseconds.
+constexpr uint32_t kProbeWaitLimit = 1u << 12;
 constexpr float kLog2e = 1.4426950408889634f;
 // Chunks whose log-decay stays within this bound use the chunk start as the decay
 // reference (every factor e^{G_t} and its reciprocal fit in fp32 and bf16); the
@@ -113,7 +115,7 @@ constexpr int SM_R = 0, SM_MUR = 64, SM_OMB = 128 /* [2][64] */, SM_ZP = 256 /* 
               SM_FLAG = 1600, SM_CF = 1608 /* [2][128] */, SM_INVD = 1864, SM_CF2 = 1928 /* [128] */,
               SM_FLOATS = 2056;
 constexpr uint32_t OFF_BAR = OFF_SMALL + SM_FLOATS * 4;
-constexpr uint32_t kSmemBytes = OFF_BAR + 80;
+constexpr uint32_t kSmemBytes = OFF_BAR + 88;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 static_assert(OFF_TF + 64 * kLDF * 4 <= OFF_XT, "T fp32 before the merge scratch");
 static_assert(OFF_XT + 32 * kLDX * 4 <= OFF_SMALL, "merge scratch before the small region");
@@ -156,6 +158,7 @@ struct TcParams {
     int last_only;        // final state of the last segment only, to S_T / p_T at bh;
                           // otherwise every CTA writes its final state to S_T at blockIdx.x
     long long p0_bh, p0_seg;   // p0 element offset of (bh, seg): bh * p0_bh + seg * p0_seg
+    int probe;            // timeout probe (KDN_FLAG_TIMEOUT_PROBE): one wait that nothing completes
 };
 
 // Kernel variants: the two KDN uncertainty models and the preconditioned delta
@@ -400,7 +403,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     // (bar_ko), q (bar_q), in the order the passes need them
     const uint32_t bar_la = sb + OFF_BAR, bar_v = bar_la + 8, bar_mma = bar_la + 16, bar_o = bar_la + 24,
                    bar_oj = bar_la + 32, bar_ops = bar_la + 40, bar_ko = bar_la + 48, bar_q = bar_la + 56,
-                   bar_js = bar_la + 72;   // state update of a chunk (once per chunk, parity n & 1)
+                   bar_js = bar_la + 72,   // state update of a chunk (once per chunk, parity n & 1)
+                   bar_probe = bar_la + 80;   // completed by nothing (timeout probe)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool wg0 = tid < 128, wg1 = tid >= 128 && tid < 256, wg2 = tid >= 256;
@@ -420,6 +424,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         mbar_init(bar_oj, 1);
         mbar_init(bar_ops, 1);
         mbar_init(bar_js, 1);
+        mbar_init(bar_probe, 1);
         mbar_fence_init();
         *s_abort = 0;
     }
@@ -855,6 +860,14 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         ++n_oj_issued;
     };
 
+    // Timeout probe (a test of the bounded-wait path): the gains warps wait, with a
+    // short bound, on a barrier that nothing completes while chunk 0's copies are in
+    // flight; the wait gives up, records KDN_ERR_TIMEOUT and the CTA takes its abort
+    // path (no MMA issued, copies in flight drained before exit).
+    if (P.probe && wg1 && !*s_abort && !mbar_wait(bar_probe, 0u, kProbeWaitLimit)) {
+        set_status(P.status, kStatusTimeout);
+        *s_abort = 1;
+    }
     if (wg1 && nchunks > 0) prep_gains(0);   // chunk 0 never splits: pend2 = 0
     ph_in ^= 1u;
     tc_fence_before();
@@ -1297,16 +1310,28 @@ bool tc_path_supported(int io, int dk, int dv, int chunk) {
     return io == 1 && dk == kD && dv == kD && chunk == kC;
 }
 
-// The split runs on one wave of CTAs of the GPU this kernel targets (152 SMs),
-// with segments of at least kMinSegTokens tokens.
-constexpr int kSplitCTAs = 152, kMinSegTokens = 1024;
+// The split runs on one wave of CTAs (one per SM of the current device; 152 on
+// GB300, also taken when no device can be queried), with segments of at least
+// kMinSegTokens tokens.
+constexpr int kDefaultSMs = 152, kMinSegTokens = 1024;
+
+int split_ctas() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();   // no device here: keep the GB300 plan
+        return kDefaultSMs;
+    }
+    return n;
+}
 
 TcSplit tc_split_plan(int B, int T, int H, uint32_t flags) {
     TcSplit sp;
     sp.seg_len = T;
     const long long BH = static_cast<long long>(B) * H;
-    if ((flags & KDN_FLAG_NO_SPLIT) || BH <= 0 || 2 * BH > kSplitCTAs) return sp;
-    long long nseg = kSplitCTAs / BH;
+    const int ctas = split_ctas();
+    if ((flags & KDN_FLAG_NO_SPLIT) || BH <= 0 || 2 * BH > ctas) return sp;
+    long long nseg = ctas / BH;
     if (nseg > T / kMinSegTokens) nseg = T / kMinSegTokens;
     if (nseg < 2) return sp;
     const int G = kGainChunk;   // a multiple of the chunk: segments start on gain-chunk carries
@@ -1356,6 +1381,7 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStrea
     P.last_only = 1;
     P.p0_bh = nu;
     P.p0_seg = 0;
+    P.probe = (a.flags & KDN_FLAG_TIMEOUT_PROBE) ? 1 : 0;
     int grid = a.B * a.H;
     auto launch = [&](auto kernel) {
         const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);

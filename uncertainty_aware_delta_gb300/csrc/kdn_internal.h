@@ -20,6 +20,7 @@ struct ForwardArgs {
     // PKDA only: beta, alpha_p, beta_p [B,T,H], center [H], -log2(x)
     const float *beta, *alpha_p, *beta_p, *center;
     float neg_log2x;
+    uint32_t flags;    // KDN_FLAG_* of the call
 };
 
 // Gain-scan workspace (CUDA-core path): gains and Moebius chunk summaries.
@@ -51,6 +52,7 @@ struct StepArgs {
     uint32_t* status;
     const float *beta, *alpha_p, *beta_p, *center;   // PKDA only
     float neg_log2x;
+    uint32_t flags;     // KDN_FLAG_* of the call
 };
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 

@@ -17,6 +17,7 @@
 // HBM exactly once in each direction, with 128-bit accesses.
 
 #include "common.cuh"
+#include "kdn.h"
 #include "kdn_internal.h"
 #include "sm100.cuh"
 
@@ -42,7 +43,6 @@ step_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TIO* __r
     __shared__ float s_scal[4];
 
     const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (bh == 0 && tid == 0 && status) *status = 0u;
     // -- the one read of this head's S (128-bit loads), issued first so its latency
     //    overlaps the gain computation below
     const int NC4 = DV / 4;                 // float4 columns
@@ -188,12 +188,15 @@ constexpr uint32_t kSBytes = kPD * kPD * 4;
 // shared-memory map (floats): ring [3][128 * 128]; staged vectors [3][6][128]
 // (q, k, v, log_alpha, omega, p); a, a*k, a*q, kappa, delta [5][128]; column partial
 // sums [2][8][128]; warp partials [8][4]; per-head scalars [2][4] by head parity;
-// mbarriers [3]
+// mbarriers [3] of the ring and one that nothing completes (timeout probe)
 constexpr int PS_VEC = kRing * kPD * kPD, PS_A = PS_VEC + kRing * 6 * kPD, PS_PART = PS_A + 5 * kPD,
-              PS_RED = PS_PART + 2 * 8 * kPD, PS_HS = PS_RED + 32, PS_BAR = PS_HS + 8, PS_FLOATS = PS_BAR + 2 * kRing;
+              PS_RED = PS_PART + 2 * 8 * kPD, PS_HS = PS_RED + 32, PS_BAR = PS_HS + 8,
+              PS_FLOATS = PS_BAR + 2 * (kRing + 1);
 constexpr uint32_t kStreamSmem = PS_FLOATS * 4;
 static_assert(PS_BAR % 2 == 0, "mbarriers 8-byte aligned");
 constexpr uint32_t kStreamWaitLimit = 1u << 20;
+// Bound of the timeout probe's wait (KDN_FLAG_TIMEOUT_PROBE): a few milliseconds.
+constexpr uint32_t kProbeWaitLimit = 1u << 12;
 
 template <typename TIO, int V>
 __global__ void __launch_bounds__(kPNT, 1)
@@ -202,7 +205,7 @@ step_stream_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const T
                    float* S, float* p, TIO* __restrict__ o, float mu, uint32_t* status,
                    const float* __restrict__ beta, const float* __restrict__ alpha_p,
                    const float* __restrict__ beta_p, const float* __restrict__ center, float neg_log2x,
-                   int BH, int H) {
+                   int BH, int H, int probe) {
     using namespace sm100;
     constexpr bool DIAG = V == 0, ISO = V == 1, PK = V == 2;
     extern __shared__ __align__(128) float sm[];
@@ -216,9 +219,9 @@ step_stream_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const T
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c4 = tid & 31, rg = tid >> 5;   // float4 column group, row group (rows rg + 8 m)
     const int G = gridDim.x, nh = (BH - static_cast<int>(blockIdx.x) + G - 1) / G;
-    if (blockIdx.x == 0 && tid == 0 && status) *status = 0u;
+    const uint32_t bar_probe = bar_s + 8 * kRing;   // completed by nothing (timeout probe)
     if (tid == 0) {
-        for (int e = 0; e < kRing; ++e) mbar_init(bar_s + 8 * e, 1);
+        for (int e = 0; e <= kRing; ++e) mbar_init(bar_s + 8 * e, 1);
         mbar_fence_init();
     }
     __syncthreads();
@@ -269,7 +272,11 @@ step_stream_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const T
         const size_t bh = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(n) * G;
         const int slot = n % kRing;
         if (tid == 0 && n + 1 < nh) load_scalars(n + 1, hsn);   // in flight during this head
-        const bool ok = mbar_wait(bar_s + 8 * slot, static_cast<uint32_t>(n / kRing) & 1u, kStreamWaitLimit);
+        // (timeout probe: the first head's wait is on a barrier that nothing completes,
+        //  with a short bound, while that head's copies are in flight)
+        const bool ok = (probe && n == 0)
+                            ? mbar_wait(bar_probe, 0u, kProbeWaitLimit)
+                            : mbar_wait(bar_s + 8 * slot, static_cast<uint32_t>(n / kRing) & 1u, kStreamWaitLimit);
         if (__syncthreads_or(!ok)) {
             if (tid == 0) set_status(status, kStatusTimeout);
             break;
@@ -431,7 +438,8 @@ cudaError_t launch_stream(const StepArgs& a, int BH, int nsm, cudaStream_t s) {
     kern<<<grid, kPNT, kStreamSmem, s>>>(static_cast<const TIO*>(a.q), static_cast<const TIO*>(a.k),
                                          static_cast<const TIO*>(a.v), a.log_alpha, a.omega, a.r, a.S, a.p,
                                          static_cast<TIO*>(a.o), a.mu, a.status, a.beta, a.alpha_p, a.beta_p,
-                                         a.center, a.neg_log2x, BH, a.H);
+                                         a.center, a.neg_log2x, BH, a.H,
+                                         (a.flags & KDN_FLAG_TIMEOUT_PROBE) ? 1 : 0);
     return cudaGetLastError();
 }
 
