@@ -292,6 +292,44 @@ kdn_status kdn_dense_forward(int B, int T, int H, int d, int io_dtype,
                              void *o, float *S_T, float *P_T, kdn_stream_t stream);
 
 /*
+ * Backward pass of the Diagonal or Isotropic KDN forward: the gradients of
+ *
+ *     L = sum(dO * o) + sum(dS_T * S_T) + sum(dp_T * p_T)
+ *
+ * with respect to every input of kdn_diag_forward / kdn_iso_forward.  The pages
+ * define the forward recurrence only (KDN paper Sec. 4.1 Eq. 23-27 and 60-65, Sec.
+ * 4.2 Eq. 40 and App. C); these are the exact adjoint of that recurrence (its
+ * training scans, Sec. 5.1), evaluated in the compact-WY chunk form of App. D with
+ * the gains from the forward's Moebius gain scan (Eq. 32-37), on CUDA cores in fp32.
+ *
+ * variant: KDN_DIAG or KDN_ISO.  Inputs q, k, v, log_alpha, omega, r, S0, p0, mu
+ * and io_dtype exactly as for the forward call being differentiated (S0, p0 may be
+ * NULL: zero memory, unit variances).  Upstream gradients: dO [B,T,H,dv] in
+ * io_dtype, dS_T [B,H,dk,dv] and dp_T ([B,H,dk] or [B,H]) fp32; each may be NULL
+ * (zero).  Outputs, all fp32, all required: grad_q, grad_k [B,T,H,dk]; grad_v
+ * [B,T,H,dv]; grad_log_alpha [B,T,H,dk]; grad_omega [B,T,H,dk] (Diagonal) or
+ * [B,T,H] (Isotropic); grad_r [B,T,H]; grad_S0 [B,H,dk,dv]; grad_p0 [B,H,dk] or
+ * [B,H] (the gradients with respect to S0 and p0, or to their defaults when those
+ * are NULL).  Outputs must not overlap each other, the inputs or the workspace.
+ * Sizes: dk, dv in {16, 32, 64, 128}; any T >= 0; B, H >= 0.
+ * Workspace: kdn_backward_workspace_size() bytes (gains, the state at every
+ * 16-token chunk start -- 4 dk dv bytes per chunk and head -- and the gain
+ * gradients); its first 256 bytes hold the device status word.
+ * Errors: as kdn_diag_forward; KDN_ERR_RANGE in the status word when a chunk's
+ * cumulative log-decay leaves the supported range.
+ */
+size_t kdn_backward_workspace_size(int variant, int B, int T, int H, int dk, int dv, int io_dtype);
+
+kdn_status kdn_backward(int variant, int B, int T, int H, int dk, int dv, float mu, int io_dtype,
+                        const void *q, const void *k, const void *v,
+                        const float *log_alpha, const float *omega, const float *r,
+                        const float *S0, const float *p0,
+                        const void *dO, const float *dS_T, const float *dp_T,
+                        float *grad_q, float *grad_k, float *grad_v, float *grad_log_alpha,
+                        float *grad_omega, float *grad_r, float *grad_S0, float *grad_p0,
+                        void *workspace, size_t workspace_bytes, kdn_stream_t stream);
+
+/*
  * Forward without a caller workspace.  The paper has no counterpart: this is
  * a convenience of the library for callers that cannot allocate device
  * memory at the point where they run the mixer -- for example code inside a

@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     for n in ("kdn_diag_forward", "kdn_iso_forward", "kdn_step", "kdn_workspace_size",
               "kdn_read_device_status", "kdn_status_string", "kdn_abi_version",
               "kdn_forward_kernel_count", "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step",
-              "kdn_dense_forward", "kdn_step_ex"):
+              "kdn_dense_forward", "kdn_step_ex", "kdn_backward", "kdn_backward_workspace_size"):
         assert n in names
 
 
@@ -47,7 +47,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings_and_version(lib):
     import uncertainty_aware_delta_gb300 as kdn
 
-    assert lib.kdn_abi_version() == 103
+    assert lib.kdn_abi_version() == 104
     for code in range(0, 11):
         s = kdn.status_string(code)
         assert s and s != "unknown status"

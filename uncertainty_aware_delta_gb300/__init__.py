@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     KDN_ISO,
     KDN_PKDA,
     KDNError,
+    kdn_backward,
     kdn_diag_forward,
     kdn_forward_noalloc,
     kdn_iso_forward,

@@ -27,6 +27,7 @@ EXPORTED = (
     "kdn_workspace_size", "kdn_diag_forward", "kdn_iso_forward", "kdn_step",
     "kdn_read_device_status", "kdn_status_string", "kdn_abi_version", "kdn_forward_kernel_count",
     "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step", "kdn_dense_forward", "kdn_step_ex",
+    "kdn_backward", "kdn_backward_workspace_size",
 )
 
 
@@ -80,6 +81,11 @@ def library():
                 [vp, fp, fp, vp, vp]
             lib.kdn_dense_forward.restype = i32
             lib.kdn_dense_forward.argtypes = [i32] * 5 + [vp] * 3 + [fp] * 5 + [vp, fp, fp, vp]
+            lib.kdn_backward_workspace_size.restype = sz
+            lib.kdn_backward_workspace_size.argtypes = [i32] * 7
+            lib.kdn_backward.restype = i32
+            lib.kdn_backward.argtypes = [i32] * 6 + [f32, i32] + [vp] * 3 + [fp] * 5 + [vp, fp, fp] + [fp] * 8 + \
+                [vp, sz, vp]
             lib.kdn_abi_version.restype = i32
             lib.kdn_abi_version.argtypes = []
             _lib = lib
@@ -380,6 +386,45 @@ def kdn_dense_forward(q, k, v, log_alpha, omega, r, S0=None, P0=None, *, out=Non
     if st != 0:
         raise KDNError(st, "kdn_dense_forward")
     return o, S_T, P_T
+
+
+def kdn_backward(variant, q, k, v, log_alpha, omega, r, S0=None, p0=None, dO=None, dS_T=None, dp_T=None, *,
+                 mu=None, workspace=None, stream=None):
+    """Gradients of sum(dO o) + sum(dS_T S_T) + sum(dp_T p_T) of the KDN forward with these
+    inputs.  Returns a dict of fp32 tensors: q, k, v, log_alpha, omega, r, S0, p0."""
+    lib = library()
+    variant = {"diag": KDN_DIAG, "iso": KDN_ISO}.get(variant, variant)
+    device = q.device
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    io = KDN_BF16 if q.dtype == torch.bfloat16 else KDN_F32
+    iot = torch.bfloat16 if io == KDN_BF16 else torch.float32
+    nu = (dk,) if variant == KDN_DIAG else ()
+    for t, name, dt, shape in ((q, "q", iot, (B, T, H, dk)), (k, "k", iot, (B, T, H, dk)),
+                               (v, "v", iot, (B, T, H, dv)), (log_alpha, "log_alpha", torch.float32, (B, T, H, dk)),
+                               (omega, "omega", torch.float32, (B, T, H) + nu), (r, "r", torch.float32, (B, T, H)),
+                               (S0, "S0", torch.float32, (B, H, dk, dv)), (p0, "p0", torch.float32, (B, H) + nu),
+                               (dO, "dO", iot, (B, T, H, dv)), (dS_T, "dS_T", torch.float32, (B, H, dk, dv)),
+                               (dp_T, "dp_T", torch.float32, (B, H) + nu)):
+        _check(t, name, dt, shape, device)
+    f = dict(dtype=torch.float32, device=device)
+    g = {"q": torch.empty((B, T, H, dk), **f), "k": torch.empty((B, T, H, dk), **f),
+         "v": torch.empty((B, T, H, dv), **f), "log_alpha": torch.empty((B, T, H, dk), **f),
+         "omega": torch.empty((B, T, H) + nu, **f), "r": torch.empty((B, T, H), **f),
+         "S0": torch.empty((B, H, dk, dv), **f), "p0": torch.empty((B, H) + nu, **f)}
+    need = lib.kdn_backward_workspace_size(variant, B, T, H, dk, dv, io)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    mu = -1.0 if mu is None else float(mu)
+    with torch.cuda.device(device):
+        st = lib.kdn_backward(variant, B, T, H, dk, dv, mu, io, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                              _ptr(omega), _ptr(r), _ptr(S0), _ptr(p0), _ptr(dO), _ptr(dS_T), _ptr(dp_T),
+                              *(_ptr(g[n]) for n in ("q", "k", "v", "log_alpha", "omega", "r", "S0", "p0")),
+                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _stream(stream, device))
+    if st != 0:
+        raise KDNError(st, "kdn_backward")
+    return g
 
 
 def kdn_read_device_status(workspace, stream=None) -> int:

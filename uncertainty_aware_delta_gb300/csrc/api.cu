@@ -366,6 +366,121 @@ kdn_status kdn_dense_forward(int B, int T, int H, int d, int io_dtype, const voi
                                                                                               : KDN_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace {
+
+struct BwLayout {
+    size_t total, kappa_off, summary_off, carry_off, pscr_off, ckpt_off, dkappa_off, pck_off;
+    int nG;
+};
+
+BwLayout bw_layout(int variant, int B, int T, int H, int dk, int dv) {
+    BwLayout w;
+    memset(&w, 0, sizeof(w));
+    const size_t BH = (size_t)B * H, nu = variant == KDN_ISO ? 1 : (size_t)dk, ntok = (size_t)B * T * H;
+    const size_t nch = (T + kdn::backward_chunk() - 1) / kdn::backward_chunk();
+    const size_t nblk = (T + kdn::backward_block() - 1) / kdn::backward_block();
+    w.nG = (T + kdn::kGainChunk - 1) / kdn::kGainChunk;
+    size_t off = kStatusBytes;
+    w.kappa_off = off;
+    off = align_up(off + 4 * ntok * dk);
+    w.summary_off = off;
+    off = align_up(off + 4 * 4 * BH * w.nG * nu);
+    w.carry_off = off;
+    off = align_up(off + 4 * BH * w.nG * nu);
+    w.pscr_off = off;
+    off = align_up(off + 4 * BH * nu);
+    w.ckpt_off = off;
+    off = align_up(off + 4 * BH * (nch + 1) * dk * dv);
+    w.dkappa_off = off;
+    off = align_up(off + 4 * ntok * dk);
+    w.pck_off = off;
+    off = align_up(off + 4 * BH * nblk * nu);
+    w.total = off;
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kdn_backward_workspace_size(int variant, int B, int T, int H, int dk, int dv, int io_dtype) {
+    if (variant != KDN_DIAG && variant != KDN_ISO) return 0;
+    if (validate_common(variant, B, T, H, dk, dv, 0, io_dtype) != KDN_OK) return 0;
+    return bw_layout(variant, B, T, H, dk, dv).total;
+}
+
+kdn_status kdn_backward(int variant, int B, int T, int H, int dk, int dv, float mu, int io_dtype,
+                        const void* q, const void* k, const void* v, const float* log_alpha,
+                        const float* omega, const float* r, const float* S0, const float* p0,
+                        const void* dO, const float* dS_T, const float* dp_T, float* dq, float* dk_out,
+                        float* dv_out, float* dlog_alpha, float* domega, float* dr, float* dS0,
+                        float* dp0, void* workspace, size_t workspace_bytes, kdn_stream_t stream) {
+    if (variant != KDN_DIAG && variant != KDN_ISO) return KDN_ERR_SHAPE;
+    kdn_status st = validate_common(variant, B, T, H, dk, dv, 0, io_dtype);
+    if (st != KDN_OK) return st;
+    const size_t BH = (size_t)B * H, ntok = (size_t)B * T * H, esz = io_dtype == KDN_BF16 ? 2 : 4;
+    const size_t nu = variant == KDN_ISO ? 1 : (size_t)dk;
+    if (!workspace) return KDN_ERR_WORKSPACE;
+    if (BH > 0 && (!dS0 || !dp0)) return KDN_ERR_NULL;
+    if (ntok > 0 && (!q || !k || !v || !log_alpha || !omega || !r || !dq || !dk_out || !dv_out ||
+                     !dlog_alpha || !domega || !dr))
+        return KDN_ERR_NULL;
+    const void* ptrs[] = {q, k, v, log_alpha, omega, r, S0, p0, dO, dS_T, dp_T, dq, dk_out, dv_out,
+                          dlog_alpha, domega, dr, dS0, dp0, workspace};
+    for (const void* x : ptrs)
+        if (x && !aligned16(x)) return KDN_ERR_ALIGN;
+    const BwLayout w = bw_layout(variant, B, T, H, dk, dv);
+    if (workspace_bytes < w.total) return KDN_ERR_WORKSPACE;
+    const Range in[] = {{q, ntok * dk * esz}, {k, ntok * dk * esz}, {v, ntok * dv * esz},
+                        {log_alpha, ntok * dk * 4}, {omega, ntok * nu * 4}, {r, ntok * 4},
+                        {S0, BH * dk * dv * 4}, {p0, BH * nu * 4}, {dO, ntok * dv * esz},
+                        {dS_T, BH * dk * dv * 4}, {dp_T, BH * nu * 4}};
+    const Range out[] = {{dq, ntok * dk * 4}, {dk_out, ntok * dk * 4}, {dv_out, ntok * dv * 4},
+                         {dlog_alpha, ntok * dk * 4}, {domega, ntok * nu * 4}, {dr, ntok * 4},
+                         {dS0, BH * dk * dv * 4}, {dp0, BH * nu * 4}, {workspace, w.total}};
+    const int nout = sizeof(out) / sizeof(out[0]);
+    for (int o1 = 0; o1 < nout; ++o1) {
+        for (const Range& x : in)
+            if (overlaps(out[o1], x)) return KDN_ERR_ALIAS;
+        for (int o2 = o1 + 1; o2 < nout; ++o2)
+            if (overlaps(out[o1], out[o2])) return KDN_ERR_ALIAS;
+    }
+    if (kdn::backward_mem_smem_bytes(dk, dv) > 232448) return KDN_ERR_UNSUPPORTED;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t* status = static_cast<uint32_t*>(workspace);
+    if (cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess) return KDN_ERR_CUDA;
+    if (BH == 0) return KDN_OK;
+    if (T == 0) {   // nothing between the initial and the final state
+        const size_t nS = BH * dk * dv * 4, np = BH * nu * 4;
+        cudaError_t e = dS_T ? cudaMemcpyAsync(dS0, dS_T, nS, cudaMemcpyDeviceToDevice, s)
+                             : cudaMemsetAsync(dS0, 0, nS, s);
+        if (e == cudaSuccess)
+            e = dp_T ? cudaMemcpyAsync(dp0, dp_T, np, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(dp0, 0, np, s);
+        return e == cudaSuccess ? KDN_OK : KDN_ERR_CUDA;
+    }
+    kdn::BackwardArgs a;
+    a.variant = variant; a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.io = io_dtype;
+    a.mu = mu < 0.f ? (float)dk : mu;
+    a.q = q; a.k = k; a.v = v; a.dO = dO; a.log_alpha = log_alpha; a.omega = omega; a.r = r;
+    a.S0 = S0; a.p0 = p0; a.dS_T = dS_T; a.dp_T = dp_T;
+    a.dq = dq; a.dk_out = dk_out; a.dv_out = dv_out; a.dla = dlog_alpha; a.domega = domega; a.dr = dr;
+    a.dS0 = dS0; a.dp0 = dp0; a.status = status;
+    char* base = static_cast<char*>(workspace);
+    kdn::BackwardWorkspace bw;
+    bw.kappa = reinterpret_cast<float*>(base + w.kappa_off);
+    bw.summary = reinterpret_cast<float*>(base + w.summary_off);
+    bw.carry = reinterpret_cast<float*>(base + w.carry_off);
+    bw.n_chunks_g = w.nG;
+    bw.p_scratch = reinterpret_cast<float*>(base + w.pscr_off);
+    bw.ckpt = reinterpret_cast<float*>(base + w.ckpt_off);
+    bw.dkappa = reinterpret_cast<float*>(base + w.dkappa_off);
+    bw.pck = reinterpret_cast<float*>(base + w.pck_off);
+    return kdn::launch_backward(a, bw, s) == cudaSuccess ? KDN_OK : KDN_ERR_CUDA;
+}
+
 kdn_status kdn_read_device_status(const void* workspace, kdn_stream_t stream) {
     if (!workspace) return KDN_ERR_NULL;
     uint32_t word = 0;
@@ -404,6 +519,6 @@ const char* kdn_status_string(int status) {
     }
 }
 
-int kdn_abi_version(void) { return 103; }
+int kdn_abi_version(void) { return 104; }
 
 }  // extern "C"

@@ -1,0 +1,542 @@
+// Backward pass of the KDN mixer on CUDA cores (fp32): the gradients of a weighted
+// sum  sum(dO * o) + sum(dS_T * S_T) + sum(dp_T * p_T)  with respect to every input
+// of kdn_diag_forward / kdn_iso_forward.
+//
+// The pages define the forward recurrence only (KDN paper Sec. 4.1 Eq. 23-27 and
+// 60-65, Sec. 4.2 Eq. 40 and App. C); the gradients are the adjoint of that
+// recurrence, evaluated in the chunk form the forward uses (App. D).  With the gains
+// kappa_t known, the memory of one chunk of C tokens in its reference frame is
+//     S_m   = diag(g_in) S_0,                g_in  = exp(G_ref),
+//     (I + L) Delta = X,  X = V - K_bar S_m, L = strict_lower(K_bar K_til^T),
+//     O     = Q_bar S_m + A Delta,           A = lower_incl(Q_bar K_til^T),
+//     S_out = diag(g_out) (S_m + K_til^T Delta),  g_out = exp(G_C - G_ref),
+// with K_bar = k exp(G - G_ref), Q_bar = q exp(G - G_ref), K_til = kappa exp(G_ref - G)
+// (G the cumulative log-decay since the chunk start).  Its adjoint, given dO and the
+// gradient dS_out of the chunk's end state, is (Gp = diag(g_out) dS_out)
+//     dDelta = K_til Gp + A^T dO,     (I + L)^T dX = dDelta,      dV = dX,
+//     dK_til = Delta Gp^T + dL^T K_bar + dA^T Q_bar,   dQ_bar = dO S_m^T + dA K_til,
+//     dK_bar = -dX S_m^T + dL K_til,   dA = lower_incl(dO Delta^T),
+//     dL = strict_lower(-dX Delta^T),  dS_m = Gp + Q_bar^T dO - K_bar^T dX,
+//     dS_0 = diag(g_in) dS_m,
+// and the decay enters through d/dG of K_bar, Q_bar, K_til and g_out (G_ref cancels
+// out of the result, so it is held fixed).  Kernels:
+//   mem_adjoint_kernel    one CTA per (b, h): a forward sweep over the chunks that
+//                         stores the state at every chunk start, then the reverse
+//                         sweep above, writing dq, dv, the memory parts of dk and
+//                         d log_alpha, dkappa and dS_0;
+//   gain_adjoint_kernel   one CTA per (b, h), one thread per key channel: the
+//                         uncertainty recurrence recomputed from checkpoints every
+//                         kPB tokens and run backwards token by token (the adjoint of
+//                         the gain and of the Moebius update), adding the gain parts of
+//                         dk and d log_alpha and writing d omega, dr and dp_0.
+// The gains kappa come from the forward's gain scan (scan.cu).
+
+#include <string.h>
+
+#include "common.cuh"
+#include "kdn_internal.h"
+
+namespace kdn {
+namespace {
+
+constexpr int kBC = 16;       // tokens per chunk of the memory adjoint
+constexpr int kMNT = 256;     // threads of the memory adjoint
+constexpr int kPB = 64;       // tokens per checkpoint block of the gain adjoint
+
+// C(r, c) (+)= alpha sum_k A(r, k) B(k, c) on shared-memory operands with arbitrary
+// strides: A(r, k) = A[r ar + k ak], B(k, c) = B[k bk + c bc], C(r, c) = C[r cr + c].
+// A warp computes TR rows x 32 TCH columns at a time (lane = column within a group
+// of 32); every thread of the block takes part.
+template <int TR, int TCH>
+__device__ void smem_gemm(int R, int N, int K, const float* A, int ar, int ak, const float* B, int bk, int bc,
+                          float* C, int cr, float alpha, bool accumulate) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int nrb = (R + TR - 1) / TR, ncb = (N + 32 * TCH - 1) / (32 * TCH);
+    for (int u = warp; u < nrb * ncb; u += nw) {
+        const int r0 = (u / ncb) * TR, c0 = (u % ncb) * 32 * TCH;
+        float acc[TR][TCH];
+#pragma unroll
+        for (int r = 0; r < TR; ++r)
+#pragma unroll
+            for (int m = 0; m < TCH; ++m) acc[r][m] = 0.f;
+        for (int k = 0; k < K; ++k) {
+            float a[TR], bv[TCH];
+#pragma unroll
+            for (int r = 0; r < TR; ++r) a[r] = (r0 + r < R) ? A[(r0 + r) * ar + k * ak] : 0.f;
+#pragma unroll
+            for (int m = 0; m < TCH; ++m) {
+                const int c = c0 + 32 * m + lane;
+                bv[m] = c < N ? B[k * bk + c * bc] : 0.f;
+            }
+#pragma unroll
+            for (int r = 0; r < TR; ++r)
+#pragma unroll
+                for (int m = 0; m < TCH; ++m) acc[r][m] = fmaf(a[r], bv[m], acc[r][m]);
+        }
+#pragma unroll
+        for (int r = 0; r < TR; ++r)
+#pragma unroll
+            for (int m = 0; m < TCH; ++m) {
+                const int c = c0 + 32 * m + lane;
+                if (r0 + r < R && c < N) {
+                    float* d = C + (r0 + r) * cr + c;
+                    *d = accumulate ? fmaf(alpha, acc[r][m], *d) : alpha * acc[r][m];
+                }
+            }
+    }
+}
+
+struct MemArgs {
+    const void *q, *k, *v, *dO;
+    const float *la, *kappa, *S0, *dS_T;
+    float *ckpt;                    // [B*H][nch + 1][DK][DV] states at chunk starts
+    float *dq, *dk, *dv, *dla, *dkappa, *dS0;
+    int T, H, DK, DV;
+    uint32_t* status;
+};
+
+size_t mem_smem_floats(int DK, int DV) {
+    const int LSK = DK + 1, LSV = DV + 1, LCC = kBC + 1;
+    return (size_t)2 * DK * LSV + 6 * kBC * LSK + 3 * kBC * LSV + 4 * kBC * LCC + 4 * DK;
+}
+
+template <typename TIO>
+__global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
+    const int DK = P.DK, DV = P.DV, LSK = DK + 1, LSV = DV + 1, LCC = kBC + 1;
+    extern __shared__ float sm[];
+    float* Sm = sm;                    // [DK][LSV] chunk-start state, then S_m
+    float* dS = Sm + DK * LSV;         // [DK][LSV] gradient of the chunk's end state
+    float* Kb = dS + DK * LSV;         // [kBC][LSK]
+    float* Qb = Kb + kBC * LSK;
+    float* Kt = Qb + kBC * LSK;
+    float* dKb = Kt + kBC * LSK;
+    float* dQb = dKb + kBC * LSK;
+    float* dKt = dQb + kBC * LSK;
+    float* X = dKt + kBC * LSK;        // [kBC][LSV] V - K_bar S_m, then Delta
+    float* dO = X + kBC * LSV;         // [kBC][LSV]
+    float* dX = dO + kBC * LSV;        // [kBC][LSV] dDelta, then the adjoint of X
+    float* L = dX + kBC * LSV;         // [kBC][LCC]
+    float* Am = L + kBC * LCC;
+    float* dL = Am + kBC * LCC;
+    float* dA = dL + kBC * LCC;
+    float* gref = dA + kBC * LCC;      // [DK]
+    float* gin = gref + DK;
+    float* gout = gin + DK;
+    float* eS = gout + DK;             // [DK] sum_j dS_out S_out (dG of the chunk's last token)
+
+    const int bh = blockIdx.x, H = P.H, T = P.T, b = bh / H, h = bh % H, tid = threadIdx.x;
+    const int nch = (T + kBC - 1) / kBC;
+    const size_t sdd = (size_t)DK * DV;
+    float* ck = P.ckpt + (size_t)bh * (nch + 1) * sdd;
+    auto row = [&](int t) { return ((size_t)b * T + t) * H + h; };   // token-head index
+
+    // per-chunk setup: cumulative log-decay (in Kt, read as G), reference and factors;
+    // the operands K_bar, Q_bar, K_til; S_m = diag(g_in) S_0 with S_0 in Sm
+    auto setup = [&](int n, int nv) {
+        const int t0 = n * kBC;
+        if (tid < DK) {
+            float g = 0.f;
+            for (int t = 0; t < kBC; ++t) {
+                if (t < nv) g += P.la[row(t0 + t) * DK + tid];
+                Kt[t * LSK + tid] = g;
+            }
+            const float gr = 0.5f * g;
+            gref[tid] = gr;
+            gin[tid] = expf(gr);
+            gout[tid] = expf(g - gr);
+            if (!(fabsf(g) <= kMaxChunkLogDecay)) set_status(P.status, kStatusRange);
+        }
+        __syncthreads();
+        for (int e = tid; e < kBC * DK; e += kMNT) {
+            const int t = e / DK, i = e % DK;
+            if (t < nv) {
+                const size_t gi = row(t0 + t) * DK + i;
+                const float g = Kt[t * LSK + i];
+                const float ef = expf(g - gref[i]);
+                Kb[t * LSK + i] = IO<TIO>::load(static_cast<const TIO*>(P.k), gi) * ef;
+                Qb[t * LSK + i] = IO<TIO>::load(static_cast<const TIO*>(P.q), gi) * ef;
+                Kt[t * LSK + i] = P.kappa[gi] / ef;
+            } else {
+                Kb[t * LSK + i] = 0.f;
+                Qb[t * LSK + i] = 0.f;
+                Kt[t * LSK + i] = 0.f;
+            }
+        }
+        for (int e = tid; e < DK * DV; e += kMNT) {
+            const int i = e / DV, j = e % DV;
+            Sm[i * LSV + j] *= gin[i];
+        }
+        for (int e = tid; e < kBC * DV; e += kMNT) {
+            const int t = e / DV, j = e % DV;
+            X[t * LSV + j] = t < nv ? IO<TIO>::load(static_cast<const TIO*>(P.v), row(t0 + t) * DV + j) : 0.f;
+        }
+        __syncthreads();
+        // L = strict_lower(K_bar K_til^T), A = lower_incl(Q_bar K_til^T), X = V - K_bar S_m
+        smem_gemm<1, 1>(kBC, kBC, DK, Kb, LSK, 1, Kt, 1, LSK, L, LCC, 1.f, false);
+        smem_gemm<1, 1>(kBC, kBC, DK, Qb, LSK, 1, Kt, 1, LSK, Am, LCC, 1.f, false);
+        smem_gemm<2, 4>(kBC, DV, DK, Kb, LSK, 1, Sm, LSV, 1, X, LSV, -1.f, true);
+        __syncthreads();
+        for (int e = tid; e < kBC * kBC; e += kMNT) {
+            const int t = e / kBC, s = e % kBC;
+            if (s >= t) L[t * LCC + s] = 0.f;
+            if (s > t) Am[t * LCC + s] = 0.f;
+        }
+        __syncthreads();
+        // forward substitution (I + L) Delta = X (one row at a time, a thread per column)
+        for (int t = 1; t < nv; ++t) {
+            for (int j = tid; j < DV; j += kMNT) {
+                float acc = X[t * LSV + j];
+                for (int s = 0; s < t; ++s) acc = fmaf(-L[t * LCC + s], X[s * LSV + j], acc);
+                X[t * LSV + j] = acc;
+            }
+            __syncthreads();
+        }
+    };
+
+    // ---- forward sweep: the state at every chunk start
+    for (int e = tid; e < DK * DV; e += kMNT) {
+        const int i = e / DV, j = e % DV;
+        Sm[i * LSV + j] = P.S0 ? P.S0[(size_t)bh * sdd + i * DV + j] : 0.f;
+    }
+    __syncthreads();
+    for (int n = 0; n < nch; ++n) {
+        const int nv = min(kBC, T - n * kBC);
+        for (int e = tid; e < DK * DV; e += kMNT) ck[(size_t)n * sdd + e] = Sm[(e / DV) * LSV + e % DV];
+        setup(n, nv);
+        // S_out = diag(g_out) (S_m + K_til^T Delta)
+        smem_gemm<2, 4>(DK, DV, kBC, Kt, 1, LSK, X, LSV, 1, Sm, LSV, 1.f, true);
+        __syncthreads();
+        for (int e = tid; e < DK * DV; e += kMNT) {
+            const int i = e / DV, j = e % DV;
+            Sm[i * LSV + j] *= gout[i];
+        }
+        __syncthreads();
+    }
+    for (int e = tid; e < DK * DV; e += kMNT) ck[(size_t)nch * sdd + e] = Sm[(e / DV) * LSV + e % DV];
+    __syncthreads();
+
+    // ---- reverse sweep
+    for (int e = tid; e < DK * DV; e += kMNT) {
+        const int i = e / DV, j = e % DV;
+        dS[i * LSV + j] = P.dS_T ? P.dS_T[(size_t)bh * sdd + i * DV + j] : 0.f;
+    }
+    for (int n = nch - 1; n >= 0; --n) {
+        const int t0 = n * kBC, nv = min(kBC, T - t0);
+        for (int e = tid; e < DK * DV; e += kMNT) Sm[(e / DV) * LSV + e % DV] = ck[(size_t)n * sdd + e];
+        __syncthreads();
+        setup(n, nv);   // Sm = S_m, X = Delta, operands, L, A
+        // dG at the chunk's last token from S_out = diag(g_out)(...): sum_j dS_out S_out
+        if (tid < DK) {
+            float acc = 0.f;
+            const float* so = ck + (size_t)(n + 1) * sdd + (size_t)tid * DV;
+            for (int j = 0; j < DV; ++j) acc = fmaf(dS[tid * LSV + j], so[j], acc);
+            eS[tid] = acc;
+        }
+        for (int e = tid; e < kBC * DV; e += kMNT) {
+            const int t = e / DV, j = e % DV;
+            dO[t * LSV + j] = (t < nv && P.dO) ? IO<TIO>::load(static_cast<const TIO*>(P.dO), row(t0 + t) * DV + j) : 0.f;
+        }
+        __syncthreads();
+        for (int e = tid; e < DK * DV; e += kMNT) {   // Gp = diag(g_out) dS_out
+            const int i = e / DV, j = e % DV;
+            dS[i * LSV + j] *= gout[i];
+        }
+        __syncthreads();
+        // dDelta = K_til Gp + A^T dO;  dK_til = Delta Gp^T;  dQ_bar = dO S_m^T;  dA = dO Delta^T
+        smem_gemm<2, 4>(kBC, DV, DK, Kt, LSK, 1, dS, LSV, 1, dX, LSV, 1.f, false);
+        smem_gemm<2, 4>(kBC, DK, DV, X, LSV, 1, dS, 1, LSV, dKt, LSK, 1.f, false);
+        smem_gemm<2, 4>(kBC, DK, DV, dO, LSV, 1, Sm, 1, LSV, dQb, LSK, 1.f, false);
+        smem_gemm<1, 1>(kBC, kBC, DV, dO, LSV, 1, X, 1, LSV, dA, LCC, 1.f, false);
+        __syncthreads();
+        smem_gemm<2, 4>(kBC, DV, kBC, Am, 1, LCC, dO, LSV, 1, dX, LSV, 1.f, true);
+        for (int e = tid; e < kBC * kBC; e += kMNT) {
+            const int t = e / kBC, s = e % kBC;
+            if (s > t) dA[t * LCC + s] = 0.f;
+        }
+        __syncthreads();
+        // back substitution (I + L)^T dX = dDelta
+        for (int t = nv - 2; t >= 0; --t) {
+            for (int j = tid; j < DV; j += kMNT) {
+                float acc = dX[t * LSV + j];
+                for (int s = t + 1; s < nv; ++s) acc = fmaf(-L[s * LCC + t], dX[s * LSV + j], acc);
+                dX[t * LSV + j] = acc;
+            }
+            __syncthreads();
+        }
+        // dL = strict_lower(-dX Delta^T); dK_bar = -dX S_m^T
+        smem_gemm<1, 1>(kBC, kBC, DV, dX, LSV, 1, X, 1, LSV, dL, LCC, -1.f, false);
+        smem_gemm<2, 4>(kBC, DK, DV, dX, LSV, 1, Sm, 1, LSV, dKb, LSK, -1.f, false);
+        __syncthreads();
+        for (int e = tid; e < kBC * kBC; e += kMNT) {
+            const int t = e / kBC, s = e % kBC;
+            if (s >= t) dL[t * LCC + s] = 0.f;
+        }
+        __syncthreads();
+        // dK_bar += dL K_til; dK_til += dL^T K_bar + dA^T Q_bar; dQ_bar += dA K_til;
+        // dS_m = Gp + Q_bar^T dO - K_bar^T dX
+        smem_gemm<2, 4>(kBC, DK, kBC, dL, LCC, 1, Kt, LSK, 1, dKb, LSK, 1.f, true);
+        smem_gemm<2, 4>(kBC, DK, kBC, dL, 1, LCC, Kb, LSK, 1, dKt, LSK, 1.f, true);
+        smem_gemm<2, 4>(kBC, DK, kBC, dA, LCC, 1, Kt, LSK, 1, dQb, LSK, 1.f, true);
+        smem_gemm<2, 4>(DK, DV, kBC, Qb, 1, LSK, dO, LSV, 1, dS, LSV, 1.f, true);
+        __syncthreads();   // (the next two accumulate into dS and dK_til again)
+        smem_gemm<2, 4>(DK, DV, kBC, Kb, 1, LSK, dX, LSV, 1, dS, LSV, -1.f, true);
+        smem_gemm<2, 4>(kBC, DK, kBC, dA, 1, LCC, Qb, LSK, 1, dKt, LSK, 1.f, true);
+        __syncthreads();
+        // per-token gradients of the inputs; dS becomes the gradient of the chunk start
+        for (int e = tid; e < kBC * DV; e += kMNT) {
+            const int t = e / DV, j = e % DV;
+            if (t < nv) P.dv[row(t0 + t) * DV + j] = dX[t * LSV + j];
+        }
+        if (tid < DK) {
+            const int i = tid;
+            float dG = eS[i];            // d/dG_t, accumulated from the last token backwards
+            float g = 2.0f * gref[i];    // G_t, the cumulative log-decay, at the last token
+            for (int t = nv - 1; t >= 0; --t) {
+                const size_t gi = row(t0 + t) * DK + i;
+                const float kb = Kb[t * LSK + i], qb = Qb[t * LSK + i], kt = Kt[t * LSK + i];
+                const float dkb = dKb[t * LSK + i], dqb = dQb[t * LSK + i], dkt = dKt[t * LSK + i];
+                // K_bar = k f, Q_bar = q f, K_til = kappa / f with f = exp(G_t - G_ref)
+                const float f = expf(g - gref[i]);
+                P.dk[gi] = dkb * f;
+                P.dq[gi] = dqb * f;
+                P.dkappa[gi] = dkt / f;
+                dG += dkb * kb + dqb * qb - dkt * kt;
+                P.dla[gi] = dG;   // d log_alpha_t = sum over tokens u >= t of dG_u
+                g -= P.la[gi];
+            }
+        }
+        for (int e = tid; e < DK * DV; e += kMNT) {
+            const int i = e / DV, j = e % DV;
+            dS[i * LSV + j] *= gin[i];
+        }
+        __syncthreads();
+    }
+    for (int e = tid; e < DK * DV; e += kMNT) {
+        const int i = e / DV, j = e % DV;
+        P.dS0[(size_t)bh * sdd + i * DV + j] = dS[i * LSV + j];
+    }
+}
+
+// ---------------------------------------------------------------- gain adjoint
+struct GainArgs {
+    int variant;                       // 0 diagonal, 1 isotropic
+    const void* k;
+    const float *la, *om, *r, *p0, *dp_T, *dkappa;
+    float *pck;                        // [B*H][nblk][nu] variance at every kPB-token block start
+    float *dk, *dla, *dom, *dr, *dp0;
+    int T, H, DK;
+    float mu;
+};
+
+// Sum of x over the block's DK threads (warp shuffles, then one value per warp).
+__device__ __forceinline__ float block_sum(float x, float* red, int nwarps) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    x = warp_sum(x);
+    __syncthreads();
+    if (lane == 0) red[warp] = x;
+    __syncthreads();
+    float s = 0.f;
+    for (int w = 0; w < nwarps; ++w) s += red[w];
+    return s;
+}
+
+template <typename TIO, int V>
+__global__ void gain_adjoint_kernel(const GainArgs P) {
+    constexpr bool ISO = V == 1;
+    __shared__ float red[4];
+    extern __shared__ float gsm[];   // per token of a block: p_prev, p_hat (diagonal: [kPB][DK]),
+                                     // den, and the isotropic a_bar, ||k||^2
+    const int DK = P.DK, T = P.T, H = P.H, bh = blockIdx.x, b = bh / H, h = bh % H;
+    const int i = threadIdx.x, nwarps = blockDim.x >> 5;
+    const bool act = i < DK;
+    const int nblk = (T + kPB - 1) / kPB, nu = ISO ? 1 : DK;
+    float* spp = gsm;                           // [kPB][DK] (isotropic: [kPB])
+    float* sph = spp + kPB * DK;                // [kPB][DK]
+    float* sden = sph + kPB * DK;               // [kPB]
+    float* sab = sden + kPB;                    // [kPB]
+    float* sk2 = sab + kPB;                     // [kPB]
+    const TIO* kp = static_cast<const TIO*>(P.k);
+    auto row = [&](int t) { return ((size_t)b * T + t) * H + h; };
+    float* pck = P.pck + (size_t)bh * nblk * nu;
+    const float mu = P.mu;
+
+    // one token forward: returns the posterior p after the token, keeps p_hat
+    float p = P.p0 ? (ISO ? P.p0[bh] : (act ? P.p0[(size_t)bh * DK + i] : 0.f)) : 1.f;
+    for (int t = 0; t < T; ++t) {
+        const size_t th = row(t);
+        if (t % kPB == 0 && (ISO ? i == 0 : act)) pck[(size_t)(t / kPB) * nu + (ISO ? 0 : i)] = p;
+        const float kv = act ? IO<TIO>::load(kp, th * DK + i) : 0.f;
+        const float a2 = act ? expf(2.f * P.la[th * DK + i]) : 0.f;
+        const float rr = P.r[th];
+        if (ISO) {
+            const float ab = block_sum(a2, red, nwarps) / DK;
+            const float k2 = block_sum(kv * kv, red, nwarps);
+            const float ph = ab * p + P.om[th];
+            const float u = mu * k2 / (DK * rr);
+            p = ph / (1.f + u * ph);
+        } else if (act) {
+            const float ph = a2 * p + P.om[th * DK + i];
+            const float u = mu * kv * kv / rr;
+            p = ph / (1.f + u * ph);
+        }
+    }
+    float dp = P.dp_T ? (ISO ? P.dp_T[bh] : (act ? P.dp_T[(size_t)bh * DK + i] : 0.f)) : 0.f;
+    for (int blk = nblk - 1; blk >= 0; --blk) {
+        const int t0 = blk * kPB, t1 = min(T, t0 + kPB);
+        __syncthreads();
+        // recompute the block forward, keeping what the adjoint needs
+        p = pck[(size_t)blk * nu + (ISO ? 0 : (act ? i : 0))];
+        for (int t = t0; t < t1; ++t) {
+            const size_t th = row(t);
+            const int tl = t - t0;
+            const float kv = act ? IO<TIO>::load(kp, th * DK + i) : 0.f;
+            const float a2 = act ? expf(2.f * P.la[th * DK + i]) : 0.f;
+            const float rr = P.r[th];
+            if (ISO) {
+                const float ab = block_sum(a2, red, nwarps) / DK;
+                const float k2 = block_sum(kv * kv, red, nwarps);
+                const float ph = ab * p + P.om[th];
+                if (i == 0) {
+                    spp[tl] = p;
+                    sph[tl] = ph;
+                    sab[tl] = ab;
+                    sk2[tl] = k2;
+                    sden[tl] = rr + ph * k2;
+                }
+                p = ph / (1.f + mu * k2 / (DK * rr) * ph);
+            } else {
+                const float ph = act ? a2 * p + P.om[th * DK + i] : 0.f;
+                const float z = block_sum(ph * kv * kv, red, nwarps);
+                if (act) {
+                    spp[tl * DK + i] = p;
+                    sph[tl * DK + i] = ph;
+                    p = ph / (1.f + mu * kv * kv / rr * ph);
+                }
+                if (i == 0) sden[tl] = rr + z;
+            }
+        }
+        __syncthreads();
+        // adjoint, newest token first
+        for (int t = t1 - 1; t >= t0; --t) {
+            const size_t th = row(t);
+            const int tl = t - t0;
+            const float kv = act ? IO<TIO>::load(kp, th * DK + i) : 0.f;
+            const float a = act ? expf(P.la[th * DK + i]) : 0.f;
+            const float rr = P.r[th];
+            const float dkap = act ? P.dkappa[th * DK + i] : 0.f;
+            const float den = sden[tl];
+            if (ISO) {
+                const float ph = sph[tl], pp = spp[tl], ab = sab[tl], k2 = sk2[tl];
+                const float u = mu * k2 / (DK * rr), gq = 1.f + u * ph, beta = ph / den;
+                float dph = dp / (gq * gq);
+                const float du = -dp * ph * ph / (gq * gq);
+                const float dbeta = block_sum(dkap * kv, red, nwarps);
+                float gk = beta * dkap;
+                dph += dbeta / den;
+                const float dden = -dbeta * ph / (den * den);
+                float dr = dden;
+                dph += dden * k2;
+                float dk2 = dden * ph + du * mu / (DK * rr);
+                dr += -du * mu * k2 / (DK * rr * rr);
+                gk += 2.f * dk2 * kv;
+                dp = ab * dph;
+                const float dab = pp * dph;
+                if (act) {
+                    P.dk[th * DK + i] += gk;
+                    P.dla[th * DK + i] += dab * 2.f * a * a / DK;   // d log a = d a * a
+                }
+                if (i == 0) {
+                    P.dom[th] = dph;
+                    P.dr[th] = dr;
+                }
+            } else {
+                const float ph = act ? sph[tl * DK + i] : 0.f, pp = act ? spp[tl * DK + i] : 0.f;
+                const float u = act ? mu * kv * kv / rr : 0.f, gq = 1.f + u * ph;
+                float dph = dp / (gq * gq);
+                const float du = -dp * ph * ph / (gq * gq);
+                dph += dkap * kv / den;
+                float gk = dkap * ph / den;
+                const float s1 = block_sum(dkap * ph * kv, red, nwarps);
+                const float s2 = block_sum(-du * mu * kv * kv / (rr * rr), red, nwarps);
+                const float dden = -s1 / (den * den);
+                dph += dden * kv * kv;
+                gk += 2.f * dden * ph * kv + du * 2.f * mu * kv / rr;
+                dp = a * a * dph;
+                if (act) {
+                    P.dk[th * DK + i] += gk;
+                    P.dla[th * DK + i] += 2.f * a * pp * dph * a;
+                    P.dom[th * DK + i] = dph;
+                }
+                if (i == 0) P.dr[th] = dden + s2;
+            }
+        }
+    }
+    if (ISO) {
+        if (i == 0) P.dp0[bh] = dp;
+    } else if (act) {
+        P.dp0[(size_t)bh * DK + i] = dp;
+    }
+}
+
+}  // namespace
+
+size_t backward_mem_smem_bytes(int dk, int dv) { return mem_smem_floats(dk, dv) * sizeof(float); }
+
+cudaError_t launch_backward(const BackwardArgs& a, const BackwardWorkspace& w, cudaStream_t s) {
+    // gains kappa_t from the forward's gain scan
+    ForwardArgs f;
+    memset(&f, 0, sizeof(f));
+    f.variant = a.variant; f.B = a.B; f.T = a.T; f.H = a.H; f.dk = a.dk; f.dv = a.dv; f.chunk = kBC;
+    f.mu = a.mu; f.io = a.io; f.q = a.q; f.k = a.k; f.v = a.v; f.log_alpha = a.log_alpha;
+    f.omega = a.omega; f.r = a.r; f.S0 = a.S0; f.p0 = a.p0; f.p_T = w.p_scratch; f.status = a.status;
+    ScanWorkspace sw;
+    sw.kappa = w.kappa;
+    sw.summary = w.summary;
+    sw.carry = w.carry;
+    sw.chunk_g = kGainChunk;
+    sw.n_chunks_g = w.n_chunks_g;
+    cudaError_t e = launch_gain_scan(f, sw, s);
+    if (e != cudaSuccess) return e;
+
+    MemArgs m;
+    m.q = a.q; m.k = a.k; m.v = a.v; m.dO = a.dO;
+    m.la = a.log_alpha; m.kappa = w.kappa; m.S0 = a.S0; m.dS_T = a.dS_T;
+    m.ckpt = w.ckpt;
+    m.dq = a.dq; m.dk = a.dk_out; m.dv = a.dv_out; m.dla = a.dla; m.dkappa = w.dkappa; m.dS0 = a.dS0;
+    m.T = a.T; m.H = a.H; m.DK = a.dk; m.DV = a.dv; m.status = a.status;
+    const size_t smem = backward_mem_smem_bytes(a.dk, a.dv);
+    const int BH = a.B * a.H;
+    if (a.io == 1) {
+        e = cudaFuncSetAttribute(mem_adjoint_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        mem_adjoint_kernel<__nv_bfloat16><<<BH, kMNT, smem, s>>>(m);
+    } else {
+        e = cudaFuncSetAttribute(mem_adjoint_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        mem_adjoint_kernel<float><<<BH, kMNT, smem, s>>>(m);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    GainArgs g;
+    g.variant = a.variant; g.k = a.k; g.la = a.log_alpha; g.om = a.omega; g.r = a.r; g.p0 = a.p0;
+    g.dp_T = a.dp_T; g.dkappa = w.dkappa; g.pck = w.pck;
+    g.dk = a.dk_out; g.dla = a.dla; g.dom = a.domega; g.dr = a.dr; g.dp0 = a.dp0;
+    g.T = a.T; g.H = a.H; g.DK = a.dk; g.mu = a.mu;
+    const int nt = ((a.dk + 31) / 32) * 32;
+    const size_t gsm = sizeof(float) * (2 * kPB * a.dk + 3 * kPB);
+    auto launch_gain = [&](auto kernel) {
+        const cudaError_t e2 = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsm);
+        if (e2 != cudaSuccess) return e2;
+        kernel<<<BH, nt, gsm, s>>>(g);
+        return cudaGetLastError();
+    };
+    if (a.variant == 1)
+        return a.io == 1 ? launch_gain(gain_adjoint_kernel<__nv_bfloat16, 1>) : launch_gain(gain_adjoint_kernel<float, 1>);
+    return a.io == 1 ? launch_gain(gain_adjoint_kernel<__nv_bfloat16, 0>) : launch_gain(gain_adjoint_kernel<float, 0>);
+}
+
+int backward_chunk() { return kBC; }
+int backward_block() { return kPB; }
+
+}  // namespace kdn

@@ -102,4 +102,28 @@ cudaError_t launch_dense_forward(const DenseArgs& a, cudaStream_t s);
 // Copy the initial state to the outputs (T == 0).  chunk_simt.cu
 cudaError_t launch_state_copy(const ForwardArgs& a, cudaStream_t s);
 
+// Backward pass (gradients of sum(dO o) + sum(dS_T S_T) + sum(dp_T p_T)).  backward.cu
+struct BackwardArgs {
+    int variant, B, T, H, dk, dv, io;   // variant: 0 diagonal, 1 isotropic
+    float mu;
+    const void *q, *k, *v, *dO;
+    const float *log_alpha, *omega, *r, *S0, *p0, *dS_T, *dp_T;
+    float *dq, *dk_out, *dv_out, *dla, *domega, *dr, *dS0, *dp0;
+    uint32_t* status;
+};
+struct BackwardWorkspace {
+    float* kappa;      // [B,T,H,dk] gains from the gain scan
+    float* summary;    // gain-scan chunk summaries and carries
+    float* carry;
+    int n_chunks_g;
+    float* p_scratch;  // [B*H, nu] (the scan's final variances, unused)
+    float* ckpt;       // [B*H][ceil(T / chunk) + 1][dk][dv] states at memory-chunk starts
+    float* dkappa;     // [B,T,H,dk]
+    float* pck;        // [B*H][ceil(T / block)][nu] variances at gain-adjoint block starts
+};
+cudaError_t launch_backward(const BackwardArgs& a, const BackwardWorkspace& w, cudaStream_t s);
+size_t backward_mem_smem_bytes(int dk, int dv);
+int backward_chunk();   // tokens per memory-adjoint chunk
+int backward_block();   // tokens per gain-adjoint checkpoint block
+
 }  // namespace kdn
