@@ -310,6 +310,22 @@ def e2e_pipelined(torch, device, hx, outs, ws, fwd, steps, warmup, barrier):
     return e0.elapsed_time(e1) / steps
 
 
+def backward_upstream(torch, w, device):
+    """Upstream gradient dO of the backward workload (N(0,1), the io dtype)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed + 1)
+    iot = torch.bfloat16 if w.io == "bf16" else torch.float32
+    return torch.randn(w.B, w.T, w.H, w.d, device=device, generator=g).to(iot)
+
+
+def backward_algorithmic_flops(B, T, H, dk, dv):
+    """Flops of the backward per call: 16 d_k d_v per token-head, the eight d_k x d_v
+    products of the chunk-form adjoint (the state recomputation K_bar S_m and
+    K_til^T Delta; dDelta = K_til Gp, dK_til = Delta Gp^T, dQ_bar = dO S_m^T,
+    dK_bar = -dX S_m^T, dS_m = Q_bar^T dO - K_bar^T dX), lower-order terms left out."""
+    return 16 * dk * dv * B * T * H
+
+
 def dense_algorithmic_flops(B, T, H, d):
     """Flops of the dense filter per call: 13 d^2 per token-head (D P D: 2 d^2,
     P_hat k: 2 d^2, P_hat - kappa u^T: 2 d^2, D S: d^2, S_hat^T k: 2 d^2,
@@ -445,6 +461,17 @@ def main():
                   file=sys.stderr)
             return 2
         return profile_decode(torch, kdn, w, device, args.steps, args.warmup)
+    if w.variant == "backward":
+        if not args.profile:
+            print("the backward workload is timed inside the default run (see 'workloads'); use --profile",
+                  file=sys.stderr)
+            return 2
+        x = device_inputs(torch, w, "diag", w.seed, device)
+        dO = backward_upstream(torch, w, device)
+        time_calls(torch, lambda: kdn.kdn_backward("diag", x["q"], x["k"], x["v"], x["log_alpha"], x["omega"],
+                                                   x["r"], dO=dO), args.steps, args.warmup, barrier)
+        print(json.dumps({"profile": w.name, "kernels_per_step": 5}), flush=True)
+        return 0
     if w.variant == "dense":
         if not args.profile:
             print("the dense workload is timed inside the default run (see 'workloads'); use --profile",
@@ -624,6 +651,26 @@ def other_workloads(torch, kdn, WORKLOADS, device, barrier, peaks):
                    "peak_tflops": peak, "alu_frac": flops / (ms / 1e3) / 1e12 / peak,
                    "peak_source": "SM count x 128 fp32 lanes x 2 flop x 2070 MHz (maximum SM clock)"}
     del x
+    # backward pass of the diagonal forward on the headline shape (fp32 CUDA cores)
+    w = WORKLOADS["backward-diag-bf16-b8h16t4096d128"]
+    x = device_inputs(torch, w, "diag", w.seed, device)
+    dO = backward_upstream(torch, w, device)
+    ws = torch.empty(kdn.library().kdn_backward_workspace_size(0, w.B, w.T, w.H, w.d, w.d, 1), dtype=torch.uint8,
+                     device=device)
+    bw = lambda: kdn.kdn_backward("diag", x["q"], x["k"], x["v"], x["log_alpha"], x["omega"], x["r"], dO=dO,
+                                  workspace=ws)
+    ms = time_calls(torch, bw, 3, 1, barrier)
+    g = bw()
+    finite = all(bool(torch.isfinite(t).all().item()) for t in g.values())
+    flops = backward_algorithmic_flops(w.B, w.T, w.H, w.d, w.d)
+    peak = dense_alu_peak_tflops(torch, device)
+    out[w.name] = {"tokens_per_s": w.B * w.T / (ms / 1e3), "ms": ms,
+                   "kernels": "gain scan (3) + mem_adjoint_kernel + gain_adjoint_kernel",
+                   "bound": "alu", "algorithmic_flops": flops, "achieved_tflops": flops / (ms / 1e3) / 1e12,
+                   "peak_tflops": peak, "alu_frac": flops / (ms / 1e3) / 1e12 / peak,
+                   "outputs_finite": finite, "device_status": kdn.kdn_read_device_status(ws),
+                   "peak_source": "SM count x 128 fp32 lanes x 2 flop x 2070 MHz (maximum SM clock)"}
+    del x, dO, ws, g
     # decode: 512-token prefill through the forward path, then 1024 single-token steps
     w = WORKLOADS["diag-decode-f32-s256h16d128"]
     pre = device_inputs(torch, w, "diag", w.seed, device, T=w.prefill)

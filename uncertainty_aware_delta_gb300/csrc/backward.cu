@@ -42,6 +42,8 @@ namespace {
 constexpr int kBC = 16;       // tokens per chunk of the memory adjoint
 constexpr int kMNT = 256;     // threads of the memory adjoint
 constexpr int kPB = 64;       // tokens per checkpoint block of the gain adjoint
+constexpr int kEl = kBC * 128 / kMNT;        // elements of a [kBC][d] tile per thread (d <= 128)
+constexpr int kS4 = 128 * 128 / 4 / kMNT;    // 16-byte groups of a [dk][dv] state per thread
 
 // C(r, c) (+)= alpha sum_k A(r, k) B(k, c) on shared-memory operands with arbitrary
 // strides: A(r, k) = A[r ar + k ak], B(k, c) = B[k bk + c bc], C(r, c) = C[r cr + c].
@@ -97,7 +99,7 @@ struct MemArgs {
 
 size_t mem_smem_floats(int DK, int DV) {
     const int LSK = DK + 1, LSV = DV + 1, LCC = kBC + 1;
-    return (size_t)2 * DK * LSV + 6 * kBC * LSK + 3 * kBC * LSV + 4 * kBC * LCC + 4 * DK;
+    return (size_t)2 * DK * LSV + 7 * kBC * LSK + 3 * kBC * LSV + 4 * kBC * LCC + 4 * DK;
 }
 
 template <typename TIO>
@@ -112,7 +114,8 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
     float* dKb = Kt + kBC * LSK;
     float* dQb = dKb + kBC * LSK;
     float* dKt = dQb + kBC * LSK;
-    float* X = dKt + kBC * LSK;        // [kBC][LSV] V - K_bar S_m, then Delta
+    float* Gc = dKt + kBC * LSK;       // [kBC][LSK] cumulative log-decay G_t within the chunk
+    float* X = Gc + kBC * LSK;         // [kBC][LSV] V - K_bar S_m, then Delta
     float* dO = X + kBC * LSV;         // [kBC][LSV]
     float* dX = dO + kBC * LSV;        // [kBC][LSV] dDelta, then the adjoint of X
     float* L = dX + kBC * LSV;         // [kBC][LCC]
@@ -130,15 +133,37 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
     float* ck = P.ckpt + (size_t)bh * (nch + 1) * sdd;
     auto row = [&](int t) { return ((size_t)b * T + t) * H + h; };   // token-head index
 
-    // per-chunk setup: cumulative log-decay (in Kt, read as G), reference and factors;
-    // the operands K_bar, Q_bar, K_til; S_m = diag(g_in) S_0 with S_0 in Sm
+    // per-chunk setup: cumulative log-decay G, reference and factors; the operands
+    // K_bar, Q_bar, K_til; S_m = diag(g_in) S_0 with S_0 in Sm.  The chunk's inputs are
+    // read into registers by one batch of loads per thread before any of them is used.
     auto setup = [&](int n, int nv) {
         const int t0 = n * kBC;
+        float rla[kEl], rk[kEl], rq[kEl], rkap[kEl], rv[kEl];
+#pragma unroll
+        for (int m = 0; m < kEl; ++m) {
+            const int e = tid + m * kMNT, t = e / DK, i = e % DK;
+            const bool ok = e < kBC * DK && t < nv;
+            const size_t gi = row(t0 + min(t, kBC - 1)) * DK + i;
+            rla[m] = ok ? P.la[gi] : 0.f;
+            rk[m] = ok ? IO<TIO>::load(static_cast<const TIO*>(P.k), gi) : 0.f;
+            rq[m] = ok ? IO<TIO>::load(static_cast<const TIO*>(P.q), gi) : 0.f;
+            rkap[m] = ok ? P.kappa[gi] : 0.f;
+            const int tv = e / DV, j = e % DV;
+            const bool okv = e < kBC * DV && tv < nv;
+            rv[m] = okv ? IO<TIO>::load(static_cast<const TIO*>(P.v), row(t0 + min(tv, kBC - 1)) * DV + j) : 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < kEl; ++m) {
+            const int e = tid + m * kMNT;
+            if (e < kBC * DK) Gc[(e / DK) * LSK + e % DK] = rla[m];
+            if (e < kBC * DV) X[(e / DV) * LSV + e % DV] = rv[m];
+        }
+        __syncthreads();
         if (tid < DK) {
             float g = 0.f;
             for (int t = 0; t < kBC; ++t) {
-                if (t < nv) g += P.la[row(t0 + t) * DK + tid];
-                Kt[t * LSK + tid] = g;
+                g += Gc[t * LSK + tid];
+                Gc[t * LSK + tid] = g;
             }
             const float gr = 0.5f * g;
             gref[tid] = gr;
@@ -147,28 +172,19 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
             if (!(fabsf(g) <= kMaxChunkLogDecay)) set_status(P.status, kStatusRange);
         }
         __syncthreads();
-        for (int e = tid; e < kBC * DK; e += kMNT) {
-            const int t = e / DK, i = e % DK;
-            if (t < nv) {
-                const size_t gi = row(t0 + t) * DK + i;
-                const float g = Kt[t * LSK + i];
-                const float ef = expf(g - gref[i]);
-                Kb[t * LSK + i] = IO<TIO>::load(static_cast<const TIO*>(P.k), gi) * ef;
-                Qb[t * LSK + i] = IO<TIO>::load(static_cast<const TIO*>(P.q), gi) * ef;
-                Kt[t * LSK + i] = P.kappa[gi] / ef;
-            } else {
-                Kb[t * LSK + i] = 0.f;
-                Qb[t * LSK + i] = 0.f;
-                Kt[t * LSK + i] = 0.f;
+#pragma unroll
+        for (int m = 0; m < kEl; ++m) {
+            const int e = tid + m * kMNT, t = e / DK, i = e % DK;
+            if (e < kBC * DK) {
+                const float ef = expf(Gc[t * LSK + i] - gref[i]);
+                Kb[t * LSK + i] = rk[m] * ef;
+                Qb[t * LSK + i] = rq[m] * ef;
+                Kt[t * LSK + i] = rkap[m] / ef;
             }
         }
         for (int e = tid; e < DK * DV; e += kMNT) {
             const int i = e / DV, j = e % DV;
             Sm[i * LSV + j] *= gin[i];
-        }
-        for (int e = tid; e < kBC * DV; e += kMNT) {
-            const int t = e / DV, j = e % DV;
-            X[t * LSV + j] = t < nv ? IO<TIO>::load(static_cast<const TIO*>(P.v), row(t0 + t) * DV + j) : 0.f;
         }
         __syncthreads();
         // L = strict_lower(K_bar K_til^T), A = lower_incl(Q_bar K_til^T), X = V - K_bar S_m
@@ -182,14 +198,38 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
             if (s > t) Am[t * LCC + s] = 0.f;
         }
         __syncthreads();
-        // forward substitution (I + L) Delta = X (one row at a time, a thread per column)
-        for (int t = 1; t < nv; ++t) {
-            for (int j = tid; j < DV; j += kMNT) {
+        // forward substitution (I + L) Delta = X: a thread per value column, which it
+        // alone reads and writes (no barrier between rows)
+        for (int j = tid; j < DV; j += kMNT) {
+            for (int t = 1; t < nv; ++t) {
                 float acc = X[t * LSV + j];
                 for (int s = 0; s < t; ++s) acc = fmaf(-L[t * LCC + s], X[s * LSV + j], acc);
                 X[t * LSV + j] = acc;
             }
-            __syncthreads();
+        }
+        __syncthreads();
+    };
+    // a checkpointed state into Sm: one batch of 16-byte loads per thread, then the
+    // shared-memory stores
+    auto load_state = [&](const float* src) {
+        const float4* s4 = reinterpret_cast<const float4*>(src);
+        const int n4 = DK * DV / 4;
+        float4 r4[kS4];
+#pragma unroll
+        for (int m = 0; m < kS4; ++m) {
+            const int e4 = tid + m * kMNT;
+            r4[m] = e4 < n4 ? s4[e4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int m = 0; m < kS4; ++m) {
+            const int e4 = tid + m * kMNT;
+            if (e4 < n4) {
+                float* d = Sm + ((4 * e4) / DV) * LSV + (4 * e4) % DV;
+                d[0] = r4[m].x;
+                d[1] = r4[m].y;
+                d[2] = r4[m].z;
+                d[3] = r4[m].w;
+            }
         }
     };
 
@@ -216,27 +256,39 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
     __syncthreads();
 
     // ---- reverse sweep
+    // eS_i = sum_j dS_out(i, j) S_out(i, j) for the chunk about to be processed; for the
+    // last chunk from S_T (still in Sm) and dS_T, then at the end of every chunk from its
+    // S_m and dS_m (the factors g_in of S_out = diag(g_in)^-1 S_m and dS_out =
+    // diag(g_in) dS_m cancel)
     for (int e = tid; e < DK * DV; e += kMNT) {
         const int i = e / DV, j = e % DV;
         dS[i * LSV + j] = P.dS_T ? P.dS_T[(size_t)bh * sdd + i * DV + j] : 0.f;
     }
+    __syncthreads();
+    for (int ri = tid >> 5; ri < DK; ri += kMNT / 32) {
+        float acc = 0.f;
+        for (int j = tid & 31; j < DV; j += 32) acc = fmaf(dS[ri * LSV + j], Sm[ri * LSV + j], acc);
+        acc = warp_sum(acc);
+        if ((tid & 31) == 0) eS[ri] = acc;
+    }
     for (int n = nch - 1; n >= 0; --n) {
         const int t0 = n * kBC, nv = min(kBC, T - t0);
-        for (int e = tid; e < DK * DV; e += kMNT) Sm[(e / DV) * LSV + e % DV] = ck[(size_t)n * sdd + e];
+        __syncthreads();
+        load_state(ck + (size_t)n * sdd);
+        float rdo[kEl];
+#pragma unroll
+        for (int m = 0; m < kEl; ++m) {
+            const int e = tid + m * kMNT, t = e / DV, j = e % DV;
+            const bool ok = P.dO && e < kBC * DV && t < nv;
+            rdo[m] = ok ? IO<TIO>::load(static_cast<const TIO*>(P.dO), row(t0 + min(t, kBC - 1)) * DV + j) : 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < kEl; ++m) {
+            const int e = tid + m * kMNT;
+            if (e < kBC * DV) dO[(e / DV) * LSV + e % DV] = rdo[m];
+        }
         __syncthreads();
         setup(n, nv);   // Sm = S_m, X = Delta, operands, L, A
-        // dG at the chunk's last token from S_out = diag(g_out)(...): sum_j dS_out S_out
-        if (tid < DK) {
-            float acc = 0.f;
-            const float* so = ck + (size_t)(n + 1) * sdd + (size_t)tid * DV;
-            for (int j = 0; j < DV; ++j) acc = fmaf(dS[tid * LSV + j], so[j], acc);
-            eS[tid] = acc;
-        }
-        for (int e = tid; e < kBC * DV; e += kMNT) {
-            const int t = e / DV, j = e % DV;
-            dO[t * LSV + j] = (t < nv && P.dO) ? IO<TIO>::load(static_cast<const TIO*>(P.dO), row(t0 + t) * DV + j) : 0.f;
-        }
-        __syncthreads();
         for (int e = tid; e < DK * DV; e += kMNT) {   // Gp = diag(g_out) dS_out
             const int i = e / DV, j = e % DV;
             dS[i * LSV + j] *= gout[i];
@@ -254,15 +306,15 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
             if (s > t) dA[t * LCC + s] = 0.f;
         }
         __syncthreads();
-        // back substitution (I + L)^T dX = dDelta
-        for (int t = nv - 2; t >= 0; --t) {
-            for (int j = tid; j < DV; j += kMNT) {
+        // back substitution (I + L)^T dX = dDelta (a thread per value column)
+        for (int j = tid; j < DV; j += kMNT) {
+            for (int t = nv - 2; t >= 0; --t) {
                 float acc = dX[t * LSV + j];
                 for (int s = t + 1; s < nv; ++s) acc = fmaf(-L[s * LCC + t], dX[s * LSV + j], acc);
                 dX[t * LSV + j] = acc;
             }
-            __syncthreads();
         }
+        __syncthreads();
         // dL = strict_lower(-dX Delta^T); dK_bar = -dX S_m^T
         smem_gemm<1, 1>(kBC, kBC, DV, dX, LSV, 1, X, 1, LSV, dL, LCC, -1.f, false);
         smem_gemm<2, 4>(kBC, DK, DV, dX, LSV, 1, Sm, 1, LSV, dKb, LSK, -1.f, false);
@@ -290,27 +342,35 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
         if (tid < DK) {
             const int i = tid;
             float dG = eS[i];            // d/dG_t, accumulated from the last token backwards
-            float g = 2.0f * gref[i];    // G_t, the cumulative log-decay, at the last token
             for (int t = nv - 1; t >= 0; --t) {
                 const size_t gi = row(t0 + t) * DK + i;
                 const float kb = Kb[t * LSK + i], qb = Qb[t * LSK + i], kt = Kt[t * LSK + i];
                 const float dkb = dKb[t * LSK + i], dqb = dQb[t * LSK + i], dkt = dKt[t * LSK + i];
                 // K_bar = k f, Q_bar = q f, K_til = kappa / f with f = exp(G_t - G_ref)
-                const float f = expf(g - gref[i]);
+                const float f = expf(Gc[t * LSK + i] - gref[i]);
                 P.dk[gi] = dkb * f;
                 P.dq[gi] = dqb * f;
                 P.dkappa[gi] = dkt / f;
                 dG += dkb * kb + dqb * qb - dkt * kt;
                 P.dla[gi] = dG;   // d log_alpha_t = sum over tokens u >= t of dG_u
-                g -= P.la[gi];
             }
         }
-        for (int e = tid; e < DK * DV; e += kMNT) {
-            const int i = e / DV, j = e % DV;
-            dS[i * LSV + j] *= gin[i];
+        __syncthreads();   // (the loop above reads eS)
+        // eS of the previous chunk; dS becomes the gradient of the chunk start (a warp
+        // per state row)
+        for (int ri = tid >> 5; ri < DK; ri += kMNT / 32) {
+            float acc = 0.f;
+            const float gi = gin[ri];
+            for (int j = tid & 31; j < DV; j += 32) {
+                const float d = dS[ri * LSV + j];
+                acc = fmaf(d, Sm[ri * LSV + j], acc);
+                dS[ri * LSV + j] = d * gi;
+            }
+            acc = warp_sum(acc);
+            if ((tid & 31) == 0) eS[ri] = acc;
         }
-        __syncthreads();
     }
+    __syncthreads();
     for (int e = tid; e < DK * DV; e += kMNT) {
         const int i = e / DV, j = e % DV;
         P.dS0[(size_t)bh * sdd + i * DV + j] = dS[i * LSV + j];
@@ -328,146 +388,202 @@ struct GainArgs {
     float mu;
 };
 
-// Sum of x over the block's DK threads (warp shuffles, then one value per warp).
-__device__ __forceinline__ float block_sum(float x, float* red, int nwarps) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    x = warp_sum(x);
-    __syncthreads();
-    if (lane == 0) red[warp] = x;
-    __syncthreads();
-    float s = 0.f;
-    for (int w = 0; w < nwarps; ++w) s += red[w];
-    return s;
-}
-
 template <typename TIO, int V>
 __global__ void gain_adjoint_kernel(const GainArgs P) {
     constexpr bool ISO = V == 1;
-    __shared__ float red[4];
-    extern __shared__ float gsm[];   // per token of a block: p_prev, p_hat (diagonal: [kPB][DK]),
-                                     // den, and the isotropic a_bar, ||k||^2
+    // per token of a block: p_prev, p_hat ([kPB][DK]; isotropic [kPB]), den, the
+    // isotropic a_bar, ||k||^2, and the token sums s1 (diagonal: sum dkappa p_hat k;
+    // isotropic: sum dkappa k); the block's inputs staged by coalesced loads: k,
+    // log_alpha (reused for d/du of each channel), dkappa ([kPB][DK]), omega
+    // ([kPB][DK]; isotropic [kPB]) and r [kPB].  Every cross-channel sum is taken for
+    // the whole block at once (none of them feeds the serial recurrence).
+    extern __shared__ float gsm[];
     const int DK = P.DK, T = P.T, H = P.H, bh = blockIdx.x, b = bh / H, h = bh % H;
-    const int i = threadIdx.x, nwarps = blockDim.x >> 5;
+    const int i = threadIdx.x, lane = i & 31, warp = i >> 5, nwarps = blockDim.x >> 5, nth = blockDim.x;
     const bool act = i < DK;
     const int nblk = (T + kPB - 1) / kPB, nu = ISO ? 1 : DK;
     float* spp = gsm;                           // [kPB][DK] (isotropic: [kPB])
-    float* sph = spp + kPB * DK;                // [kPB][DK]
+    float* sph = spp + kPB * DK;                // [kPB][DK] (isotropic: [kPB])
     float* sden = sph + kPB * DK;               // [kPB]
     float* sab = sden + kPB;                    // [kPB]
     float* sk2 = sab + kPB;                     // [kPB]
+    float* ss1 = sk2 + kPB;                     // [kPB]
+    float* xk = ss1 + kPB;                      // [kPB][DK]
+    float* xla = xk + kPB * DK;                 // [kPB][DK]
+    float* xdk = xla + kPB * DK;                // [kPB][DK]
+    float* xom = xdk + kPB * DK;                // [kPB][nu]
+    float* xr = xom + kPB * nu;                 // [kPB]
     const TIO* kp = static_cast<const TIO*>(P.k);
     auto row = [&](int t) { return ((size_t)b * T + t) * H + h; };
     float* pck = P.pck + (size_t)bh * nblk * nu;
     const float mu = P.mu;
+    // (eight elements per thread per round: the loads of a round are all in flight together)
+    auto stage = [&](int t0, int nt, bool with_dkappa) {
+        __syncthreads();
+        for (int e0 = i; e0 < nt * DK; e0 += 8 * nth) {
+            float rk[8], rla[8], rom[8], rdk[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int e = e0 + m * nth;
+                const bool ok = e < nt * DK;
+                const size_t g = row(t0 + (ok ? e / DK : 0)) * DK + e % DK;
+                rk[m] = ok ? IO<TIO>::load(kp, g) : 0.f;
+                rla[m] = ok ? P.la[g] : 0.f;
+                rom[m] = (ok && !ISO) ? P.om[g] : 0.f;
+                rdk[m] = (ok && with_dkappa) ? P.dkappa[g] : 0.f;
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int e = e0 + m * nth;
+                if (e < nt * DK) {
+                    xk[e] = rk[m];
+                    xla[e] = rla[m];
+                    if (!ISO) xom[e] = rom[m];
+                    if (with_dkappa) xdk[e] = rdk[m];
+                }
+            }
+        }
+        for (int e = i; e < nt; e += nth) {
+            xr[e] = P.r[row(t0 + e)];
+            if (ISO) xom[e] = P.om[row(t0 + e)];
+        }
+        __syncthreads();
+    };
+    // out[t] = sum over channels c of f(t, c), for every token of the block (a warp per token)
+    auto token_sums = [&](int nt, auto f, float* out) {
+        __syncthreads();
+        for (int t = warp; t < nt; t += nwarps) {
+            float acc = 0.f;
+            for (int c = lane; c < DK; c += 32) acc += f(t, c);
+            acc = warp_sum(acc);
+            if (lane == 0) out[t] = acc;
+        }
+        __syncthreads();
+    };
+    auto iso_stats = [&](int nt) {   // a_bar_t = mean exp(2 log_alpha), ||k_t||^2
+        token_sums(nt, [&](int t, int c) { return expf(2.f * xla[t * DK + c]); }, sab);
+        token_sums(nt, [&](int t, int c) { return xk[t * DK + c] * xk[t * DK + c]; }, sk2);
+    };
 
-    // one token forward: returns the posterior p after the token, keeps p_hat
+    // forward over the sequence: the variance at every block start
     float p = P.p0 ? (ISO ? P.p0[bh] : (act ? P.p0[(size_t)bh * DK + i] : 0.f)) : 1.f;
-    for (int t = 0; t < T; ++t) {
-        const size_t th = row(t);
-        if (t % kPB == 0 && (ISO ? i == 0 : act)) pck[(size_t)(t / kPB) * nu + (ISO ? 0 : i)] = p;
-        const float kv = act ? IO<TIO>::load(kp, th * DK + i) : 0.f;
-        const float a2 = act ? expf(2.f * P.la[th * DK + i]) : 0.f;
-        const float rr = P.r[th];
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int t0 = blk * kPB, nt = min(kPB, T - t0);
+        if (ISO ? i == 0 : act) pck[(size_t)blk * nu + (ISO ? 0 : i)] = p;
+        stage(t0, nt, false);
         if (ISO) {
-            const float ab = block_sum(a2, red, nwarps) / DK;
-            const float k2 = block_sum(kv * kv, red, nwarps);
-            const float ph = ab * p + P.om[th];
-            const float u = mu * k2 / (DK * rr);
-            p = ph / (1.f + u * ph);
+            iso_stats(nt);
+            for (int tl = 0; tl < nt; ++tl) {   // (every thread runs the scalar recurrence)
+                const float ph = sab[tl] / DK * p + xom[tl];
+                p = ph / (1.f + mu * sk2[tl] / (DK * xr[tl]) * ph);
+            }
         } else if (act) {
-            const float ph = a2 * p + P.om[th * DK + i];
-            const float u = mu * kv * kv / rr;
-            p = ph / (1.f + u * ph);
+            for (int tl = 0; tl < nt; ++tl) {
+                const float kv = xk[tl * DK + i];
+                const float ph = expf(2.f * xla[tl * DK + i]) * p + xom[tl * DK + i];
+                p = ph / (1.f + mu * kv * kv / xr[tl] * ph);
+            }
         }
     }
     float dp = P.dp_T ? (ISO ? P.dp_T[bh] : (act ? P.dp_T[(size_t)bh * DK + i] : 0.f)) : 0.f;
     for (int blk = nblk - 1; blk >= 0; --blk) {
-        const int t0 = blk * kPB, t1 = min(T, t0 + kPB);
-        __syncthreads();
-        // recompute the block forward, keeping what the adjoint needs
+        const int t0 = blk * kPB, nt = min(kPB, T - t0);
+        stage(t0, nt, true);
+        // recompute the block forward, keeping p_prev and p_hat; then den and s1
         p = pck[(size_t)blk * nu + (ISO ? 0 : (act ? i : 0))];
-        for (int t = t0; t < t1; ++t) {
-            const size_t th = row(t);
-            const int tl = t - t0;
-            const float kv = act ? IO<TIO>::load(kp, th * DK + i) : 0.f;
-            const float a2 = act ? expf(2.f * P.la[th * DK + i]) : 0.f;
-            const float rr = P.r[th];
-            if (ISO) {
-                const float ab = block_sum(a2, red, nwarps) / DK;
-                const float k2 = block_sum(kv * kv, red, nwarps);
-                const float ph = ab * p + P.om[th];
-                if (i == 0) {
+        if (ISO) {
+            iso_stats(nt);
+            if (i == 0) {
+                for (int tl = 0; tl < nt; ++tl) {
+                    const float ph = sab[tl] / DK * p + xom[tl];
                     spp[tl] = p;
                     sph[tl] = ph;
-                    sab[tl] = ab;
-                    sk2[tl] = k2;
-                    sden[tl] = rr + ph * k2;
+                    sden[tl] = xr[tl] + ph * sk2[tl];
+                    p = ph / (1.f + mu * sk2[tl] / (DK * xr[tl]) * ph);
                 }
-                p = ph / (1.f + mu * k2 / (DK * rr) * ph);
-            } else {
-                const float ph = act ? a2 * p + P.om[th * DK + i] : 0.f;
-                const float z = block_sum(ph * kv * kv, red, nwarps);
-                if (act) {
+            }
+            token_sums(nt, [&](int t, int c) { return xdk[t * DK + c] * xk[t * DK + c]; }, ss1);
+        } else {
+            if (act) {
+                for (int tl = 0; tl < nt; ++tl) {
+                    const float kv = xk[tl * DK + i];
+                    const float ph = expf(2.f * xla[tl * DK + i]) * p + xom[tl * DK + i];
                     spp[tl * DK + i] = p;
                     sph[tl * DK + i] = ph;
-                    p = ph / (1.f + mu * kv * kv / rr * ph);
+                    p = ph / (1.f + mu * kv * kv / xr[tl] * ph);
                 }
-                if (i == 0) sden[tl] = rr + z;
             }
+            token_sums(nt, [&](int t, int c) { return sph[t * DK + c] * xk[t * DK + c] * xk[t * DK + c]; }, sden);
+            token_sums(nt, [&](int t, int c) { return xdk[t * DK + c] * sph[t * DK + c] * xk[t * DK + c]; }, ss1);
+            for (int t = i; t < nt; t += nth) sden[t] += xr[t];
+            __syncthreads();
         }
-        __syncthreads();
-        // adjoint, newest token first
-        for (int t = t1 - 1; t >= t0; --t) {
-            const size_t th = row(t);
-            const int tl = t - t0;
-            const float kv = act ? IO<TIO>::load(kp, th * DK + i) : 0.f;
-            const float a = act ? expf(P.la[th * DK + i]) : 0.f;
-            const float rr = P.r[th];
-            const float dkap = act ? P.dkappa[th * DK + i] : 0.f;
-            const float den = sden[tl];
+        // adjoint, newest token first (no cross-channel sums inside)
+        for (int tl = nt - 1; tl >= 0; --tl) {
+            const size_t th = row(t0 + tl);
+            const float rr = xr[tl], den = sden[tl];
             if (ISO) {
-                const float ph = sph[tl], pp = spp[tl], ab = sab[tl], k2 = sk2[tl];
+                const float ph = sph[tl], pp = spp[tl], ab = sab[tl] / DK, k2 = sk2[tl];
                 const float u = mu * k2 / (DK * rr), gq = 1.f + u * ph, beta = ph / den;
                 float dph = dp / (gq * gq);
                 const float du = -dp * ph * ph / (gq * gq);
-                const float dbeta = block_sum(dkap * kv, red, nwarps);
-                float gk = beta * dkap;
+                const float dbeta = ss1[tl];
                 dph += dbeta / den;
                 const float dden = -dbeta * ph / (den * den);
-                float dr = dden;
                 dph += dden * k2;
-                float dk2 = dden * ph + du * mu / (DK * rr);
-                dr += -du * mu * k2 / (DK * rr * rr);
-                gk += 2.f * dk2 * kv;
+                const float dk2 = dden * ph + du * mu / (DK * rr);
                 dp = ab * dph;
-                const float dab = pp * dph;
                 if (act) {
-                    P.dk[th * DK + i] += gk;
-                    P.dla[th * DK + i] += dab * 2.f * a * a / DK;   // d log a = d a * a
+                    const float kv = xk[tl * DK + i], a = expf(xla[tl * DK + i]);
+                    xdk[tl * DK + i] = beta * xdk[tl * DK + i] + 2.f * dk2 * kv;
+                    xla[tl * DK + i] = pp * dph * 2.f * a * a / DK;   // d log a = d a * a
                 }
                 if (i == 0) {
                     P.dom[th] = dph;
-                    P.dr[th] = dr;
+                    P.dr[th] = dden - du * mu * k2 / (DK * rr * rr);
                 }
-            } else {
-                const float ph = act ? sph[tl * DK + i] : 0.f, pp = act ? spp[tl * DK + i] : 0.f;
-                const float u = act ? mu * kv * kv / rr : 0.f, gq = 1.f + u * ph;
+            } else if (act) {
+                const float kv = xk[tl * DK + i], a = expf(xla[tl * DK + i]), dkap = xdk[tl * DK + i];
+                const float ph = sph[tl * DK + i], pp = spp[tl * DK + i];
+                const float u = mu * kv * kv / rr, gq = 1.f + u * ph;
                 float dph = dp / (gq * gq);
                 const float du = -dp * ph * ph / (gq * gq);
-                dph += dkap * kv / den;
-                float gk = dkap * ph / den;
-                const float s1 = block_sum(dkap * ph * kv, red, nwarps);
-                const float s2 = block_sum(-du * mu * kv * kv / (rr * rr), red, nwarps);
-                const float dden = -s1 / (den * den);
-                dph += dden * kv * kv;
-                gk += 2.f * dden * ph * kv + du * 2.f * mu * kv / rr;
+                const float dden = -ss1[tl] / (den * den);
+                dph += dkap * kv / den + dden * kv * kv;
+                const float gk = dkap * ph / den + 2.f * dden * ph * kv + du * 2.f * mu * kv / rr;
                 dp = a * a * dph;
-                if (act) {
-                    P.dk[th * DK + i] += gk;
-                    P.dla[th * DK + i] += 2.f * a * pp * dph * a;
-                    P.dom[th * DK + i] = dph;
+                xdk[tl * DK + i] = gk;                   // (this token's inputs are no longer
+                spp[tl * DK + i] = 2.f * a * pp * dph * a;   //  needed: the buffers take its
+                xla[tl * DK + i] = du;                   //  gradients)
+                P.dom[th * DK + i] = dph;
+            }
+        }
+        if (!ISO) {   // dr_t = dden_t + sum_i -du_i mu k_i^2 / r_t^2
+            token_sums(nt, [&](int t, int c) { return xla[t * DK + c] * xk[t * DK + c] * xk[t * DK + c]; }, sab);
+            for (int t = i; t < nt; t += nth) {
+                const float rr = xr[t], den = sden[t];
+                P.dr[row(t0 + t)] = -ss1[t] / (den * den) - mu * sab[t] / (rr * rr);
+            }
+        }
+        __syncthreads();
+        const float* gla = ISO ? xla : spp;
+        for (int e0 = i; e0 < nt * DK; e0 += 8 * nth) {
+            float rk[8], rla[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int e = e0 + m * nth;
+                const size_t g = row(t0 + (e < nt * DK ? e / DK : 0)) * DK + e % DK;
+                rk[m] = e < nt * DK ? P.dk[g] : 0.f;
+                rla[m] = e < nt * DK ? P.dla[g] : 0.f;
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int e = e0 + m * nth;
+                if (e < nt * DK) {
+                    const size_t g = row(t0 + e / DK) * DK + e % DK;
+                    P.dk[g] = rk[m] + xdk[e];
+                    P.dla[g] = rla[m] + gla[e];
                 }
-                if (i == 0) P.dr[th] = dden + s2;
             }
         }
     }
@@ -524,7 +640,8 @@ cudaError_t launch_backward(const BackwardArgs& a, const BackwardWorkspace& w, c
     g.dk = a.dk_out; g.dla = a.dla; g.dom = a.domega; g.dr = a.dr; g.dp0 = a.dp0;
     g.T = a.T; g.H = a.H; g.DK = a.dk; g.mu = a.mu;
     const int nt = ((a.dk + 31) / 32) * 32;
-    const size_t gsm = sizeof(float) * (2 * kPB * a.dk + 3 * kPB);
+    const int nu = a.variant == 1 ? 1 : a.dk;
+    const size_t gsm = sizeof(float) * (5 * kPB * a.dk + 6 * kPB + kPB * nu);
     auto launch_gain = [&](auto kernel) {
         const cudaError_t e2 = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsm);
         if (e2 != cudaSuccess) return e2;

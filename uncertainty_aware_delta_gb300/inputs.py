@@ -41,7 +41,7 @@ import numpy as np
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    variant: str          # "diag", "iso", "pkda" or "dense"
+    variant: str          # "diag", "iso", "pkda", "dense" or "backward"
     B: int
     H: int
     T: int
@@ -66,6 +66,9 @@ WORKLOADS = {
         Workload("pkda-bf16-b8h16t4096d128", "pkda", 8, 16, 4096, 128, 64, "bf16", (1e-3, 0.1), 20260912),
         # the dense-covariance (exact) filter on the headline shape; inputs as the diagonal recipe
         Workload("dense-bf16-b8h16t4096d128", "dense", 8, 16, 4096, 128, 0, "bf16", (1e-3, 0.1), 20260913),
+        # the backward pass of the diagonal forward on the headline shape; inputs as the diagonal recipe
+        Workload("backward-diag-bf16-b8h16t4096d128", "backward", 8, 16, 4096, 128, 16, "bf16", (1e-3, 0.1),
+                 20260914),
     ]
 }
 
@@ -156,7 +159,7 @@ def workload_inputs(w: Workload, variant: str | None = None):
     workload this returns the prefill tokens only; see :func:`decode_step_inputs`."""
     T = w.prefill if w.steps else w.T
     variant = variant or w.variant
-    if variant == "dense":   # the dense filter takes the diagonal recipe's inputs
+    if variant in ("dense", "backward"):   # these take the diagonal recipe's inputs
         variant = "diag"
     if variant == "pkda":
         return make_pkda_inputs(w.B, T, w.H, w.d, w.d, w.io, w.seed, w.log_alpha_range)
