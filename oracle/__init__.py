@@ -15,6 +15,11 @@ Contents
                  recurrence (KDN paper Eq. 32-37) and the weighted ridge
                  regression closed form (Preconditioned DeltaNet Eq. 1-5;
                  Gated KalmaNet test-time ridge regression).
+  gates       -- the gate branches of the end-to-end layer (KDN reading notes
+                 Sec. 5.1: alpha = sigma(.), omega = softplus(.), r = r_min +
+                 softplus(.), r_min = 0.01), the effective write strength
+                 beta_eff = k^T kappa (Sec. 3.2, App. B Eq. 58-61), and the
+                 forward driven by gate logits.
   backward    -- numpy fp64 adjoint of the token recurrence (the gradients of
                  a weighted sum of o, S_T and p_T with respect to every input),
                  for tiny inputs; the pages give no backward pass.
@@ -22,7 +27,7 @@ Contents
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 against printed values, closed forms, special-case reductions and brute force;
 the backward by ``tests/test_backward_oracle.py`` against central finite
-differences of the forward.
+differences of the forward; the gates by ``tests/test_gates_oracle.py``.
 """
 from .recurrence import build_oracle, forward, step, library_path  # noqa: F401
 from .dense import (  # noqa: F401
@@ -32,3 +37,4 @@ from .dense import (  # noqa: F401
     mobius_product,
     ridge_closed_form,
 )
+from . import gates  # noqa: F401,E402

@@ -24,6 +24,14 @@ q, k, v and log_alpha as above, then per (b, t, h)
   beta_p     = sigmoid(N(0, 1)) * scale    statistic weight (scale 1 unless a test
                                            widens it to push log A above the centre);
 and per head center = exp(N(0, 0.5)) (the pages' positive log-space centre).
+
+Gated workloads (the layer's gate pre-activations, KDN notes Sec. 5.1) draw q,
+k, v as above, then the logits, stored like q, k, v (bf16 for bf16 workloads):
+  alpha_logit ~ U(2.3, 6.9) per (b, t, h, channel): sigma of it lies in about
+               [0.90, 0.999], the decay range of the log_alpha recipe;
+  omega_logit ~ N(-6, 1): per (b, t, h, channel) (diagonal) or per (b, t, h)
+               (isotropic); its softplus is about e^-6, as the omega recipe;
+  r_logit     ~ N(0, 1) per (b, t, h).
 The pages' models L2-normalise q and k (their architecture table), as here.
 
 The shapes follow the KDN paper's 750M/1.3B mixer layers (16 heads of width
@@ -41,7 +49,7 @@ import numpy as np
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    variant: str          # "diag", "iso", "pkda", "dense" or "backward"
+    variant: str          # "diag", "iso", "pkda", "dense", "backward" or "gated"
     B: int
     H: int
     T: int
@@ -69,6 +77,8 @@ WORKLOADS = {
         # the backward pass of the diagonal forward on the headline shape; inputs as the diagonal recipe
         Workload("backward-diag-bf16-b8h16t4096d128", "backward", 8, 16, 4096, 128, 16, "bf16", (1e-3, 0.1),
                  20260914),
+        # the diagonal forward driven by bf16 gate logits (fused gate prologue)
+        Workload("gated-diag-bf16-b8h16t4096d128", "gated", 8, 16, 4096, 128, 64, "bf16", (1e-3, 0.1), 20260915),
     ]
 }
 
@@ -118,6 +128,38 @@ def make_inputs(variant: str, B: int, T: int, H: int, dk: int, dv: int, io: str 
     return out
 
 
+def make_gated_inputs(variant: str, B: int, T: int, H: int, dk: int, dv: int, io: str = "f32",
+                      seed: int = 0, alpha_logit_range=(2.3, 6.9), omega_logit_mean: float = -6.0):
+    """Draw one batch of the gated recipe; returns a dict of fp32 numpy arrays
+    (bf16-valued where io == "bf16").
+
+    Keys: q, k [B,T,H,dk]; v [B,T,H,dv]; alpha_logit [B,T,H,dk]; omega_logit
+    [B,T,H,dk] (diag) or [B,T,H] (iso); r_logit [B,T,H]; plus "io".
+    """
+    if variant not in ("diag", "iso"):
+        raise ValueError(variant)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = {"io": io}
+
+    def store(x64):
+        x32 = x64.astype(np.float32)
+        return round_bf16(x32) if io == "bf16" else x32
+
+    for name in ("q", "k"):
+        x = rng.standard_normal((B, T, H, dk))
+        if dk > 0 and x.size:
+            x /= np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+        out[name] = store(x)
+        del x
+    out["v"] = store(rng.standard_normal((B, T, H, dv)))
+    lo, hi = alpha_logit_range
+    out["alpha_logit"] = store(rng.uniform(lo, hi, size=(B, T, H, dk)))
+    oshape = (B, T, H, dk) if variant == "diag" else (B, T, H)
+    out["omega_logit"] = store(omega_logit_mean + rng.standard_normal(oshape))
+    out["r_logit"] = store(rng.standard_normal((B, T, H)))
+    return out
+
+
 def _sigmoid(x):
     return 1.0 / (1.0 + np.exp(-x))
 
@@ -163,6 +205,8 @@ def workload_inputs(w: Workload, variant: str | None = None):
         variant = "diag"
     if variant == "pkda":
         return make_pkda_inputs(w.B, T, w.H, w.d, w.d, w.io, w.seed, w.log_alpha_range)
+    if variant == "gated":
+        return make_gated_inputs("diag", w.B, T, w.H, w.d, w.d, w.io, w.seed)
     return make_inputs(variant, w.B, T, w.H, w.d, w.d, w.io, w.seed, w.log_alpha_range)
 
 
