@@ -94,6 +94,25 @@ def device_inputs(torch, w, variant, seed, device, T=None, B=None):
     return {"q": q, "k": k, "v": v, "log_alpha": la, "omega": om, "r": r}
 
 
+def device_gated_inputs(torch, w, variant, seed, device):
+    """Gated inputs on the device with the workload recipe (q, k, v as above; gate
+    pre-activations alpha_logit ~ U(2.3, 6.9), omega_logit ~ N(-6, 1), r_logit ~
+    N(0, 1), stored in the io dtype)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    B, T, H, d = w.B, w.T, w.H, w.d
+    iot = torch.bfloat16 if w.io == "bf16" else torch.float32
+    f = dict(device=device, generator=g)
+    q = torch.nn.functional.normalize(torch.randn(B, T, H, d, **f), dim=-1).to(iot)
+    k = torch.nn.functional.normalize(torch.randn(B, T, H, d, **f), dim=-1).to(iot)
+    v = torch.randn(B, T, H, d, **f).to(iot)
+    al = (2.3 + 4.6 * torch.rand(B, T, H, d, **f)).to(iot)
+    oshape = (B, T, H, d) if variant == "diag" else (B, T, H)
+    wl = (-6.0 + torch.randn(*oshape, **f)).to(iot)
+    rl = torch.randn(B, T, H, **f).to(iot)
+    return {"q": q, "k": k, "v": v, "alpha_logit": al, "omega_logit": wl, "r_logit": rl}
+
+
 def device_pkda_inputs(torch, w, seed, device):
     """PKDA inputs on the device with the workload recipe (q, k, v and
     log_alpha as above; beta = sigmoid(N(0,1)), alpha_p = exp(-U(lo, hi)),
@@ -130,6 +149,16 @@ def algorithmic_bytes(B, T, H, dk, dv, io, variant):
     e = 2 if io == "bf16" else 4
     per_tok = e * (2 * dk + dv) + 4 * dk + 4 * (dk if variant == "diag" else 1) + 4 + e * dv
     nu = dk if variant == "diag" else 1
+    return B * T * H * per_tok + B * H * (dk * dv + nu) * 4
+
+
+def gated_algorithmic_bytes(B, T, H, dk, dv, io, variant, beta_eff=False):
+    """Gated forward: q, k, v and the gate logits (alpha [dk], omega [dk] or [1], r)
+    read once in the io dtype, o written once (plus beta_eff, fp32, when requested),
+    final S_T and p_T written once."""
+    e = 2 if io == "bf16" else 4
+    nu = dk if variant == "diag" else 1
+    per_tok = e * (2 * dk + dv) + e * dk + e * nu + e + e * dv + (4 if beta_eff else 0)
     return B * T * H * per_tok + B * H * (dk * dv + nu) * 4
 
 
@@ -482,6 +511,19 @@ def main():
                                                         x["r"]), args.steps, args.warmup, barrier)
         print(json.dumps({"profile": w.name, "kernels_per_step": 1}), flush=True)
         return 0
+    if w.variant == "gated":
+        if not args.profile:
+            print("the gated workload is timed inside the default run (see 'workloads'); use --profile",
+                  file=sys.stderr)
+            return 2
+        x = device_gated_inputs(torch, w, "diag", w.seed, device)
+        gws = torch.empty(kdn.gated_workspace_size(kdn.KDN_DIAG, w.B, w.T, w.H, w.d, w.d, w.chunk, kdn.KDN_BF16),
+                          dtype=torch.uint8, device=device)
+        time_calls(torch, lambda: kdn.kdn_gated_forward("diag", x["q"], x["k"], x["v"], x["alpha_logit"],
+                                                        x["omega_logit"], x["r_logit"], chunk=w.chunk,
+                                                        workspace=gws), args.steps, args.warmup, barrier)
+        print(json.dumps({"profile": w.name, "kernels_per_step": 2}), flush=True)
+        return 0
     variant = w.variant
     vcode = {"diag": kdn.KDN_DIAG, "iso": kdn.KDN_ISO, "pkda": kdn.KDN_PKDA}[variant]
     io = kdn.KDN_BF16 if w.io == "bf16" else kdn.KDN_F32
@@ -625,6 +667,31 @@ def other_workloads(torch, kdn, WORKLOADS, device, barrier, peaks):
                      "hbm_frac": ab / (ms / 1e3) / 1e9 / hbm, "algorithmic_bytes": ab,
                      "traffic": traffic_for("kdn_fused_tc_kernel", name)}
         del x
+    # the forward driven by bf16 gate logits (fused gate prologue) on the headline shape,
+    # without and with the effective write strength
+    w = WORKLOADS["gated-diag-bf16-b8h16t4096d128"]
+    x = device_gated_inputs(torch, w, "diag", w.seed, device)
+    gws = torch.empty(kdn.gated_workspace_size(kdn.KDN_DIAG, w.B, w.T, w.H, w.d, w.d, w.chunk, kdn.KDN_BF16),
+                      dtype=torch.uint8, device=device)
+    beo = torch.empty(w.B, w.T, w.H, device=device)
+    row = {}
+    for with_beta in (False, True):
+        gated = lambda: kdn.kdn_gated_forward("diag", x["q"], x["k"], x["v"], x["alpha_logit"], x["omega_logit"],
+                                              x["r_logit"], chunk=w.chunk, workspace=gws,
+                                              beta_eff=beo if with_beta else False)
+        ms = time_calls(torch, gated, 20, 5, barrier)
+        ab = gated_algorithmic_bytes(w.B, w.T, w.H, w.d, w.d, w.io, "diag", with_beta)
+        key = "with_beta_eff" if with_beta else "plain"
+        row[key] = {"tokens_per_s": w.B * w.T / (ms / 1e3), "ms": ms, "hbm_frac": ab / (ms / 1e3) / 1e9 / hbm,
+                    "algorithmic_bytes": ab}
+    o, S_T, _, _ = kdn.kdn_gated_forward("diag", x["q"], x["k"], x["v"], x["alpha_logit"], x["omega_logit"],
+                                         x["r_logit"], chunk=w.chunk, workspace=gws, beta_eff=beo)
+    row["outputs_finite"] = bool(torch.isfinite(o).all().item() and torch.isfinite(beo).all().item())
+    row["beta_eff_range"] = [float(beo.min().item()), float(beo.max().item())]
+    row["kernel"] = "kdn_fused_tc_kernel (gated instance)"
+    row["traffic"] = traffic_for("kdn_fused_tc_kernel", w.name)
+    out[w.name] = row
+    del x, gws, beo, o, S_T
     # PKDA (preconditioned delta rule with per-channel decay) on the headline shape
     w = WORKLOADS["pkda-bf16-b8h16t4096d128"]
     x = device_pkda_inputs(torch, w, w.seed, device)

@@ -184,6 +184,53 @@ kdn_status kdn_iso_forward(int B, int T, int H, int dk, int dv, int chunk, float
                            void *workspace, size_t workspace_bytes, kdn_stream_t stream);
 
 /*
+ * KDN forward driven by the layer's gate pre-activations (the fused gate
+ * prologue).  KDN reading notes Sec. 5.1: the end-to-end network produces
+ *
+ *   alpha_t = sigma(a_t),  omega_t = softplus(w_t),  r_t = r_min + softplus(rho_t),
+ *
+ * where a, w, rho are the projections W x + b of the layer input (computing
+ * them is the caller's GEMM).  This call takes a, w, rho and runs the forward of
+ * kdn_diag_forward / kdn_iso_forward on log alpha = log sigma(a) = -softplus(-a),
+ * omega and r.  Optionally it also writes the effective write strength of every
+ * token (reading notes Sec. 3.2; the paper's App. B, Eq. 58-61)
+ *
+ *   beta_eff_t = k_t^T kappa_t = z_t / (r_t + z_t),   z_t = k_t^T P_hat_t k_t,
+ *
+ * the fraction of the innovation along k_t that the write removes, in [0, 1).
+ *
+ * variant: KDN_DIAG or KDN_ISO (other values: KDN_ERR_SHAPE).
+ * Inputs : q, k, v, S0, p0, mu, chunk, flags as kdn_diag_forward / kdn_iso_forward;
+ *          alpha_logit [B,T,H,dk] io_dtype; omega_logit [B,T,H,dk] (diagonal) or
+ *          [B,T,H] (isotropic) io_dtype; r_logit [B,T,H] io_dtype.
+ *          r_min: floor of the observation-noise variance (< 0 selects the notes'
+ *          0.01; NaN or infinity returns KDN_ERR_SHAPE).
+ * Outputs: o, S_T, p_T as the ungated forward; beta_eff [B,T,H] fp32, or NULL.
+ * Paths  : one elementwise kernel over every SM evaluates the three branches from
+ *          the logits into fp32 log alpha, omega and r in the workspace; the
+ *          ungated forward path for these sizes (see "Supported sizes") then runs on
+ *          them.  beta_eff comes from the gains that path forms: on the tensor-core
+ *          path from the diagonal of the chunk's gain system, z_t = r_t +
+ *          k_t^T P_hat_t k_t (requesting it keeps one CTA per sequence: no sequence
+ *          split), on the CUDA-core path as k^T kappa from the gain scan.  (The
+ *          branches evaluated inside the fused kernel's gain pass instead were measured
+ *          slower: that pass is serial per token and the transcendentals lengthen it.)
+ * Workspace: kdn_gated_workspace_size() bytes (at least kdn_workspace_size() of
+ *          the same arguments).
+ * Errors : as kdn_diag_forward; KDN_ERR_ALIAS also when beta_eff overlaps an
+ *          input or another output.
+ */
+size_t kdn_gated_workspace_size(int variant, int B, int T, int H, int dk, int dv, int chunk,
+                                int io_dtype, uint32_t flags);
+kdn_status kdn_gated_forward(int variant, int B, int T, int H, int dk, int dv, int chunk, float mu,
+                             float r_min, int io_dtype, uint32_t flags,
+                             const void *q, const void *k, const void *v,
+                             const void *alpha_logit, const void *omega_logit, const void *r_logit,
+                             const float *S0, const float *p0,
+                             void *o, float *S_T, float *p_T, float *beta_eff,
+                             void *workspace, size_t workspace_bytes, kdn_stream_t stream);
+
+/*
  * Preconditioned delta rule with per-channel decay, PKDA ("Preconditioned
  * DeltaNet", arXiv:2604.21100v1: Sec. 2.4 Eq. 9, the write key; Sec. 2.5, the
  * decayed state; Sec. 2.6, its chunkwise form).  PGDN is the special case of

@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
     for n in ("kdn_diag_forward", "kdn_iso_forward", "kdn_step", "kdn_workspace_size",
               "kdn_read_device_status", "kdn_status_string", "kdn_abi_version",
               "kdn_forward_kernel_count", "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step",
-              "kdn_dense_forward", "kdn_step_ex", "kdn_backward", "kdn_backward_workspace_size"):
+              "kdn_dense_forward", "kdn_step_ex", "kdn_backward", "kdn_backward_workspace_size",
+              "kdn_gated_forward", "kdn_gated_workspace_size"):
         assert n in names
 
 
@@ -47,7 +48,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings_and_version(lib):
     import uncertainty_aware_delta_gb300 as kdn
 
-    assert lib.kdn_abi_version() == 104
+    assert lib.kdn_abi_version() == 105
     for code in range(0, 11):
         s = kdn.status_string(code)
         assert s and s != "unknown status"
@@ -140,6 +141,52 @@ def test_validation_rejects_before_launch(lib, variant):
     assert _call(lib, _fwd_args(k=72), variant) == 4           # KDN_ERR_ALIGN (72 % 16 != 0)
     assert _call(lib, _fwd_args(o=64 + 16), variant) == 10     # KDN_ERR_ALIAS (o overlaps q)
     assert _call(lib, _fwd_args(ws=1 << 20), variant) == 10    # workspace overlaps o
+
+
+def test_gated_workspace_rules(lib):
+    import uncertainty_aware_delta_gb300 as kdn
+
+    gws, ws = kdn.gated_workspace_size, kdn.workspace_size
+    assert gws(2, 1, 64, 2, 16, 16, 16, 0, 0) == 0            # PKDA has no gates
+    assert gws(0, 1, 64, 2, 24, 16, 16, 0, 0) == 0
+    # every path: the ungated scratch plus fp32 log alpha, omega and r
+    for (B, T, H, d, io) in ((2, 100, 3, 32, 0), (8, 4096, 16, 128, 1), (1, 65536, 16, 128, 1)):
+        for v, nu in ((0, d), (1, 1)):
+            n = B * T * H
+            assert gws(v, B, T, H, d, d, 0, io, 0) >= ws(v, B, T, H, d, d, 0, io, 0) + 4 * n * (d + nu + 1)
+            assert gws(v, B, T, H, d, d, 0, io, 0) % 256 == 0
+    # T = 0: nothing beyond the status word
+    assert gws(0, 2, 0, 2, 128, 128, 0, 1, 0) == ws(0, 2, 0, 2, 128, 128, 0, 1, 0)
+
+
+def test_gated_validation_rejects_before_launch(lib):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+
+    def call(variant=0, dk=16, io=0, T=64, r_min=-1.0, wsb=1 << 20, **ptr):
+        p = dict(q=64, k=64, v=64, al=64, wl=64, rl=64, S0=None, p0=None, o=1 << 20, S_T=2 << 20, p_T=3 << 20,
+                 be=None, ws=4 << 20)
+        p.update(ptr)
+        return lib.kdn_gated_forward(variant, 1, T, 2, dk, 16, 16, -1.0, r_min, io, 0, vp(p["q"]), vp(p["k"]),
+                                     vp(p["v"]), vp(p["al"]), vp(p["wl"]), vp(p["rl"]), vp(p["S0"]), vp(p["p0"]),
+                                     vp(p["o"]), vp(p["S_T"]), vp(p["p_T"]), vp(p["be"]), vp(p["ws"]), wsb, None)
+
+    assert call(variant=2) == 2                      # KDN_ERR_SHAPE: no gates for PKDA
+    assert call(dk=24) == 6                          # KDN_ERR_UNSUPPORTED
+    assert call(io=3) == 3                           # KDN_ERR_DTYPE
+    assert call(T=-1) == 2
+    assert call(r_min=float("nan")) == 2
+    assert call(r_min=float("inf")) == 2
+    assert call(q=None) == 1                         # KDN_ERR_NULL
+    assert call(wl=None) == 1
+    assert call(S_T=None) == 1
+    assert call(ws=None) == 5                        # KDN_ERR_WORKSPACE
+    assert call(wsb=256) == 5
+    assert call(rl=72) == 4                          # KDN_ERR_ALIGN
+    assert call(be=(5 << 20) + 8) == 4
+    assert call(o=64 + 16) == 10                     # KDN_ERR_ALIAS: o overlaps the inputs
+    assert call(be=(1 << 20) + 64) == 10             # beta_eff overlaps o
+    assert call(be=64) == 10                         # beta_eff overlaps the inputs
+    assert call(ws=(3 << 20)) == 10                  # workspace overlaps p_T
 
 
 def test_dense_validation_rejects_before_launch(lib):

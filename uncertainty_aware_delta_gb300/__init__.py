@@ -19,6 +19,7 @@ from .binding import (  # noqa: F401
     kdn_backward,
     kdn_diag_forward,
     kdn_forward_noalloc,
+    kdn_gated_forward,
     kdn_iso_forward,
     kdn_dense_forward,
     kdn_pkda_forward,
@@ -26,6 +27,7 @@ from .binding import (  # noqa: F401
     kdn_read_device_status,
     kdn_step,
     forward_kernel_count,
+    gated_workspace_size,
     library,
     library_path,
     status_string,

@@ -27,7 +27,7 @@ EXPORTED = (
     "kdn_workspace_size", "kdn_diag_forward", "kdn_iso_forward", "kdn_step",
     "kdn_read_device_status", "kdn_status_string", "kdn_abi_version", "kdn_forward_kernel_count",
     "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step", "kdn_dense_forward", "kdn_step_ex",
-    "kdn_backward", "kdn_backward_workspace_size",
+    "kdn_backward", "kdn_backward_workspace_size", "kdn_gated_forward", "kdn_gated_workspace_size",
 )
 
 
@@ -86,6 +86,11 @@ def library():
             lib.kdn_backward.restype = i32
             lib.kdn_backward.argtypes = [i32] * 6 + [f32, i32] + [vp] * 3 + [fp] * 5 + [vp, fp, fp] + [fp] * 8 + \
                 [vp, sz, vp]
+            lib.kdn_gated_workspace_size.restype = sz
+            lib.kdn_gated_workspace_size.argtypes = [i32] * 8 + [u32]
+            lib.kdn_gated_forward.restype = i32
+            lib.kdn_gated_forward.argtypes = [i32] * 7 + [f32, f32, i32, u32] + [vp] * 6 + [fp, fp] + \
+                [vp, fp, fp, fp] + [vp, sz, vp]
             lib.kdn_abi_version.restype = i32
             lib.kdn_abi_version.argtypes = []
             _lib = lib
@@ -192,6 +197,73 @@ def kdn_iso_forward(q, k, v, log_alpha, omega, r, S0=None, p0=None, *, mu=None, 
     """Isotropic KDN forward (KDN paper Sec. 4.2): omega [B,T,H], p0/p_T [B,H]."""
     return _forward(KDN_ISO, q, k, v, log_alpha, omega, r, S0, p0, mu, chunk, flags, out,
                     workspace, stream)
+
+
+def gated_workspace_size(variant, B, T, H, dk, dv, chunk=0, io=KDN_BF16, flags=0) -> int:
+    return int(library().kdn_gated_workspace_size(variant, B, T, H, dk, dv, chunk, io, flags))
+
+
+def kdn_gated_forward(variant, q, k, v, alpha_logit, omega_logit, r_logit, S0=None, p0=None, *, mu=None,
+                      r_min=None, chunk=0, flags=0, beta_eff=False, out=None, workspace=None, stream=None):
+    """KDN forward driven by gate pre-activations (KDN notes Sec. 5.1):
+    alpha = sigmoid(alpha_logit), omega = softplus(omega_logit), r = r_min +
+    softplus(r_logit).  Returns (o, S_T, p_T, beta_eff or None).
+
+    variant: "diag" / "iso" (or KDN_DIAG / KDN_ISO).  The logits have the io dtype
+    of q: alpha_logit [B,T,H,dk], omega_logit [B,T,H,dk] (diag) or [B,T,H] (iso),
+    r_logit [B,T,H].  r_min=None selects 0.01.  ``beta_eff=True`` also returns the
+    effective write strength k^T kappa [B,T,H] fp32 (or pass a tensor to fill).
+    ``out=(o, S_T, p_T)`` writes into given tensors.
+    """
+    variant = {"diag": KDN_DIAG, "iso": KDN_ISO}.get(variant, variant)
+    lib = library()
+    device = q.device
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    io = KDN_BF16 if q.dtype == torch.bfloat16 else KDN_F32
+    iot = torch.bfloat16 if io == KDN_BF16 else torch.float32
+    nu = (dk,) if variant == KDN_DIAG else ()
+    _check(q, "q", iot, (B, T, H, dk), device)
+    _check(k, "k", iot, (B, T, H, dk), device)
+    _check(v, "v", iot, (B, T, H, dv), device)
+    _check(alpha_logit, "alpha_logit", iot, (B, T, H, dk), device)
+    _check(omega_logit, "omega_logit", iot, (B, T, H) + nu, device)
+    _check(r_logit, "r_logit", iot, (B, T, H), device)
+    _check(S0, "S0", torch.float32, (B, H, dk, dv), device)
+    _check(p0, "p0", torch.float32, (B, H) + nu, device)
+    if out is None:
+        o = torch.empty((B, T, H, dv), dtype=iot, device=device)
+        S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=device)
+        p_T = torch.empty((B, H) + nu, dtype=torch.float32, device=device)
+    else:
+        o, S_T, p_T = out
+        _check(o, "o", iot, (B, T, H, dv), device)
+        _check(S_T, "S_T", torch.float32, (B, H, dk, dv), device)
+        _check(p_T, "p_T", torch.float32, (B, H) + nu, device)
+    if beta_eff is True:
+        be = torch.empty((B, T, H), dtype=torch.float32, device=device)
+    elif beta_eff is False or beta_eff is None:
+        be = None
+    else:
+        be = beta_eff
+        _check(be, "beta_eff", torch.float32, (B, T, H), device)
+    need = lib.kdn_gated_workspace_size(variant, B, T, H, dk, dv, chunk, io, flags)
+    if need == 0:
+        raise KDNError(6, "kdn_gated_workspace_size rejected the arguments")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds {workspace.numel()} bytes, {need} needed")
+    mu = -1.0 if mu is None else float(mu)
+    r_min = -1.0 if r_min is None else float(r_min)
+    with torch.cuda.device(device):
+        st = lib.kdn_gated_forward(variant, B, T, H, dk, dv, int(chunk), mu, r_min, io, int(flags), _ptr(q),
+                                   _ptr(k), _ptr(v), _ptr(alpha_logit), _ptr(omega_logit), _ptr(r_logit),
+                                   _ptr(S0), _ptr(p0), _ptr(o), _ptr(S_T), _ptr(p_T), _ptr(be), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream, device))
+    if st != 0:
+        raise KDNError(st, "kdn_gated_forward")
+    return o, S_T, p_T, be
 
 
 def kdn_step(variant, q, k, v, log_alpha, omega, r, S, p, *, mu=None, o=None, workspace=None,

@@ -1,6 +1,7 @@
 // C ABI of the KDN mixer library: argument validation, workspace carving and
 // kernel dispatch.  See include/kdn.h for the contract of every entry point.
 
+#include <cmath>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -118,7 +119,7 @@ kdn_status forward_impl(int variant, int B, int T, int H, int dk, int dv, int ch
                         const float* log_alpha, const float* omega, const float* r,
                         const float* S0, const float* p0, void* o, float* S_T, float* p_T,
                         void* workspace, size_t workspace_bytes, kdn_stream_t stream,
-                        const PkdaInputs& pk) {
+                        const PkdaInputs& pk, float* beta_eff = nullptr) {
     kdn_status st = validate_common(variant, B, T, H, dk, dv, chunk, io);
     if (st != KDN_OK) return st;
     chunk = resolve_chunk(chunk, T);
@@ -170,6 +171,7 @@ kdn_status forward_impl(int variant, int B, int T, int H, int dk, int dv, int ch
     a.beta = pk.beta; a.alpha_p = pk.alpha_p; a.beta_p = pk.beta_p; a.center = pk.center;
     a.neg_log2x = -log2f(resolve_x(pk.x));
     a.flags = flags;
+    a.beta_eff = beta_eff;
 
     cudaError_t e;
     if (T == 0) {
@@ -197,6 +199,8 @@ kdn_status forward_impl(int variant, int B, int T, int H, int dk, int dv, int ch
         sw.n_chunks_g = w.nG;
         e = kdn::launch_gain_scan(a, sw, s);
         if (e == cudaSuccess) e = kdn::launch_chunk_simt(a, sw.kappa, s);
+        // effective write strength k^T kappa from the scan's gains
+        if (e == cudaSuccess && beta_eff) e = kdn::launch_beta_from_kappa(B, T, H, dk, io, k, sw.kappa, beta_eff, s);
     }
     return e == cudaSuccess ? KDN_OK : KDN_ERR_CUDA;
 }
@@ -243,6 +247,106 @@ kdn_status kdn_pkda_forward(int B, int T, int H, int dk, int dv, int chunk, floa
     return forward_impl(KDN_PKDA, B, T, H, dk, dv, chunk, 0.f, io_dtype, flags, q, k, v, log_alpha,
                         nullptr, nullptr, S0, A0, o, S_T, A_T, workspace, workspace_bytes, stream,
                         PkdaInputs{beta, alpha_p, beta_p, center, x});
+}
+
+}  // extern "C"
+
+namespace {
+
+// Gated forward: the ungated path's workspace first, then the fp32 gates
+// (log alpha [B,T,H,dk], omega [B,T,H,dk] or [B,T,H], r [B,T,H]) the gate prologue
+// writes and that path reads.
+struct GatedLayout {
+    size_t base;                 // the ungated path's workspace (kdn_workspace_size)
+    size_t la_off, om_off, r_off, total;
+};
+
+GatedLayout gated_layout(int variant, int B, int T, int H, int dk, int dv, int chunk, int io, uint32_t flags) {
+    GatedLayout g;
+    memset(&g, 0, sizeof(g));
+    g.base = align_up(ws_layout(variant, B, T, H, dk, dv, chunk, io, flags).total);
+    size_t off = g.base;
+    if (T > 0) {
+        const size_t ntok = (size_t)B * T * H, nu = variant == KDN_ISO ? 1 : (size_t)dk;
+        g.la_off = off;
+        off = align_up(off + 4 * ntok * dk);
+        g.om_off = off;
+        off = align_up(off + 4 * ntok * nu);
+        g.r_off = off;
+        off = align_up(off + 4 * ntok);
+    }
+    g.total = off;
+    return g;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kdn_gated_workspace_size(int variant, int B, int T, int H, int dk, int dv, int chunk,
+                                int io_dtype, uint32_t flags) {
+    if (variant != KDN_DIAG && variant != KDN_ISO) return 0;
+    if (validate_common(variant, B, T, H, dk, dv, chunk, io_dtype) != KDN_OK) return 0;
+    chunk = resolve_chunk(chunk, T);
+    return gated_layout(variant, B, T, H, dk, dv, chunk, io_dtype, flags).total;
+}
+
+kdn_status kdn_gated_forward(int variant, int B, int T, int H, int dk, int dv, int chunk, float mu,
+                             float r_min, int io_dtype, uint32_t flags, const void* q, const void* k,
+                             const void* v, const void* alpha_logit, const void* omega_logit,
+                             const void* r_logit, const float* S0, const float* p0, void* o, float* S_T,
+                             float* p_T, float* beta_eff, void* workspace, size_t workspace_bytes,
+                             kdn_stream_t stream) {
+    if (variant != KDN_DIAG && variant != KDN_ISO) return KDN_ERR_SHAPE;
+    kdn_status st = validate_common(variant, B, T, H, dk, dv, chunk, io_dtype);
+    if (st != KDN_OK) return st;
+    if (std::isnan(r_min) || std::isinf(r_min)) return KDN_ERR_SHAPE;
+    if (r_min < 0.f) r_min = 0.01f;
+    chunk = resolve_chunk(chunk, T);
+    const size_t BH = (size_t)B * H, ntok = (size_t)B * T * H, esz = io_dtype == KDN_BF16 ? 2 : 4;
+    const size_t nu = variant == KDN_ISO ? 1 : (size_t)dk;
+    if (!workspace) return KDN_ERR_WORKSPACE;
+    if (BH > 0 && (!S_T || !p_T)) return KDN_ERR_NULL;
+    if (ntok > 0 && (!q || !k || !v || !alpha_logit || !omega_logit || !r_logit || !o)) return KDN_ERR_NULL;
+    const void* ptrs[] = {q, k, v, alpha_logit, omega_logit, r_logit, S0, p0, o, S_T, p_T, beta_eff, workspace};
+    for (const void* x : ptrs)
+        if (x && !aligned16(x)) return KDN_ERR_ALIGN;
+    const GatedLayout g = gated_layout(variant, B, T, H, dk, dv, chunk, io_dtype, flags);
+    if (workspace_bytes < g.total) return KDN_ERR_WORKSPACE;
+    const Range in[] = {{q, ntok * dk * esz}, {k, ntok * dk * esz}, {v, ntok * dv * esz},
+                        {alpha_logit, ntok * dk * esz}, {omega_logit, ntok * nu * esz}, {r_logit, ntok * esz},
+                        {S0, BH * dk * dv * 4}, {p0, BH * nu * 4}};
+    const Range out[] = {{o, ntok * dv * esz}, {S_T, BH * dk * dv * 4}, {p_T, BH * nu * 4},
+                         {beta_eff, ntok * 4}, {workspace, g.total}};
+    const int nout = sizeof(out) / sizeof(out[0]);
+    for (int o1 = 0; o1 < nout; ++o1) {
+        for (const Range& x : in) {
+            // resuming in place: S_T may be S0 and p_T may be p0
+            if ((o1 == 1 && x.p == S0 && S0 == (const float*)S_T) || (o1 == 2 && x.p == p0 && p0 == (const float*)p_T))
+                continue;
+            if (overlaps(out[o1], x)) return KDN_ERR_ALIAS;
+        }
+        for (int o2 = o1 + 1; o2 < nout; ++o2)
+            if (overlaps(out[o1], out[o2])) return KDN_ERR_ALIAS;
+    }
+
+    // fp32 gates into the workspace (one elementwise kernel over all SMs), then the
+    // ungated path on them, its own scratch at the start of the workspace.  With
+    // beta_eff requested the tensor-core path keeps one CTA per sequence (the split
+    // path does not form it); its workspace is then no larger.
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(workspace);
+    float* la = reinterpret_cast<float*>(base + g.la_off);
+    float* om = reinterpret_cast<float*>(base + g.om_off);
+    float* rr = reinterpret_cast<float*>(base + g.r_off);
+    if (T > 0 && BH > 0 &&
+        kdn::launch_gate_expand(variant, B, T, H, dk, io_dtype, r_min, alpha_logit, omega_logit, r_logit, la, om, rr,
+                                s) != cudaSuccess)
+        return KDN_ERR_CUDA;
+    const bool on = T > 0;
+    return forward_impl(variant, B, T, H, dk, dv, chunk, mu, io_dtype, beta_eff ? (flags | KDN_FLAG_NO_SPLIT) : flags,
+                        q, k, v, on ? la : nullptr, on ? om : nullptr, on ? rr : nullptr, S0, p0, o, S_T, p_T,
+                        workspace, g.base, stream, PkdaInputs{}, on ? beta_eff : nullptr);
 }
 
 }  // extern "C"
@@ -519,6 +623,6 @@ const char* kdn_status_string(int status) {
     }
 }
 
-int kdn_abi_version(void) { return 104; }
+int kdn_abi_version(void) { return 105; }
 
 }  // extern "C"

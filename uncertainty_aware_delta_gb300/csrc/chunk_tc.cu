@@ -27,7 +27,8 @@
 //       (Eq. 25).  Since K_bar_t . K_til'_t = sum_i p_hat_t,i k_t,i^2 (the decay
 //       factors cancel), the scaled innovations Delta' = diag(1/z) Delta solve
 //       M Delta' = V - K_bar S_m  with  M = diag(r) + lower_incl(K_bar K_til'^T),
-//       so z comes out of the Gram MMA.  T = M^{-1}: 16x16 diagonal blocks by
+//       so z comes out of the Gram MMA (and with it, on request, the effective
+//       write strength k^T kappa = (z - r) / z of App. B Eq. 58-61).  T = M^{-1}: 16x16 diagonal blocks by
 //       forward substitution, merged 16 -> 32 -> 64 (tf32 mma.sync).
 //   G   state: S_m^T = S_in^T diag(e^{G_ref}) in TMEM, plus a bf16 copy in TMEM
 //       that is the A operand of the prediction/query MMA.  The state is kept with
@@ -159,6 +160,7 @@ struct TcParams {
                           // otherwise every CTA writes its final state to S_T at blockIdx.x
     long long p0_bh, p0_seg;   // p0 element offset of (bh, seg): bh * p0_bh + seg * p0_seg
     int probe;            // timeout probe (KDN_FLAG_TIMEOUT_PROBE): one wait that nothing completes
+    float* beta_eff;      // KDN, whole sequences: effective write strength [B,T,H], or null
 };
 
 // Kernel variants: the two KDN uncertainty models and the preconditioned delta
@@ -1018,6 +1020,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                         const float z = sm[SM_RZ + pb * 64 + lt] + __uint_as_float(x[0]);
                         row[lt] = z;
                         sm[SM_INVD + lt] = 1.0f / z;
+                        // effective write strength k^T kappa = (z - r) / z: the Gram
+                        // diagonal over z (isotropic: both divided by b_hat)
+                        if (!SEG && P.beta_eff && lt < nv)
+                            P.beta_eff[(static_cast<size_t>(b) * Tall + t0 + lt) * H + h] = __uint_as_float(x[0]) / z;
                     }
                 } else {
                     const int t = lt - 64;
@@ -1382,6 +1388,9 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStrea
     P.p0_bh = nu;
     P.p0_seg = 0;
     P.probe = (a.flags & KDN_FLAG_TIMEOUT_PROBE) ? 1 : 0;
+    // (the split path never writes the effective write strength: its callers keep
+    //  one CTA per sequence when they want it)
+    P.beta_eff = (sp.nseg > 1 || a.variant == kVarPkda) ? nullptr : a.beta_eff;
     int grid = a.B * a.H;
     auto launch = [&](auto kernel) {
         const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);

@@ -21,7 +21,20 @@ struct ForwardArgs {
     const float *beta, *alpha_p, *beta_p, *center;
     float neg_log2x;
     uint32_t flags;    // KDN_FLAG_* of the call
+    // KDN: effective write strength k^T kappa [B,T,H] fp32, or null (not written).
+    // The tensor-core path writes it only when it runs whole sequences.
+    float* beta_eff;
 };
+
+// Gate branches on pre-activations into fp32 log_alpha [B,T,H,dk], omega
+// [B,T,H,dk] (diagonal) or [B,T,H] (isotropic) and r [B,T,H], for the paths that
+// take fp32 gates.  gates.cu
+cudaError_t launch_gate_expand(int variant, int B, int T, int H, int dk, int io, float r_min,
+                               const void* alpha_logit, const void* omega_logit, const void* r_logit,
+                               float* log_alpha, float* omega, float* r, cudaStream_t s);
+// beta_eff [B,T,H] = sum_i k_i kappa_i from the gain scan's kappa [B,T,H,dk].  gates.cu
+cudaError_t launch_beta_from_kappa(int B, int T, int H, int dk, int io, const void* k, const float* kappa,
+                                   float* beta_eff, cudaStream_t s);
 
 // Gain-scan workspace (CUDA-core path): gains and Moebius chunk summaries.
 struct ScanWorkspace {
