@@ -688,8 +688,8 @@ def other_workloads(torch, kdn, WORKLOADS, device, barrier, peaks):
                                          x["r_logit"], chunk=w.chunk, workspace=gws, beta_eff=beo)
     row["outputs_finite"] = bool(torch.isfinite(o).all().item() and torch.isfinite(beo).all().item())
     row["beta_eff_range"] = [float(beo.min().item()), float(beo.max().item())]
-    row["kernel"] = "kdn_fused_tc_kernel (gated instance)"
-    row["traffic"] = traffic_for("kdn_fused_tc_kernel", w.name)
+    row["kernels"] = "gate_expand_bf16_kernel + kdn_fused_tc_kernel"
+    row["traffic"] = {k: traffic_for(k, w.name) for k in ("gate_expand_bf16_kernel", "kdn_fused_tc_kernel")}
     out[w.name] = row
     del x, gws, beo, o, S_T
     # PKDA (preconditioned delta rule with per-channel decay) on the headline shape
@@ -736,6 +736,7 @@ def other_workloads(torch, kdn, WORKLOADS, device, barrier, peaks):
                    "bound": "alu", "algorithmic_flops": flops, "achieved_tflops": flops / (ms / 1e3) / 1e12,
                    "peak_tflops": peak, "alu_frac": flops / (ms / 1e3) / 1e12 / peak,
                    "outputs_finite": finite, "device_status": kdn.kdn_read_device_status(ws),
+                   "traffic": {k: traffic_for(k, w.name) for k in ("mem_adjoint_kernel", "gain_adjoint_kernel")},
                    "peak_source": "SM count x 128 fp32 lanes x 2 flop x 2070 MHz (maximum SM clock)"}
     del x, dO, ws, g
     # decode: 512-token prefill through the forward path, then 1024 single-token steps
