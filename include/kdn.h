@@ -328,15 +328,26 @@ kdn_status kdn_pkda_step(int B, int H, int dk, int dv, float x, int io_dtype,
  * Outputs: o [B,T,H,d] io_dtype; S_T, P_T [B,H,d,d] fp32 (the state after token
  *          T-1; S_T == S0 and P_T == P0 are allowed).
  * Sizes  : d in {32, 64, 128} (d_k = d_v = d); any T >= 0; B, H >= 0.
- * The tokens of a head run in order on one CTA with P and S in registers (O(d^2)
- * work per token and head, fp32; no workspace, no device status).  Alignment,
- * aliasing and errors as kdn_diag_forward.
+ * Two passes.  The covariance recurrence runs token by token, one CTA per head
+ * with P in registers, and writes the gains kappa_t [B,T,H,d] fp32 into the
+ * workspace (with the decay held outside P: P_t = G_t Ptil_t G_t for the
+ * running product G_t of the decays, so a token costs one matrix-vector product
+ * and one rank-1 downdate, 2 d^2 multiply-adds; G is folded into Ptil whenever a
+ * channel's running decay would fall below 2^-20).  Given the gains, the mean
+ * S = diag(a) S + kappa (v - (diag(a) S)^T k)^T is the delta rule with write
+ * key kappa and runs chunkwise: on the fused tensor-core kernel (bf16 io,
+ * d = 128, T > 32) or on the CUDA-core chunk path.
+ * Workspace: kdn_dense_workspace_size() bytes (its first 256 bytes hold the
+ *          device status word; then kappa, 4 B T H d bytes).
+ * Alignment, aliasing and errors as kdn_diag_forward.
  */
+size_t kdn_dense_workspace_size(int B, int T, int H, int d, int io_dtype);
 kdn_status kdn_dense_forward(int B, int T, int H, int d, int io_dtype,
                              const void *q, const void *k, const void *v,
                              const float *log_alpha, const float *omega, const float *r,
                              const float *S0, const float *P0,
-                             void *o, float *S_T, float *P_T, kdn_stream_t stream);
+                             void *o, float *S_T, float *P_T,
+                             void *workspace, size_t workspace_bytes, kdn_stream_t stream);
 
 /*
  * Backward pass of the Diagonal or Isotropic KDN forward: the gradients of

@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
               "kdn_read_device_status", "kdn_status_string", "kdn_abi_version",
               "kdn_forward_kernel_count", "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step",
               "kdn_dense_forward", "kdn_step_ex", "kdn_backward", "kdn_backward_workspace_size",
-              "kdn_gated_forward", "kdn_gated_workspace_size"):
+              "kdn_gated_forward", "kdn_gated_workspace_size", "kdn_dense_workspace_size"):
         assert n in names
 
 
@@ -48,7 +48,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings_and_version(lib):
     import uncertainty_aware_delta_gb300 as kdn
 
-    assert lib.kdn_abi_version() == 105
+    assert lib.kdn_abi_version() == 106
     for code in range(0, 11):
         s = kdn.status_string(code)
         assert s and s != "unknown status"
@@ -193,13 +193,18 @@ def test_dense_validation_rejects_before_launch(lib):
     # B=1 T=64 H=2 d=32: inputs of 64*2*32 elements; each case fails a host check
     vp = ctypes.c_void_p
 
-    def call(d=32, io=0, T=64, **ptr):
+    def call(d=32, io=0, T=64, wsb=1 << 20, **ptr):
         p = dict(q=1 << 16, k=2 << 16, v=3 << 16, la=4 << 16, om=5 << 16, r=6 << 16, S0=None, P0=None,
-                 o=1 << 20, S_T=2 << 20, P_T=3 << 20)
+                 o=1 << 20, S_T=2 << 20, P_T=3 << 20, ws=4 << 20)
         p.update(ptr)
         args = [vp(p[n]) if p[n] is not None else None
-                for n in ("q", "k", "v", "la", "om", "r", "S0", "P0", "o", "S_T", "P_T")]
-        return lib.kdn_dense_forward(1, T, 2, d, io, *args, None)
+                for n in ("q", "k", "v", "la", "om", "r", "S0", "P0", "o", "S_T", "P_T", "ws")]
+        return lib.kdn_dense_forward(1, T, 2, d, io, *args, wsb, None)
+
+    # the workspace holds the status word and the gains kappa [B,T,H,d] fp32
+    assert lib.kdn_dense_workspace_size(1, 64, 2, 32, 0) >= 256 + 4 * 64 * 2 * 32
+    assert lib.kdn_dense_workspace_size(1, 64, 2, 16, 0) == 0
+    assert lib.kdn_dense_workspace_size(1, 64, 2, 32, 2) == 0
 
     assert call(d=16) == 6                     # KDN_ERR_UNSUPPORTED
     assert call(io=2) == 3                     # KDN_ERR_DTYPE
@@ -210,6 +215,9 @@ def test_dense_validation_rejects_before_launch(lib):
     assert call(o=(1 << 16) + 64) == 10        # KDN_ERR_ALIAS: o overlaps q
     assert call(P_T=(2 << 20) + 256) == 10     # P_T overlaps S_T
     assert call(P0=(2 << 20)) == 10            # P0 overlaps S_T
+    assert call(ws=None) == 5                  # KDN_ERR_WORKSPACE
+    assert call(wsb=1024) == 5
+    assert call(ws=(3 << 20) + 4096) == 10     # workspace overlaps P_T
 
 
 def test_step_validation_rejects_before_launch(lib):

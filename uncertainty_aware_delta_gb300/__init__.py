@@ -26,6 +26,7 @@ from .binding import (  # noqa: F401
     kdn_pkda_step,
     kdn_read_device_status,
     kdn_step,
+    dense_workspace_size,
     forward_kernel_count,
     gated_workspace_size,
     library,

@@ -28,6 +28,7 @@ EXPORTED = (
     "kdn_read_device_status", "kdn_status_string", "kdn_abi_version", "kdn_forward_kernel_count",
     "kdn_forward_noalloc", "kdn_pkda_forward", "kdn_pkda_step", "kdn_dense_forward", "kdn_step_ex",
     "kdn_backward", "kdn_backward_workspace_size", "kdn_gated_forward", "kdn_gated_workspace_size",
+    "kdn_dense_workspace_size",
 )
 
 
@@ -80,7 +81,9 @@ def library():
             lib.kdn_forward_noalloc.argtypes = [i32] * 7 + [f32, i32, u32] + [vp] * 3 + [fp] * 5 + \
                 [vp, fp, fp, vp, vp]
             lib.kdn_dense_forward.restype = i32
-            lib.kdn_dense_forward.argtypes = [i32] * 5 + [vp] * 3 + [fp] * 5 + [vp, fp, fp, vp]
+            lib.kdn_dense_forward.argtypes = [i32] * 5 + [vp] * 3 + [fp] * 5 + [vp, fp, fp] + [vp, sz, vp]
+            lib.kdn_dense_workspace_size.restype = sz
+            lib.kdn_dense_workspace_size.argtypes = [i32] * 5
             lib.kdn_backward_workspace_size.restype = sz
             lib.kdn_backward_workspace_size.argtypes = [i32] * 7
             lib.kdn_backward.restype = i32
@@ -425,12 +428,17 @@ def kdn_forward_noalloc(variant, q, k, v, log_alpha, omega, r, S0=None, p0=None,
     return o, S_T, p_T
 
 
-def kdn_dense_forward(q, k, v, log_alpha, omega, r, S0=None, P0=None, *, out=None, stream=None):
+def dense_workspace_size(B, T, H, d, io=KDN_BF16) -> int:
+    return int(library().kdn_dense_workspace_size(B, T, H, d, io))
+
+
+def kdn_dense_forward(q, k, v, log_alpha, omega, r, S0=None, P0=None, *, out=None, workspace=None, stream=None):
     """Dense-covariance (exact) Kalman memory forward (KDN paper Sec. 3.2).  Returns (o, S_T, P_T).
 
     q, k, v [B,T,H,d] in fp32 or bf16 (d in 32, 64, 128); log_alpha, omega [B,T,H,d],
     r [B,T,H] fp32; optional S0 [B,H,d,d] (zero) and P0 [B,H,d,d] (identity) fp32.
-    ``out=(o, S_T, P_T)`` writes into given tensors.
+    ``out=(o, S_T, P_T)`` writes into given tensors; ``workspace`` (uint8 device
+    tensor of dense_workspace_size() bytes) is allocated when not given.
     """
     lib = library()
     device = q.device
@@ -451,10 +459,17 @@ def kdn_dense_forward(q, k, v, log_alpha, omega, r, S0=None, P0=None, *, out=Non
         _check(o, "o", iot, (B, T, H, d), device)
         _check(S_T, "S_T", torch.float32, (B, H, d, d), device)
         _check(P_T, "P_T", torch.float32, (B, H, d, d), device)
+    need = lib.kdn_dense_workspace_size(B, T, H, d, io)
+    if need == 0:
+        raise KDNError(6, "kdn_dense_workspace_size rejected the arguments")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds {workspace.numel()} bytes, {need} needed")
     with torch.cuda.device(device):
         st = lib.kdn_dense_forward(B, T, H, d, io, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(omega),
-                                   _ptr(r), _ptr(S0), _ptr(P0), _ptr(o), _ptr(S_T), _ptr(P_T),
-                                   _stream(stream, device))
+                                   _ptr(r), _ptr(S0), _ptr(P0), _ptr(o), _ptr(S_T), _ptr(P_T), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream, device))
     if st != 0:
         raise KDNError(st, "kdn_dense_forward")
     return o, S_T, P_T

@@ -434,10 +434,17 @@ kdn_status kdn_pkda_step(int B, int H, int dk, int dv, float x, int io_dtype, co
                      PkdaInputs{beta, alpha_p, beta_p, center, x}, 0u);
 }
 
+size_t kdn_dense_workspace_size(int B, int T, int H, int d, int io_dtype) {
+    if (io_dtype != KDN_F32 && io_dtype != KDN_BF16) return 0;
+    if (B < 0 || T < 0 || H < 0 || (d != 32 && d != 64 && d != 128)) return 0;
+    if ((double)B * (double)T * (double)H * 128.0 > 1.0e12 || (double)B * (double)H > 2.0e9) return 0;
+    return kStatusBytes + align_up(sizeof(float) * (size_t)B * T * H * d);
+}
+
 kdn_status kdn_dense_forward(int B, int T, int H, int d, int io_dtype, const void* q, const void* k,
                              const void* v, const float* log_alpha, const float* omega, const float* r,
                              const float* S0, const float* P0, void* o, float* S_T, float* P_T,
-                             kdn_stream_t stream) {
+                             void* workspace, size_t workspace_bytes, kdn_stream_t stream) {
     if (io_dtype != KDN_F32 && io_dtype != KDN_BF16) return KDN_ERR_DTYPE;
     if (B < 0 || T < 0 || H < 0) return KDN_ERR_SHAPE;
     if (d != 32 && d != 64 && d != 128) return KDN_ERR_UNSUPPORTED;
@@ -446,28 +453,60 @@ kdn_status kdn_dense_forward(int B, int T, int H, int d, int io_dtype, const voi
     const size_t BH = (size_t)B * H, ntok = (size_t)B * T * H, esz = io_dtype == KDN_BF16 ? 2 : 4;
     if (BH > 0 && (!S_T || !P_T)) return KDN_ERR_NULL;
     if (ntok > 0 && (!q || !k || !v || !log_alpha || !omega || !r || !o)) return KDN_ERR_NULL;
-    const void* ptrs[] = {q, k, v, log_alpha, omega, r, S0, P0, o, S_T, P_T};
+    if (!workspace) return KDN_ERR_WORKSPACE;
+    const void* ptrs[] = {q, k, v, log_alpha, omega, r, S0, P0, o, S_T, P_T, workspace};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return KDN_ERR_ALIGN;
+    const size_t need = kdn_dense_workspace_size(B, T, H, d, io_dtype);
+    if (workspace_bytes < need) return KDN_ERR_WORKSPACE;
     const size_t nd = ntok * d, ns = BH * d * d;
     const Range in[] = {{q, nd * esz}, {k, nd * esz}, {v, nd * esz}, {log_alpha, nd * 4},
                         {omega, nd * 4}, {r, ntok * 4}, {S0, ns * 4}, {P0, ns * 4}};
-    const Range ro = {o, nd * esz}, rs = {S_T, ns * 4}, rp = {P_T, ns * 4};
+    const Range ro = {o, nd * esz}, rs = {S_T, ns * 4}, rp = {P_T, ns * 4}, rw = {workspace, need};
     for (const Range& x : in) {
-        if (overlaps(ro, x)) return KDN_ERR_ALIAS;
+        if (overlaps(ro, x) || overlaps(rw, x)) return KDN_ERR_ALIAS;
         if (x.p != S0 && overlaps(rs, x)) return KDN_ERR_ALIAS;
         if (x.p != P0 && overlaps(rp, x)) return KDN_ERR_ALIAS;
     }
-    if (overlaps(ro, rs) || overlaps(ro, rp) || overlaps(rs, rp)) return KDN_ERR_ALIAS;
+    if (overlaps(ro, rs) || overlaps(ro, rp) || overlaps(rs, rp) || overlaps(rw, ro) || overlaps(rw, rs) ||
+        overlaps(rw, rp))
+        return KDN_ERR_ALIAS;
     if (S0 && S0 != (const float*)S_T && overlaps(rs, Range{S0, ns * 4})) return KDN_ERR_ALIAS;
     if (P0 && P0 != (const float*)P_T && overlaps(rp, Range{P0, ns * 4})) return KDN_ERR_ALIAS;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t* status = static_cast<uint32_t*>(workspace);
+    if (cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess) return KDN_ERR_CUDA;
     if (BH == 0) return KDN_OK;
+    float* kappa = reinterpret_cast<float*>(static_cast<char*>(workspace) + kStatusBytes);
+
+    // (1) the covariance recurrence, token by token: kappa and P_T
     kdn::DenseArgs a;
     a.B = B; a.T = T; a.H = H; a.d = d; a.io = io_dtype;
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.omega = omega; a.r = r;
     a.S0 = S0; a.P0 = P0; a.o = o; a.S_T = S_T; a.P_T = P_T;
-    return kdn::launch_dense_forward(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KDN_OK
-                                                                                              : KDN_ERR_CUDA;
+    if (kdn::launch_dense_covariance(a, kappa, s) != cudaSuccess) return KDN_ERR_CUDA;
+    // (2) the mean with the gains given
+    if (T == 0) {
+        cudaError_t e = S0 ? (S0 == (const float*)S_T ? cudaSuccess
+                                                        : cudaMemcpyAsync(S_T, S0, ns * 4, cudaMemcpyDeviceToDevice, s))
+                           : cudaMemsetAsync(S_T, 0, ns * 4, s);
+        return e == cudaSuccess ? KDN_OK : KDN_ERR_CUDA;
+    }
+    kdn::ForwardArgs f;
+    memset(&f, 0, sizeof(f));
+    f.B = B; f.T = T; f.H = H; f.dk = d; f.dv = d; f.io = io_dtype;
+    f.chunk = resolve_chunk(0, T);
+    f.q = q; f.k = k; f.v = v; f.log_alpha = log_alpha; f.omega = kappa;
+    f.S0 = S0; f.o = o; f.S_T = S_T; f.status = status;
+    cudaError_t e;
+    if (use_tc_path(io_dtype, d, d, f.chunk, 0)) {
+        f.variant = 3;   // the fused kernel's given-gains instance (whole sequences)
+        e = kdn::launch_forward_tc(f, kdn::TcSplit{}, s);
+    } else {
+        f.variant = KDN_DIAG;   // (the chunk pass reads only the gains)
+        e = kdn::launch_chunk_simt(f, kappa, s);
+    }
+    return e == cudaSuccess ? KDN_OK : KDN_ERR_CUDA;
 }
 
 }  // extern "C"
@@ -623,6 +662,6 @@ const char* kdn_status_string(int status) {
     }
 }
 
-int kdn_abi_version(void) { return 105; }
+int kdn_abi_version(void) { return 106; }
 
 }  // extern "C"

@@ -163,9 +163,11 @@ struct TcParams {
     float* beta_eff;      // KDN, whole sequences: effective write strength [B,T,H], or null
 };
 
-// Kernel variants: the two KDN uncertainty models and the preconditioned delta
-// rule with per-channel decay.
-constexpr int kVarDiag = 0, kVarIso = 1, kVarPkda = 2;
+// Kernel variants: the two KDN uncertainty models, the preconditioned delta
+// rule with per-channel decay, and the memory pass with given gains (the
+// dense-covariance filter's mean: S = diag(a) S + kappa (v - (diag(a) S)^T k)^T
+// with kappa read from global memory, a unit-diagonal triangular system).
+constexpr int kVarDiag = 0, kVarIso = 1, kVarPkda = 2, kVarGiven = 3;
 // PKDA: the statistic enters the logarithm no smaller than this.
 constexpr float kStatFloor = 1e-20f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -378,6 +380,8 @@ __device__ __noinline__ void strong_decay_factors(const TcParams& P, unsigned ch
             }
         } else if (ISO) {
             kp = ex2(R2 - gg);
+        } else if (V == kVarGiven) {
+            kp = (t < nvc ? P.om[e] : 0.0f) * ex2(R2 - gg);
         } else {
             const float A = fmaf(sm[SM_OMI + t], sts, sm[SM_MUR + t] * kx * kx);
             sts = A;
@@ -394,7 +398,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     // MODE 0: whole sequences; 1: segments of a split sequence; 2: segments with the
     // values read as zero (a segment's transition map; no v copies)
     constexpr bool SEG = MODE != 0, NOV = MODE == 2;
-    constexpr bool ISO = V == kVarIso, PK = V == kVarPkda;
+    constexpr bool ISO = V == kVarIso, PK = V == kVarPkda, GK = V == kVarGiven;
+    static_assert(!GK || MODE == 0, "given gains: whole sequences");
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_addr(base);
@@ -439,8 +444,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         const int t0 = n * kC;
         mbar_expect_tx(bar_la, 32768u);
         tma_load_4d(sb + OFF_LA, &P.tla, 0, h, tb + t0, b, bar_la);
-        mbar_expect_tx(bar_ko, V == kVarDiag ? 49152u : 16384u);
-        if (V == kVarDiag) tma_load_4d(sb + OFF_OM, &P.tom, 0, h, tb + t0, b, bar_ko);
+        // (diagonal: omega; given gains: kappa, into the omega tile)
+        mbar_expect_tx(bar_ko, (V == kVarDiag || GK) ? 49152u : 16384u);
+        if (V == kVarDiag || GK) tma_load_4d(sb + OFF_OM, &P.tom, 0, h, tb + t0, b, bar_ko);
         tma_load_4d(sb + OFF_KIN, &P.tk, 0, h, tb + t0, b, bar_ko);
         tma_load_4d(sb + OFF_KIN + 8192, &P.tk, 64, h, tb + t0, b, bar_ko);
         mbar_expect_tx(bar_q, 16384u);
@@ -557,7 +563,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 sm[SM_R + t] = be;
                 sm[SM_MUR + t] = bp;
                 sm[SM_OMI + t] = ap;
-            } else {
+            } else if (!GK) {
                 float rr = 1.0f, om = 0.0f;
                 if (t < nvc) {
                     const size_t th = (static_cast<size_t>(b) * Tall + tb + t0c + t) * H + h;
@@ -598,7 +604,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     const int t = tb + u;
                     la[u] = LA[t * kD + i];
                     kv[u] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(kin + sw128_off(t, kch)));
-                    om[u] = V == kVarDiag ? OM[t * kD + i] : 0.0f;
+                    om[u] = (V == kVarDiag || GK) ? OM[t * kD + i] : 0.0f;
                 }
 #pragma unroll
                 for (int u4 = 0; u4 < kGB / 4; ++u4) {
@@ -652,6 +658,20 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                         const float2 ex = ffma2(sg, make_float2(P.neg_log2x, P.neg_log2x), make_float2(-gr0, -gr1));
                         OM[t * kD + i] = be[u] * ex2(ex.x);
                         OM[(t + 1) * kD + i] = be[u + 1] * ex2(ex.y);
+                    }
+                } else if (GK) {
+                    // given gains: decay factors, and kappa / e1 over kappa in place
+#pragma unroll
+                    for (int u = 0; u < kGB; u += 2) {
+                        const int t = tb + u;
+                        const float2 l2 = fmul2(make_float2(la[u], la[u + 1]), make_float2(kLog2e, kLog2e));
+                        g2 = fadd2(g2, l2);
+                        e1 *= ex2(l2.x);
+                        LA[t * kD + i] = e1;
+                        OM[t * kD + i] = om[u] * rcp_approx(e1);
+                        e1 *= ex2(l2.y);
+                        LA[(t + 1) * kD + i] = e1;
+                        OM[(t + 1) * kD + i] = om[u + 1] * rcp_approx(e1);
                     }
                 } else if (!ISO) {
 #pragma unroll
@@ -921,7 +941,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     const uint2 kr = *reinterpret_cast<const uint2*>(base + OFF_KIN + a * 8192 + sw);
                     const uint2 qr = *reinterpret_cast<const uint2*>(base + OFF_QIN + a * 8192 + sw);
                     const float4 e = *reinterpret_cast<const float4*>(LA + t * kD + 64 * a + 4 * g);
-                    // p_hat / e1 (PKDA: write scale / e1), formed by warps 4-7; isotropic: 1 / e1
+                    // p_hat / e1 (PKDA: write scale / e1; given gains: kappa / e1), formed by
+                    // warps 4-7; isotropic: 1 / e1
                     float4 kp;
                     if (ISO) {
                         kp = make_float4(rcp_approx(e.x), rcp_approx(e.y), rcp_approx(e.z), rcp_approx(e.w));
@@ -937,10 +958,11 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                     qb[4 * a + 1] = bf_hi(qr.x) * e.y;
                     qb[4 * a + 2] = bf_lo(qr.y) * e.z;
                     qb[4 * a + 3] = bf_hi(qr.y) * e.w;
-                    kt[4 * a + 0] = k0 * kp.x;
-                    kt[4 * a + 1] = k1 * kp.y;
-                    kt[4 * a + 2] = k2 * kp.z;
-                    kt[4 * a + 3] = k3 * kp.w;
+                    // (given gains: the tile holds kappa / e1, the write key itself)
+                    kt[4 * a + 0] = GK ? kp.x : k0 * kp.x;
+                    kt[4 * a + 1] = GK ? kp.y : k1 * kp.y;
+                    kt[4 * a + 2] = GK ? kp.z : k2 * kp.z;
+                    kt[4 * a + 3] = GK ? kp.w : k3 * kp.w;
                 }
 #pragma unroll
                 for (int a = 0; a < 2; ++a) {
@@ -1003,7 +1025,7 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                                         __uint_as_float(s + 2 < 32 ? v0[s + 2] : v1[s + 2 - 32]),
                                         __uint_as_float(s + 3 < 32 ? v0[s + 3] : v1[s + 3 - 32]));
                     }
-                    if (PK) {
+                    if (PK || GK) {
                         row[lt] = 1.0f;
                         sm[SM_INVD + lt] = 1.0f;
                     } else {
@@ -1361,9 +1383,10 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStrea
               encode_4d(&P.tk, a.k, BF, 2, a.B, a.T, a.H, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
               encode_4d(&P.tv, a.v, BF, 2, a.B, a.T, a.H, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
               encode_4d(&P.tla, a.log_alpha, F32, 4, a.B, a.T, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (ok && a.variant == kVarDiag)
+    if (ok && (a.variant == kVarDiag || a.variant == kVarGiven))   // omega, or the given kappa
         ok = encode_4d(&P.tom, a.omega, F32, 4, a.B, a.T, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return cudaErrorInvalidValue;
+    if (a.variant == kVarGiven && sp.nseg > 1) return cudaErrorInvalidValue;   // whole sequences only
     P.r = a.r;
     P.la = a.log_alpha;
     P.om = a.omega;
@@ -1390,7 +1413,7 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStrea
     P.probe = (a.flags & KDN_FLAG_TIMEOUT_PROBE) ? 1 : 0;
     // (the split path never writes the effective write strength: its callers keep
     //  one CTA per sequence when they want it)
-    P.beta_eff = (sp.nseg > 1 || a.variant == kVarPkda) ? nullptr : a.beta_eff;
+    P.beta_eff = (sp.nseg > 1 || a.variant == kVarPkda || a.variant == kVarGiven) ? nullptr : a.beta_eff;
     int grid = a.B * a.H;
     auto launch = [&](auto kernel) {
         const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
@@ -1401,6 +1424,7 @@ cudaError_t launch_forward_tc(const ForwardArgs& a, const TcSplit& sp, cudaStrea
     // kernel instance: whole sequences, segments, or segments without values
     auto run = [&]() {
         if (P.nseg <= 1) {
+            if (a.variant == kVarGiven) return launch(kdn_fused_tc_kernel<kVarGiven, 0>);
             if (a.variant == kVarDiag) return launch(kdn_fused_tc_kernel<kVarDiag, 0>);
             if (a.variant == kVarIso) return launch(kdn_fused_tc_kernel<kVarIso, 0>);
             return launch(kdn_fused_tc_kernel<kVarPkda, 0>);

@@ -102,7 +102,7 @@ int tc_kernel_count(int nseg);
 cudaError_t launch_segment_states(const ForwardArgs& a, const TcSplit& sp, cudaStream_t s);
 cudaError_t launch_segment_correction(const ForwardArgs& a, const TcSplit& sp, cudaStream_t s);
 
-// Dense-covariance (exact) Kalman memory forward, token by token.  dense.cu
+// Dense-covariance (exact) Kalman memory forward.
 struct DenseArgs {
     int B, T, H, d, io;
     const void *q, *k, *v;
@@ -110,7 +110,8 @@ struct DenseArgs {
     void* o;
     float *S_T, *P_T;
 };
-cudaError_t launch_dense_forward(const DenseArgs& a, cudaStream_t s);
+// The covariance recurrence token by token: kappa [B,T,H,d] fp32 and P_T.  dense.cu
+cudaError_t launch_dense_covariance(const DenseArgs& a, float* kappa, cudaStream_t s);
 
 // Copy the initial state to the outputs (T == 0).  chunk_simt.cu
 cudaError_t launch_state_copy(const ForwardArgs& a, cudaStream_t s);
