@@ -43,48 +43,91 @@ constexpr int kBC = 16;       // tokens per chunk of the memory adjoint
 constexpr int kMNT = 256;     // threads of the memory adjoint
 constexpr int kPB = 64;       // tokens per checkpoint block of the gain adjoint
 constexpr int kEl = kBC * 128 / kMNT;        // elements of a [kBC][d] tile per thread (d <= 128)
-constexpr int kS4 = 128 * 128 / 4 / kMNT;    // 16-byte groups of a [dk][dv] state per thread
 
 // C(r, c) (+)= alpha sum_k A(r, k) B(k, c) on shared-memory operands with arbitrary
-// strides: A(r, k) = A[r ar + k ak], B(k, c) = B[k bk + c bc], C(r, c) = C[r cr + c].
-// A warp computes TR rows x 32 TCH columns at a time (lane = column within a group
-// of 32); every thread of the block takes part.
-template <int TR, int TCH>
+// strides: A(r, k) = A[r ar + k ak], B(k, c) = B[k bk + c bc], C(r, c) = C[r cr + c];
+// R a multiple of 16, N of 8 NT, K of 8.  Warp-level m16n8k8 TF32 tensor-core MMAs
+// (fp32 accumulation) in the 3xTF32 split: each operand x = hi + lo with hi and lo
+// TF32 (round to nearest), and the product takes lo*hi + hi*lo + hi*hi, which keeps
+// fp32-level accuracy (the dropped lo*lo term is below 2^-22 of the product).  A warp
+// computes one 16-row tile of NT 8-column tiles at a time; every warp of the block
+// takes part.  Fragment layouts (m16n8k8, A row-major, B column-major): lane = 4 g + q;
+// A: (g, q), (g + 8, q), (g, q + 4), (g + 8, q + 4); B: (k = q, n = g), (k = q + 4, n = g);
+// C: (g, 2 q), (g, 2 q + 1), (g + 8, 2 q), (g + 8, 2 q + 1).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = to_tf32(x);
+    lo = to_tf32(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_m16n8k8_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only), or 16 zero bytes when !valid
+// (no global read then); completion by cp_async_wait_all() and a barrier.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, bool valid) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gsrc), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+template <int NT>
 __device__ void smem_gemm(int R, int N, int K, const float* A, int ar, int ak, const float* B, int bk, int bc,
                           float* C, int cr, float alpha, bool accumulate) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int nrb = (R + TR - 1) / TR, ncb = (N + 32 * TCH - 1) / (32 * TCH);
-    for (int u = warp; u < nrb * ncb; u += nw) {
-        const int r0 = (u / ncb) * TR, c0 = (u % ncb) * 32 * TCH;
-        float acc[TR][TCH];
+    const int g = lane >> 2, q = lane & 3;
+    const int nrt = R / 16, nct = N / (8 * NT);
+    for (int u = warp; u < nrt * nct; u += nw) {
+        const int r0 = (u / nct) * 16, c0 = (u % nct) * 8 * NT;
+        float acc[NT][4];
 #pragma unroll
-        for (int r = 0; r < TR; ++r)
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
-            for (int m = 0; m < TCH; ++m) acc[r][m] = 0.f;
-        for (int k = 0; k < K; ++k) {
-            float a[TR], bv[TCH];
+            for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+        const float* ap = A + (r0 + g) * ar + q * ak;
+        for (int k0 = 0; k0 < K; k0 += 8) {
+            uint32_t ah[4], al[4];
+            split_tf32(ap[k0 * ak], ah[0], al[0]);
+            split_tf32(ap[8 * ar + k0 * ak], ah[1], al[1]);
+            split_tf32(ap[(k0 + 4) * ak], ah[2], al[2]);
+            split_tf32(ap[8 * ar + (k0 + 4) * ak], ah[3], al[3]);
 #pragma unroll
-            for (int r = 0; r < TR; ++r) a[r] = (r0 + r < R) ? A[(r0 + r) * ar + k * ak] : 0.f;
-#pragma unroll
-            for (int m = 0; m < TCH; ++m) {
-                const int c = c0 + 32 * m + lane;
-                bv[m] = c < N ? B[k * bk + c * bc] : 0.f;
+            for (int n = 0; n < NT; ++n) {
+                const float* bp = B + (k0 + q) * bk + (c0 + 8 * n + g) * bc;
+                uint32_t bh0, bl0, bh1, bl1;
+                split_tf32(bp[0], bh0, bl0);
+                split_tf32(bp[4 * bk], bh1, bl1);
+                mma_m16n8k8_tf32(acc[n], al, bh0, bh1);
+                mma_m16n8k8_tf32(acc[n], ah, bl0, bl1);
+                mma_m16n8k8_tf32(acc[n], ah, bh0, bh1);
             }
-#pragma unroll
-            for (int r = 0; r < TR; ++r)
-#pragma unroll
-                for (int m = 0; m < TCH; ++m) acc[r][m] = fmaf(a[r], bv[m], acc[r][m]);
         }
 #pragma unroll
-        for (int r = 0; r < TR; ++r)
-#pragma unroll
-            for (int m = 0; m < TCH; ++m) {
-                const int c = c0 + 32 * m + lane;
-                if (r0 + r < R && c < N) {
-                    float* d = C + (r0 + r) * cr + c;
-                    *d = accumulate ? fmaf(alpha, acc[r][m], *d) : alpha * acc[r][m];
-                }
+        for (int n = 0; n < NT; ++n) {
+            float* d0 = C + (r0 + g) * cr + c0 + 8 * n + 2 * q;
+            float* d1 = d0 + 8 * cr;
+            if (accumulate) {
+                d0[0] = fmaf(alpha, acc[n][0], d0[0]);
+                d0[1] = fmaf(alpha, acc[n][1], d0[1]);
+                d1[0] = fmaf(alpha, acc[n][2], d1[0]);
+                d1[1] = fmaf(alpha, acc[n][3], d1[1]);
+            } else {
+                d0[0] = alpha * acc[n][0];
+                d0[1] = alpha * acc[n][1];
+                d1[0] = alpha * acc[n][2];
+                d1[1] = alpha * acc[n][3];
             }
+        }
     }
 }
 
@@ -97,14 +140,18 @@ struct MemArgs {
     uint32_t* status;
 };
 
+// Rows of the d-wide operands are padded to d + 4 words: the MMA fragment loads (lane
+// 4 g + q reading word g * ld + q, or q * ld + g) then meet at most 2-way bank conflicts.
+constexpr int kRowPad = 4;
+
 size_t mem_smem_floats(int DK, int DV) {
-    const int LSK = DK + 1, LSV = DV + 1, LCC = kBC + 1;
+    const int LSK = DK + kRowPad, LSV = DV + kRowPad, LCC = kBC + 1;
     return (size_t)2 * DK * LSV + 7 * kBC * LSK + 3 * kBC * LSV + 4 * kBC * LCC + 4 * DK;
 }
 
 template <typename TIO>
-__global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
-    const int DK = P.DK, DV = P.DV, LSK = DK + 1, LSV = DV + 1, LCC = kBC + 1;
+__global__ void __launch_bounds__(kMNT, 1) mem_adjoint_kernel(const MemArgs P) {
+    const int DK = P.DK, DV = P.DV, LSK = DK + kRowPad, LSV = DV + kRowPad, LCC = kBC + 1;
     extern __shared__ float sm[];
     float* Sm = sm;                    // [DK][LSV] chunk-start state, then S_m
     float* dS = Sm + DK * LSV;         // [DK][LSV] gradient of the chunk's end state
@@ -133,21 +180,48 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
     float* ck = P.ckpt + (size_t)bh * (nch + 1) * sdd;
     auto row = [&](int t) { return ((size_t)b * T + t) * H + h; };   // token-head index
 
+    // row-wise passes over a [DK][LSV] state tile: a warp per row, 16-byte accesses
+    // (LSV and DV are multiples of 4), no index division
+    auto scale_rows = [&](float* M, const float* f) {   // M(i, :) *= f[i]
+        for (int ri = tid >> 5; ri < DK; ri += kMNT / 32) {
+            const float sc = f[ri];
+            float4* m4 = reinterpret_cast<float4*>(M + ri * LSV);
+            for (int j4 = tid & 31; j4 < DV / 4; j4 += 32) {
+                float4 v = m4[j4];
+                v.x *= sc; v.y *= sc; v.z *= sc; v.w *= sc;
+                m4[j4] = v;
+            }
+        }
+    };
+    auto store_state = [&](float* dst) {   // dst[i][j] (dense [DK][DV]) = Sm(i, j)
+        for (int ri = tid >> 5; ri < DK; ri += kMNT / 32) {
+            const float4* m4 = reinterpret_cast<const float4*>(Sm + ri * LSV);
+            float4* d4 = reinterpret_cast<float4*>(dst + (size_t)ri * DV);
+            for (int j4 = tid & 31; j4 < DV / 4; j4 += 32) d4[j4] = m4[j4];
+        }
+    };
+
     // per-chunk setup: cumulative log-decay G, reference and factors; the operands
     // K_bar, Q_bar, K_til; S_m = diag(g_in) S_0 with S_0 in Sm.  The chunk's inputs are
     // read into registers by one batch of loads per thread before any of them is used.
     auto setup = [&](int n, int nv) {
         const int t0 = n * kBC;
-        float rla[kEl], rk[kEl], rq[kEl], rkap[kEl], rv[kEl];
+        // log_alpha -> Gc and kappa -> Kt by 16-byte async copies (rows past the
+        // sequence end zero-filled); k, q, v through registers
+        for (int e4 = tid; e4 < kBC * DK / 4; e4 += kMNT) {
+            const int t = (4 * e4) / DK, i = (4 * e4) % DK;
+            const size_t gi = row(t0 + min(t, nv - 1)) * DK + i;
+            cp_async16(Gc + t * LSK + i, P.la + gi, t < nv);
+            cp_async16(Kt + t * LSK + i, P.kappa + gi, t < nv);
+        }
+        float rk[kEl], rq[kEl], rv[kEl];
 #pragma unroll
         for (int m = 0; m < kEl; ++m) {
             const int e = tid + m * kMNT, t = e / DK, i = e % DK;
             const bool ok = e < kBC * DK && t < nv;
             const size_t gi = row(t0 + min(t, kBC - 1)) * DK + i;
-            rla[m] = ok ? P.la[gi] : 0.f;
             rk[m] = ok ? IO<TIO>::load(static_cast<const TIO*>(P.k), gi) : 0.f;
             rq[m] = ok ? IO<TIO>::load(static_cast<const TIO*>(P.q), gi) : 0.f;
-            rkap[m] = ok ? P.kappa[gi] : 0.f;
             const int tv = e / DV, j = e % DV;
             const bool okv = e < kBC * DV && tv < nv;
             rv[m] = okv ? IO<TIO>::load(static_cast<const TIO*>(P.v), row(t0 + min(tv, kBC - 1)) * DV + j) : 0.f;
@@ -155,9 +229,9 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
 #pragma unroll
         for (int m = 0; m < kEl; ++m) {
             const int e = tid + m * kMNT;
-            if (e < kBC * DK) Gc[(e / DK) * LSK + e % DK] = rla[m];
             if (e < kBC * DV) X[(e / DV) * LSV + e % DV] = rv[m];
         }
+        cp_async_wait_all();
         __syncthreads();
         if (tid < DK) {
             float g = 0.f;
@@ -179,18 +253,15 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
                 const float ef = expf(Gc[t * LSK + i] - gref[i]);
                 Kb[t * LSK + i] = rk[m] * ef;
                 Qb[t * LSK + i] = rq[m] * ef;
-                Kt[t * LSK + i] = rkap[m] / ef;
+                Kt[t * LSK + i] /= ef;   // kappa e^{-(G_t - G_ref)}
             }
         }
-        for (int e = tid; e < DK * DV; e += kMNT) {
-            const int i = e / DV, j = e % DV;
-            Sm[i * LSV + j] *= gin[i];
-        }
+        scale_rows(Sm, gin);
         __syncthreads();
         // L = strict_lower(K_bar K_til^T), A = lower_incl(Q_bar K_til^T), X = V - K_bar S_m
-        smem_gemm<1, 1>(kBC, kBC, DK, Kb, LSK, 1, Kt, 1, LSK, L, LCC, 1.f, false);
-        smem_gemm<1, 1>(kBC, kBC, DK, Qb, LSK, 1, Kt, 1, LSK, Am, LCC, 1.f, false);
-        smem_gemm<2, 4>(kBC, DV, DK, Kb, LSK, 1, Sm, LSV, 1, X, LSV, -1.f, true);
+        smem_gemm<1>(kBC, kBC, DK, Kb, LSK, 1, Kt, 1, LSK, L, LCC, 1.f, false);
+        smem_gemm<1>(kBC, kBC, DK, Qb, LSK, 1, Kt, 1, LSK, Am, LCC, 1.f, false);
+        smem_gemm<2>(kBC, DV, DK, Kb, LSK, 1, Sm, LSV, 1, X, LSV, -1.f, true);
         __syncthreads();
         for (int e = tid; e < kBC * kBC; e += kMNT) {
             const int t = e / kBC, s = e % kBC;
@@ -198,39 +269,29 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
             if (s > t) Am[t * LCC + s] = 0.f;
         }
         __syncthreads();
-        // forward substitution (I + L) Delta = X: a thread per value column, which it
-        // alone reads and writes (no barrier between rows)
+        // forward substitution (I + L) Delta = X: a thread per value column, held in
+        // registers, which it alone reads and writes (no barrier between rows)
         for (int j = tid; j < DV; j += kMNT) {
-            for (int t = 1; t < nv; ++t) {
-                float acc = X[t * LSV + j];
-                for (int s = 0; s < t; ++s) acc = fmaf(-L[t * LCC + s], X[s * LSV + j], acc);
-                X[t * LSV + j] = acc;
+            float x[kBC];
+#pragma unroll
+            for (int t = 0; t < kBC; ++t) x[t] = X[t * LSV + j];
+#pragma unroll
+            for (int t = 1; t < kBC; ++t) {
+                if (t < nv) {
+#pragma unroll
+                    for (int s = 0; s < t; ++s) x[t] = fmaf(-L[t * LCC + s], x[s], x[t]);
+                }
             }
+#pragma unroll
+            for (int t = 0; t < kBC; ++t) X[t * LSV + j] = x[t];
         }
         __syncthreads();
     };
-    // a checkpointed state into Sm: one batch of 16-byte loads per thread, then the
-    // shared-memory stores
+    // a checkpointed state into Sm: 16-byte async copies, all in flight together (the
+    // caller waits and synchronises)
     auto load_state = [&](const float* src) {
-        const float4* s4 = reinterpret_cast<const float4*>(src);
-        const int n4 = DK * DV / 4;
-        float4 r4[kS4];
-#pragma unroll
-        for (int m = 0; m < kS4; ++m) {
-            const int e4 = tid + m * kMNT;
-            r4[m] = e4 < n4 ? s4[e4] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int m = 0; m < kS4; ++m) {
-            const int e4 = tid + m * kMNT;
-            if (e4 < n4) {
-                float* d = Sm + ((4 * e4) / DV) * LSV + (4 * e4) % DV;
-                d[0] = r4[m].x;
-                d[1] = r4[m].y;
-                d[2] = r4[m].z;
-                d[3] = r4[m].w;
-            }
-        }
+        for (int e4 = tid; e4 < DK * DV / 4; e4 += kMNT)
+            cp_async16(Sm + ((4 * e4) / DV) * LSV + (4 * e4) % DV, src + 4 * e4, true);
     };
 
     // ---- forward sweep: the state at every chunk start
@@ -241,18 +302,15 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
     __syncthreads();
     for (int n = 0; n < nch; ++n) {
         const int nv = min(kBC, T - n * kBC);
-        for (int e = tid; e < DK * DV; e += kMNT) ck[(size_t)n * sdd + e] = Sm[(e / DV) * LSV + e % DV];
+        store_state(ck + (size_t)n * sdd);
         setup(n, nv);
         // S_out = diag(g_out) (S_m + K_til^T Delta)
-        smem_gemm<2, 4>(DK, DV, kBC, Kt, 1, LSK, X, LSV, 1, Sm, LSV, 1.f, true);
+        smem_gemm<2>(DK, DV, kBC, Kt, 1, LSK, X, LSV, 1, Sm, LSV, 1.f, true);
         __syncthreads();
-        for (int e = tid; e < DK * DV; e += kMNT) {
-            const int i = e / DV, j = e % DV;
-            Sm[i * LSV + j] *= gout[i];
-        }
+        scale_rows(Sm, gout);
         __syncthreads();
     }
-    for (int e = tid; e < DK * DV; e += kMNT) ck[(size_t)nch * sdd + e] = Sm[(e / DV) * LSV + e % DV];
+    store_state(ck + (size_t)nch * sdd);
     __syncthreads();
 
     // ---- reverse sweep
@@ -274,7 +332,7 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
     for (int n = nch - 1; n >= 0; --n) {
         const int t0 = n * kBC, nv = min(kBC, T - t0);
         __syncthreads();
-        load_state(ck + (size_t)n * sdd);
+        load_state(ck + (size_t)n * sdd);   // (completed below, before the barrier)
         float rdo[kEl];
 #pragma unroll
         for (int m = 0; m < kEl; ++m) {
@@ -287,37 +345,41 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
             const int e = tid + m * kMNT;
             if (e < kBC * DV) dO[(e / DV) * LSV + e % DV] = rdo[m];
         }
+        cp_async_wait_all();
         __syncthreads();
         setup(n, nv);   // Sm = S_m, X = Delta, operands, L, A
-        for (int e = tid; e < DK * DV; e += kMNT) {   // Gp = diag(g_out) dS_out
-            const int i = e / DV, j = e % DV;
-            dS[i * LSV + j] *= gout[i];
-        }
+        scale_rows(dS, gout);   // Gp = diag(g_out) dS_out
         __syncthreads();
         // dDelta = K_til Gp + A^T dO;  dK_til = Delta Gp^T;  dQ_bar = dO S_m^T;  dA = dO Delta^T
-        smem_gemm<2, 4>(kBC, DV, DK, Kt, LSK, 1, dS, LSV, 1, dX, LSV, 1.f, false);
-        smem_gemm<2, 4>(kBC, DK, DV, X, LSV, 1, dS, 1, LSV, dKt, LSK, 1.f, false);
-        smem_gemm<2, 4>(kBC, DK, DV, dO, LSV, 1, Sm, 1, LSV, dQb, LSK, 1.f, false);
-        smem_gemm<1, 1>(kBC, kBC, DV, dO, LSV, 1, X, 1, LSV, dA, LCC, 1.f, false);
+        smem_gemm<2>(kBC, DV, DK, Kt, LSK, 1, dS, LSV, 1, dX, LSV, 1.f, false);
+        smem_gemm<2>(kBC, DK, DV, X, LSV, 1, dS, 1, LSV, dKt, LSK, 1.f, false);
+        smem_gemm<2>(kBC, DK, DV, dO, LSV, 1, Sm, 1, LSV, dQb, LSK, 1.f, false);
+        smem_gemm<1>(kBC, kBC, DV, dO, LSV, 1, X, 1, LSV, dA, LCC, 1.f, false);
         __syncthreads();
-        smem_gemm<2, 4>(kBC, DV, kBC, Am, 1, LCC, dO, LSV, 1, dX, LSV, 1.f, true);
+        smem_gemm<2>(kBC, DV, kBC, Am, 1, LCC, dO, LSV, 1, dX, LSV, 1.f, true);
         for (int e = tid; e < kBC * kBC; e += kMNT) {
             const int t = e / kBC, s = e % kBC;
             if (s > t) dA[t * LCC + s] = 0.f;
         }
         __syncthreads();
-        // back substitution (I + L)^T dX = dDelta (a thread per value column)
+        // back substitution (I + L)^T dX = dDelta (a thread per value column, in registers;
+        // rows past the sequence end are zero in L)
         for (int j = tid; j < DV; j += kMNT) {
-            for (int t = nv - 2; t >= 0; --t) {
-                float acc = dX[t * LSV + j];
-                for (int s = t + 1; s < nv; ++s) acc = fmaf(-L[s * LCC + t], dX[s * LSV + j], acc);
-                dX[t * LSV + j] = acc;
+            float x[kBC];
+#pragma unroll
+            for (int t = 0; t < kBC; ++t) x[t] = dX[t * LSV + j];
+#pragma unroll
+            for (int t = kBC - 2; t >= 0; --t) {
+#pragma unroll
+                for (int s = t + 1; s < kBC; ++s) x[t] = fmaf(-L[s * LCC + t], x[s], x[t]);
             }
+#pragma unroll
+            for (int t = 0; t < kBC; ++t) dX[t * LSV + j] = x[t];
         }
         __syncthreads();
         // dL = strict_lower(-dX Delta^T); dK_bar = -dX S_m^T
-        smem_gemm<1, 1>(kBC, kBC, DV, dX, LSV, 1, X, 1, LSV, dL, LCC, -1.f, false);
-        smem_gemm<2, 4>(kBC, DK, DV, dX, LSV, 1, Sm, 1, LSV, dKb, LSK, -1.f, false);
+        smem_gemm<1>(kBC, kBC, DV, dX, LSV, 1, X, 1, LSV, dL, LCC, -1.f, false);
+        smem_gemm<2>(kBC, DK, DV, dX, LSV, 1, Sm, 1, LSV, dKb, LSK, -1.f, false);
         __syncthreads();
         for (int e = tid; e < kBC * kBC; e += kMNT) {
             const int t = e / kBC, s = e % kBC;
@@ -326,13 +388,13 @@ __global__ void __launch_bounds__(kMNT) mem_adjoint_kernel(const MemArgs P) {
         __syncthreads();
         // dK_bar += dL K_til; dK_til += dL^T K_bar + dA^T Q_bar; dQ_bar += dA K_til;
         // dS_m = Gp + Q_bar^T dO - K_bar^T dX
-        smem_gemm<2, 4>(kBC, DK, kBC, dL, LCC, 1, Kt, LSK, 1, dKb, LSK, 1.f, true);
-        smem_gemm<2, 4>(kBC, DK, kBC, dL, 1, LCC, Kb, LSK, 1, dKt, LSK, 1.f, true);
-        smem_gemm<2, 4>(kBC, DK, kBC, dA, LCC, 1, Kt, LSK, 1, dQb, LSK, 1.f, true);
-        smem_gemm<2, 4>(DK, DV, kBC, Qb, 1, LSK, dO, LSV, 1, dS, LSV, 1.f, true);
+        smem_gemm<2>(kBC, DK, kBC, dL, LCC, 1, Kt, LSK, 1, dKb, LSK, 1.f, true);
+        smem_gemm<2>(kBC, DK, kBC, dL, 1, LCC, Kb, LSK, 1, dKt, LSK, 1.f, true);
+        smem_gemm<2>(kBC, DK, kBC, dA, LCC, 1, Kt, LSK, 1, dQb, LSK, 1.f, true);
+        smem_gemm<2>(DK, DV, kBC, Qb, 1, LSK, dO, LSV, 1, dS, LSV, 1.f, true);
         __syncthreads();   // (the next two accumulate into dS and dK_til again)
-        smem_gemm<2, 4>(DK, DV, kBC, Kb, 1, LSK, dX, LSV, 1, dS, LSV, -1.f, true);
-        smem_gemm<2, 4>(kBC, DK, kBC, dA, 1, LCC, Qb, LSK, 1, dKt, LSK, 1.f, true);
+        smem_gemm<2>(DK, DV, kBC, Kb, 1, LSK, dX, LSV, 1, dS, LSV, -1.f, true);
+        smem_gemm<2>(kBC, DK, kBC, dA, 1, LCC, Qb, LSK, 1, dKt, LSK, 1.f, true);
         __syncthreads();
         // per-token gradients of the inputs; dS becomes the gradient of the chunk start
         for (int e = tid; e < kBC * DV; e += kMNT) {
