@@ -81,10 +81,12 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
+// (wofs rotates the units over the warps, so small products issued back to back
+//  without a barrier can land on different warps)
 template <int NT>
 __device__ void smem_gemm(int R, int N, int K, const float* A, int ar, int ak, const float* B, int bk, int bc,
-                          float* C, int cr, float alpha, bool accumulate) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+                          float* C, int cr, float alpha, bool accumulate, int wofs = 0) {
+    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5, warp = ((threadIdx.x >> 5) + wofs) % nw;
     const int g = lane >> 2, q = lane & 3;
     const int nrt = R / 16, nct = N / (8 * NT);
     for (int u = warp; u < nrt * nct; u += nw) {
@@ -254,13 +256,14 @@ __global__ void __launch_bounds__(kMNT, 1) mem_adjoint_kernel(const MemArgs P) {
                 Kb[t * LSK + i] = rk[m] * ef;
                 Qb[t * LSK + i] = rq[m] * ef;
                 Kt[t * LSK + i] /= ef;   // kappa e^{-(G_t - G_ref)}
+                Gc[t * LSK + i] = ef;    // (G itself is not needed again in the chunk)
             }
         }
         scale_rows(Sm, gin);
         __syncthreads();
         // L = strict_lower(K_bar K_til^T), A = lower_incl(Q_bar K_til^T), X = V - K_bar S_m
-        smem_gemm<1>(kBC, kBC, DK, Kb, LSK, 1, Kt, 1, LSK, L, LCC, 1.f, false);
-        smem_gemm<1>(kBC, kBC, DK, Qb, LSK, 1, Kt, 1, LSK, Am, LCC, 1.f, false);
+        smem_gemm<1>(kBC, kBC, DK, Kb, LSK, 1, Kt, 1, LSK, L, LCC, 1.f, false, 2);    // (warps 6-7)
+        smem_gemm<1>(kBC, kBC, DK, Qb, LSK, 1, Kt, 1, LSK, Am, LCC, 1.f, false, 4);   // (warps 4-5)
         smem_gemm<2>(kBC, DV, DK, Kb, LSK, 1, Sm, LSV, 1, X, LSV, -1.f, true);
         __syncthreads();
         for (int e = tid; e < kBC * kBC; e += kMNT) {
@@ -408,8 +411,8 @@ __global__ void __launch_bounds__(kMNT, 1) mem_adjoint_kernel(const MemArgs P) {
                 const size_t gi = row(t0 + t) * DK + i;
                 const float kb = Kb[t * LSK + i], qb = Qb[t * LSK + i], kt = Kt[t * LSK + i];
                 const float dkb = dKb[t * LSK + i], dqb = dQb[t * LSK + i], dkt = dKt[t * LSK + i];
-                // K_bar = k f, Q_bar = q f, K_til = kappa / f with f = exp(G_t - G_ref)
-                const float f = expf(Gc[t * LSK + i] - gref[i]);
+                // K_bar = k f, Q_bar = q f, K_til = kappa / f with f = exp(G_t - G_ref) (in Gc)
+                const float f = Gc[t * LSK + i];
                 P.dk[gi] = dkb * f;
                 P.dq[gi] = dqb * f;
                 P.dkappa[gi] = dkt / f;
