@@ -21,24 +21,31 @@
 //
 // One CTA owns one (b, h) and one slice of VS value columns (the columns are
 // independent given kappa) and walks the chunks in order, keeping its slice
-// of S in shared memory in fp32.  The triangular system is solved by forward
-// substitution.
+// of S in shared memory in fp32.  The products (Gram matrices, the state's
+// predictions and reads, the output and state updates) run as warp-level
+// m16n8k8 TF32 tensor-core MMAs in the 3xTF32 split, which keeps fp32-level
+// accuracy.  The triangular system is solved blockwise: each 16-row diagonal
+// block by substitution (a thread per value column, in registers), then the rows
+// below it updated by one product.
 
 #include "common.cuh"
 #include "kdn_internal.h"
+#include "mma_tf32x3.cuh"
 
 namespace kdn {
 namespace {
 
 constexpr int kNT = 256;
+constexpr int kPadW = 4;   // row padding (words) of the d-wide and VS-wide tiles
+constexpr int kSB = 16;    // rows of a diagonal block of the triangular solve
 
 template <typename TIO>
-__global__ void __launch_bounds__(kNT)
+__global__ void __launch_bounds__(kNT, 1)
 chunk_simt_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TIO* __restrict__ v,
                   const float* __restrict__ la, const float* __restrict__ kappa,
                   const float* __restrict__ S0, TIO* __restrict__ o, float* __restrict__ S_T,
                   int Tn, int H, int DK, int dv, int C, int VS, uint32_t* status) {
-    const int LD = DK + 1, LS = VS + 1, LC = C + 1;
+    const int LD = DK + kPadW, LS = VS + kPadW, LC = C + 1;
     extern __shared__ float sm[];
     float* Kb = sm;                 // [C][LD]
     float* Qb = Kb + C * LD;        // [C][LD]
@@ -51,6 +58,8 @@ chunk_simt_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TI
     float* gref = O + C * LS;       // [DK]
     float* gin = gref + DK;         // [DK] exp(G_ref)
     float* gout = gin + DK;         // [DK] exp(G_C - G_ref)
+    float* G = gout + DK;           // [C][DK] log_alpha, then the cumulative log-decay
+    // (every region starts on a 16-byte boundary: all sizes above are multiples of 4 words)
 
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const int j0 = blockIdx.y * VS;
@@ -64,12 +73,47 @@ chunk_simt_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TI
     const int nchunks = (Tn + C - 1) / C;
     for (int n = 0; n < nchunks; ++n) {
         const int t0 = n * C, nv = min(C, Tn - t0);
-        // 1. cumulative log-decay per channel
+        // 1. the chunk's inputs: log_alpha, kappa and, for fp32 inputs, k, q, v by 16-byte
+        //    async copies (rows past the sequence end zero-filled); bf16 k, q, v through
+        //    loads unrolled by eight
+        const size_t tok0 = ((size_t)b * Tn + t0) * H + h;   // token-head index of the chunk's first token
+        for (int e4 = tid; e4 < C * DK / 4; e4 += kNT) {
+            const int t = (4 * e4) / DK, i = (4 * e4) % DK;
+            const size_t gi = (tok0 + (size_t)min(t, nv - 1) * H) * DK + i;
+            cp_async16(G + t * DK + i, la + gi, t < nv);
+            cp_async16(Kt + t * LD + i, kappa + gi, t < nv);
+            if constexpr (sizeof(TIO) == 4) {
+                cp_async16(Kb + t * LD + i, k + gi, t < nv);
+                cp_async16(Qb + t * LD + i, q + gi, t < nv);
+            }
+        }
+        if constexpr (sizeof(TIO) == 4) {
+            for (int e4 = tid; e4 < C * VS / 4; e4 += kNT) {
+                const int t = (4 * e4) / VS, j = (4 * e4) % VS;
+                cp_async16(X + t * LS + j, v + (tok0 + (size_t)min(t, nv - 1) * H) * dv + j0 + j, t < nv);
+            }
+        } else {
+#pragma unroll 8
+            for (int e = tid; e < C * DK; e += kNT) {
+                const int t = e / DK, i = e % DK;
+                const size_t gi = (tok0 + (size_t)t * H) * DK + i;
+                Kb[t * LD + i] = t < nv ? IO<TIO>::load(k, gi) : 0.f;
+                Qb[t * LD + i] = t < nv ? IO<TIO>::load(q, gi) : 0.f;
+            }
+#pragma unroll 8
+            for (int e = tid; e < C * VS; e += kNT) {
+                const int t = e / VS, j = e % VS;
+                X[t * LS + j] = t < nv ? IO<TIO>::load(v, (tok0 + (size_t)t * H) * dv + j0 + j) : 0.f;
+            }
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        // cumulative log-decay per channel, its reference and factors
         if (tid < DK) {
             float g = 0.f;
             for (int t = 0; t < C; ++t) {
-                if (t < nv) g += la[(((size_t)b * Tn + t0 + t) * H + h) * DK + tid];
-                Kt[t * LD + tid] = g;
+                g += G[t * DK + tid];
+                G[t * DK + tid] = g;
             }
             const float gr = 0.5f * g;
             gref[tid] = gr;
@@ -78,85 +122,65 @@ chunk_simt_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TI
             if (!(fabsf(g) <= kMaxChunkLogDecay)) set_status(status, kStatusRange);
         }
         __syncthreads();
-        // 2. decayed operands; state into the chunk's reference frame
+        // 2. decayed operands (in place); state into the chunk's reference frame
         for (int e = tid; e < C * DK; e += kNT) {
             const int t = e / DK, i = e % DK;
-            if (t < nv) {
-                const size_t gi = (((size_t)b * Tn + t0 + t) * H + h) * DK + i;
-                const float g = Kt[t * LD + i];
-                const float ef = expf(g - gref[i]);
-                const float eb = expf(gref[i] - g);
-                Kb[t * LD + i] = IO<TIO>::load(k, gi) * ef;
-                Qb[t * LD + i] = IO<TIO>::load(q, gi) * ef;
-                Kt[t * LD + i] = kappa[gi] * eb;
-            } else {
-                Kb[t * LD + i] = 0.f;
-                Qb[t * LD + i] = 0.f;
-                Kt[t * LD + i] = 0.f;
-            }
+            const float g = G[t * DK + i];
+            Kb[t * LD + i] *= expf(g - gref[i]);
+            Qb[t * LD + i] *= expf(g - gref[i]);
+            Kt[t * LD + i] *= expf(gref[i] - g);
         }
         for (int e = tid; e < DK * VS; e += kNT) {
             const int i = e / VS, j = e % VS;
             S[i * LS + j] *= gin[i];
         }
         __syncthreads();
-        // 3. Gram matrices (lower triangles) and 4. state products
+        // 3. Gram matrices L = K_bar K_til^T, A = Q_bar K_til^T (triangles taken below) and
+        // 4. state products X = V - K_bar S_m, O = Q_bar S_m
+        smem_gemm<2>(C, C, DK, Kb, LD, 1, Kt, 1, LD, L, LC, 1.f, false);
+        smem_gemm<2>(C, C, DK, Qb, LD, 1, Kt, 1, LD, A, LC, 1.f, false);
+        smem_gemm<2>(C, VS, DK, Kb, LD, 1, S, LS, 1, X, LS, -1.f, true);
+        smem_gemm<2>(C, VS, DK, Qb, LD, 1, S, LS, 1, O, LS, 1.f, false);
+        __syncthreads();
         for (int e = tid; e < C * C; e += kNT) {
             const int t = e / C, s = e % C;
-            float l = 0.f, aq = 0.f;
-            if (s <= t) {
-                for (int i = 0; i < DK; ++i) {
-                    const float kt = Kt[s * LD + i];
-                    l = fmaf(Kb[t * LD + i], kt, l);
-                    aq = fmaf(Qb[t * LD + i], kt, aq);
-                }
-            }
-            L[t * LC + s] = (s < t) ? l : 0.f;
-            A[t * LC + s] = (s <= t) ? aq : 0.f;
-        }
-        for (int e = tid; e < C * VS; e += kNT) {
-            const int t = e / VS, j = e % VS;
-            float x = 0.f, oo = 0.f;
-            for (int i = 0; i < DK; ++i) {
-                const float sv = S[i * LS + j];
-                x = fmaf(Kb[t * LD + i], sv, x);
-                oo = fmaf(Qb[t * LD + i], sv, oo);
-            }
-            const float vv = (t < nv)
-                ? IO<TIO>::load(v, (((size_t)b * Tn + t0 + t) * H + h) * dv + j0 + j) : 0.f;
-            X[t * LS + j] = vv - x;
-            O[t * LS + j] = oo;
+            if (s >= t) L[t * LC + s] = 0.f;
+            if (s > t) A[t * LC + s] = 0.f;
         }
         __syncthreads();
-        // 5. forward substitution (I + L) Delta = X, one row at a time;
-        //    8 threads share a column's sum over earlier rows.
-        {
-            const int j = tid >> 3, g8 = tid & 7;
-            for (int t = 1; t < nv; ++t) {
-                float part = 0.f;
-                if (j < VS)
-                    for (int s = g8; s < t; s += 8) part = fmaf(L[t * LC + s], X[s * LS + j], part);
-                part += __shfl_xor_sync(0xffffffffu, part, 4);
-                part += __shfl_xor_sync(0xffffffffu, part, 2);
-                part += __shfl_xor_sync(0xffffffffu, part, 1);
-                if (j < VS && g8 == 0) X[t * LS + j] -= part;
+        // 5. forward substitution (I + L) Delta = X, blockwise: each 16-row diagonal block
+        //    by substitution (a thread per value column, in registers), then the rows
+        //    below it updated by one product
+        for (int r0 = 0; r0 < C; r0 += kSB) {
+            for (int j = tid; j < VS; j += kNT) {
+                float x[kSB];
+#pragma unroll
+                for (int t = 0; t < kSB; ++t) x[t] = X[(r0 + t) * LS + j];
+#pragma unroll
+                for (int t = 1; t < kSB; ++t)
+#pragma unroll
+                    for (int s2 = 0; s2 < t; ++s2) x[t] = fmaf(-L[(r0 + t) * LC + r0 + s2], x[s2], x[t]);
+#pragma unroll
+                for (int t = 0; t < kSB; ++t) X[(r0 + t) * LS + j] = x[t];
+            }
+            __syncthreads();
+            if (r0 + kSB < C) {
+                smem_gemm<2>(C - r0 - kSB, VS, kSB, L + (r0 + kSB) * LC + r0, LC, 1, X + r0 * LS, LS, 1,
+                             X + (r0 + kSB) * LS, LS, -1.f, true);
                 __syncthreads();
             }
         }
-        // 6. output rows and 7. state update
+        // 6. output rows O += A Delta and 7. state update S = diag(g_out) (S_m + K_til^T Delta)
+        smem_gemm<2>(C, VS, C, A, LC, 1, X, LS, 1, O, LS, 1.f, true);
+        smem_gemm<2>(DK, VS, C, Kt, 1, LD, X, LS, 1, S, LS, 1.f, true);
+        __syncthreads();
         for (int e = tid; e < C * VS; e += kNT) {
             const int t = e / VS, j = e % VS;
-            if (t < nv) {
-                float acc = O[t * LS + j];
-                for (int s = 0; s <= t; ++s) acc = fmaf(A[t * LC + s], X[s * LS + j], acc);
-                IO<TIO>::store(o, (((size_t)b * Tn + t0 + t) * H + h) * dv + j0 + j, acc);
-            }
+            if (t < nv) IO<TIO>::store(o, (((size_t)b * Tn + t0 + t) * H + h) * dv + j0 + j, O[t * LS + j]);
         }
         for (int e = tid; e < DK * VS; e += kNT) {
             const int i = e / VS, j = e % VS;
-            float acc = S[i * LS + j];
-            for (int s = 0; s < nv; ++s) acc = fmaf(Kt[s * LD + i], X[s * LS + j], acc);
-            S[i * LS + j] = acc * gout[i];
+            S[i * LS + j] *= gout[i];
         }
         __syncthreads();
     }
@@ -167,8 +191,8 @@ chunk_simt_kernel(const TIO* __restrict__ q, const TIO* __restrict__ k, const TI
 }
 
 size_t simt_smem_bytes(int DK, int C, int VS) {
-    const size_t LD = DK + 1, LS = VS + 1, LC = C + 1;
-    return sizeof(float) * (3 * C * LD + DK * LS + 2 * C * LC + 2 * C * LS + 3 * DK);
+    const size_t LD = DK + kPadW, LS = VS + kPadW, LC = C + 1;
+    return sizeof(float) * (3 * C * LD + DK * LS + 2 * C * LC + 2 * C * LS + 3 * DK + C * DK);
 }
 
 template <typename TIO>
