@@ -162,3 +162,29 @@ def test_dense_equals_diagonal_kdn_on_one_hot_keys():
     assert err(np.diagonal(P_T, axis1=-2, axis2=-1), to_host(diag[2]), "f32") <= 1e-4
     assert np.max(np.abs(P_T - np.einsum("bhi,ij->bhij", np.diagonal(P_T, axis1=-2, axis2=-1), np.eye(d)))) == 0.0
     del torch
+
+
+@pytest.mark.parametrize("io, d", [("f32", 64), ("bf16", 128)])
+def test_dense_strong_decay_renormalises(io, d):
+    """Channels that decay by e^-2 and e^-2.4 per token: the covariance pass holds the
+    decay outside P and folds it back in whenever a channel's running decay would
+    fall below 2^-20, here every six to seven tokens; the mean pass's 64-token chunks
+    then decay by 128 and 154 (within its range of 160, and beyond the 80 at which the
+    fused kernel takes the mid-chunk reference).  The result must still be the fp64
+    filter's; bf16 d = 128 takes the tensor-core mean pass, fp32 the CUDA-core one."""
+    import torch
+
+    kdn = _kdn()
+    B, T, H = 1, 150, 2
+    x = make_inputs("diag", B, T, H, d, d, io=io, seed=3131)
+    x["log_alpha"][:, :, 0, : d // 8] = -2.0
+    x["log_alpha"][:, :, 1, : d // 16] = -2.4
+    t = to_device(x)
+    ws = torch.empty(kdn.dense_workspace_size(B, T, H, d, kdn.KDN_BF16 if io == "bf16" else kdn.KDN_F32),
+                     dtype=torch.uint8, device="cuda")
+    got = kdn.kdn_dense_forward(t["q"], t["k"], t["v"], t["log_alpha"], t["omega"], t["r"], workspace=ws)
+    assert kdn.kdn_read_device_status(ws) == 0
+    o, S_T, P_T = (to_host(a) for a in got)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S_T)) and np.all(np.isfinite(P_T))
+    e = _check(got, _reference(x), io, f"strong decay {io} d={d}")
+    print(f"[parity] dense strong decay {io} d={d}: {e}")

@@ -66,6 +66,7 @@ size_t mem_smem_floats(int DK, int DV) {
 template <typename TIO>
 __global__ void __launch_bounds__(kMNT, 1) mem_adjoint_kernel(const MemArgs P) {
     const int DK = P.DK, DV = P.DV, LSK = DK + kRowPad, LSV = DV + kRowPad, LCC = kBC + 1;
+    constexpr int kEPC = 16 / static_cast<int>(sizeof(TIO));   // elements per 16-byte copy
     extern __shared__ float sm[];
     float* Sm = sm;                    // [DK][LSV] chunk-start state, then S_m
     float* dS = Sm + DK * LSV;         // [DK][LSV] gradient of the chunk's end state
@@ -120,33 +121,35 @@ __global__ void __launch_bounds__(kMNT, 1) mem_adjoint_kernel(const MemArgs P) {
     // read into registers by one batch of loads per thread before any of them is used.
     auto setup = [&](int n, int nv) {
         const int t0 = n * kBC;
-        // log_alpha -> Gc and kappa -> Kt by 16-byte async copies (rows past the
-        // sequence end zero-filled); k, q, v through registers
+        // log_alpha -> Gc and kappa -> Kt, and k, q (into the dK_bar, dQ_bar tiles, sized
+        // by d_k) and v (into the dX tile, sized by d_v) in their storage type, dense rows,
+        // by 16-byte async copies, rows past the sequence end zero-filled (those tiles are
+        // free until the reverse products)
+        const TIO* kg = static_cast<const TIO*>(P.k);
+        const TIO* qg = static_cast<const TIO*>(P.q);
+        const TIO* vg = static_cast<const TIO*>(P.v);
+        TIO* rawK = reinterpret_cast<TIO*>(dKb);
+        TIO* rawQ = reinterpret_cast<TIO*>(dQb);
+        TIO* rawV = reinterpret_cast<TIO*>(dX);
         for (int e4 = tid; e4 < kBC * DK / 4; e4 += kMNT) {
             const int t = (4 * e4) / DK, i = (4 * e4) % DK;
             const size_t gi = row(t0 + min(t, nv - 1)) * DK + i;
             cp_async16(Gc + t * LSK + i, P.la + gi, t < nv);
             cp_async16(Kt + t * LSK + i, P.kappa + gi, t < nv);
         }
-        float rk[kEl], rq[kEl], rv[kEl];
-#pragma unroll
-        for (int m = 0; m < kEl; ++m) {
-            const int e = tid + m * kMNT, t = e / DK, i = e % DK;
-            const bool ok = e < kBC * DK && t < nv;
-            const size_t gi = row(t0 + min(t, kBC - 1)) * DK + i;
-            rk[m] = ok ? IO<TIO>::load(static_cast<const TIO*>(P.k), gi) : 0.f;
-            rq[m] = ok ? IO<TIO>::load(static_cast<const TIO*>(P.q), gi) : 0.f;
-            const int tv = e / DV, j = e % DV;
-            const bool okv = e < kBC * DV && tv < nv;
-            rv[m] = okv ? IO<TIO>::load(static_cast<const TIO*>(P.v), row(t0 + min(tv, kBC - 1)) * DV + j) : 0.f;
+        for (int e = tid * kEPC; e < kBC * DK; e += kMNT * kEPC) {
+            const int t = e / DK, i = e % DK;
+            const size_t gi = row(t0 + min(t, nv - 1)) * DK + i;
+            cp_async16(rawK + e, kg + gi, t < nv);
+            cp_async16(rawQ + e, qg + gi, t < nv);
         }
-#pragma unroll
-        for (int m = 0; m < kEl; ++m) {
-            const int e = tid + m * kMNT;
-            if (e < kBC * DV) X[(e / DV) * LSV + e % DV] = rv[m];
+        for (int e = tid * kEPC; e < kBC * DV; e += kMNT * kEPC) {
+            const int t = e / DV, j = e % DV;
+            cp_async16(rawV + e, vg + row(t0 + min(t, nv - 1)) * DV + j, t < nv);
         }
         cp_async_wait_all();
         __syncthreads();
+        for (int e = tid; e < kBC * DV; e += kMNT) X[(e / DV) * LSV + e % DV] = IO<TIO>::load(rawV, e);
         if (tid < DK) {
             float g = 0.f;
             for (int t = 0; t < kBC; ++t) {
@@ -165,8 +168,8 @@ __global__ void __launch_bounds__(kMNT, 1) mem_adjoint_kernel(const MemArgs P) {
             const int e = tid + m * kMNT, t = e / DK, i = e % DK;
             if (e < kBC * DK) {
                 const float ef = expf(Gc[t * LSK + i] - gref[i]);
-                Kb[t * LSK + i] = rk[m] * ef;
-                Qb[t * LSK + i] = rq[m] * ef;
+                Kb[t * LSK + i] = IO<TIO>::load(rawK, e) * ef;
+                Qb[t * LSK + i] = IO<TIO>::load(rawQ, e) * ef;
                 Kt[t * LSK + i] /= ef;   // kappa e^{-(G_t - G_ref)}
                 Gc[t * LSK + i] = ef;    // (G itself is not needed again in the chunk)
             }
@@ -247,20 +250,19 @@ __global__ void __launch_bounds__(kMNT, 1) mem_adjoint_kernel(const MemArgs P) {
     for (int n = nch - 1; n >= 0; --n) {
         const int t0 = n * kBC, nv = min(kBC, T - t0);
         __syncthreads();
-        load_state(ck + (size_t)n * sdd);   // (completed below, before the barrier)
-        float rdo[kEl];
-#pragma unroll
-        for (int m = 0; m < kEl; ++m) {
-            const int e = tid + m * kMNT, t = e / DV, j = e % DV;
-            const bool ok = P.dO && e < kBC * DV && t < nv;
-            rdo[m] = ok ? IO<TIO>::load(static_cast<const TIO*>(P.dO), row(t0 + min(t, kBC - 1)) * DV + j) : 0.f;
+        load_state(ck + (size_t)n * sdd);
+        // dO in its storage type into the dX tile (sized by d_v, free here), then converted
+        {
+            const TIO* og = P.dO ? static_cast<const TIO*>(P.dO) : static_cast<const TIO*>(P.q);
+            TIO* rawO = reinterpret_cast<TIO*>(dX);
+            for (int e = tid * kEPC; e < kBC * DV; e += kMNT * kEPC) {
+                const int t = e / DV, j = e % DV;
+                cp_async16(rawO + e, og + row(t0 + min(t, nv - 1)) * DV + j, P.dO && t < nv);
+            }
+            cp_async_wait_all();
+            __syncthreads();
+            for (int e = tid; e < kBC * DV; e += kMNT) dO[(e / DV) * LSV + e % DV] = IO<TIO>::load(rawO, e);
         }
-#pragma unroll
-        for (int m = 0; m < kEl; ++m) {
-            const int e = tid + m * kMNT;
-            if (e < kBC * DV) dO[(e / DV) * LSV + e % DV] = rdo[m];
-        }
-        cp_async_wait_all();
         __syncthreads();
         setup(n, nv);   // Sm = S_m, X = Delta, operands, L, A
         scale_rows(dS, gout);   // Gp = diag(g_out) dS_out
