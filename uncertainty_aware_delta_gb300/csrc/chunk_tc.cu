@@ -268,6 +268,42 @@ __device__ __forceinline__ void store_tile_bf16(const float (&x)[2][4], unsigned
     }
 }
 
+// ---- warp-level bf16 MMA of a 16x16 block of X Y^T, X and Y K-major bf16 tiles in the
+// 128-byte-swizzled layout of the tensor-core operands (128-byte rows of 64 channels,
+// two K-atoms of 64 channels at atom strides xa and ya bytes)
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_m16n8k16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// x[n8 tile][4] = rows r0..r0+15 of X times rows c0..c0+15 of Y, over 128 channels.
+// ldmatrix: lane l addresses row (l & 7) of 8x8 matrix l >> 3; the A matrices are
+// (rows 0-7 | 8-15) x (channels 0-7 | 8-15) of each 16-channel step, the B matrices
+// (columns 0-7 | 8-15) x (channels 0-7 | 8-15).
+__device__ __forceinline__ void gram_block16(float (&x)[2][4], uint32_t X, uint32_t xa, uint32_t Y, uint32_t ya,
+                                             int r0, int c0, int lane) {
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[n][e] = 0.0f;
+    const int mi = lane >> 3, rr = lane & 7;
+    const int ra = r0 + rr + 8 * (mi & 1), rb = c0 + 8 * (mi >> 1) + rr;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        uint32_t a[4], bq[4];
+        ldmatrix_x4(X + (ks >> 2) * xa + sw128_off(ra, 2 * (ks & 3) + (mi >> 1)), a);
+        ldmatrix_x4(Y + (ks >> 2) * ya + sw128_off(rb, 2 * (ks & 3) + (mi & 1)), bq);
+        mma_bf16_m16n8k16(x[0], a, bq[0], bq[1]);
+        mma_bf16_m16n8k16(x[1], a, bq[2], bq[3]);
+    }
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
@@ -400,6 +436,11 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
     constexpr bool SEG = MODE != 0, NOV = MODE == 2;
     constexpr bool ISO = V == kVarIso, PK = V == kVarPkda, GK = V == kVarGiven;
     static_assert(!GK || MODE == 0, "given gains: whole sequences");
+    // Measured per variant (A/B on the B8 H16 T4096 workloads): the diagonal blocks of
+    // the triangular system by warp-level MMAs while the Gram MMA runs (DB), and the
+    // inputs of the chunk after next prefetched into L2 (PF).
+    constexpr bool DB = V == kVarPkda || V == kVarGiven;
+    constexpr bool PF = V == kVarDiag || V == kVarPkda || V == kVarGiven;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_addr(base);
@@ -457,6 +498,21 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         mbar_expect_tx(bar_v, 16384u);
         tma_load_4d(sb + OFF_VIN, &P.tv, 0, h, tb + n * kC, b, bar_v);
         tma_load_4d(sb + OFF_VIN + 8192, &P.tv, 64, h, tb + n * kC, b, bar_v);
+    };
+    // The tiles of chunk n into L2 (no shared memory written): issued while the copy
+    // engine is idle, a chunk before their copy to shared memory, which then reads L2.
+    auto prefetch_inputs = [&](int n) {
+        const int t0 = tb + n * kC;
+        tma_prefetch_4d(&P.tla, 0, h, t0, b);
+        if (V == kVarDiag || GK) tma_prefetch_4d(&P.tom, 0, h, t0, b);
+        tma_prefetch_4d(&P.tk, 0, h, t0, b);
+        tma_prefetch_4d(&P.tk, 64, h, t0, b);
+        tma_prefetch_4d(&P.tq, 0, h, t0, b);
+        tma_prefetch_4d(&P.tq, 64, h, t0, b);
+        if (!NOV) {
+            tma_prefetch_4d(&P.tv, 0, h, t0, b);
+            tma_prefetch_4d(&P.tv, 64, h, t0, b);
+        }
     };
     __syncthreads();
     // copies and MMA commits issued so far (thread 0: v, MMAs; thread 256: the Gram MMAs;
@@ -702,8 +758,8 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                         pn = nd.x;
                         pd = nd.y;
                         if ((u & 3) == 2) {   // exact rescale: pd back to [1, 2)
-                            const int ex = min((__float_as_int(pd) >> 23) & 0xff, 253);
-                            const float sc = __int_as_float((254 - ex) << 23);
+                            const int eb = min(__float_as_int(pd) & 0x7f800000, 253 << 23);
+                            const float sc = __int_as_float(0x7f000000 - eb);   // 2^(127 - exponent)
                             pn *= sc;
                             pd *= sc;
                         }
@@ -999,12 +1055,91 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
         }
         // ================= step 3
         if (wg2) {
-            // ---- Gram rows out of TMEM: M (fp32), query-write matrix A' (bf16)
             const int lt = tid - 256, lw = warp - 8;
-            if (ISO) {   // gain denominators of chunk n, while the Gram MMA runs
-                if (lw == 3) iso_scan(n, nv);
+            unsigned char* tt = base + OFF_TT;
+            const int g8 = lane >> 2, q4 = lane & 3;
+            // ---- T = M^{-1}, first its 16x16 diagonal blocks; each finished block also
+            //      goes to the bf16 tile T [t][s] (its blocks above the diagonal stay zero
+            //      from the start)
+            auto invert_diagonal_blocks = [&]() {
+                if (lt < 64) {  // 16x16 diagonal blocks: right-looking substitution, one column per thread
+                    const int blk = lt >> 4, c = lt & 15, o = 16 * blk;
+                    float acc[16], inv[16];
+#pragma unroll
+                    for (int r4 = 0; r4 < 4; ++r4) {
+                        const float4 d4 = *reinterpret_cast<const float4*>(sm + SM_INVD + o + 4 * r4);
+                        inv[4 * r4 + 0] = d4.x;
+                        inv[4 * r4 + 1] = d4.y;
+                        inv[4 * r4 + 2] = d4.z;
+                        inv[4 * r4 + 3] = d4.w;
+                    }
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) acc[r] = (r == c) ? 1.0f : 0.0f;
+#pragma unroll
+                    for (int s4 = 0; s4 < 16; s4 += 4) {
+                        // columns s4..s4+3 of the rows below, one 16-byte load per row
+                        float4 lq[16];
+#pragma unroll
+                        for (int r = s4 + 1; r < 16; ++r)
+                            lq[r] = *reinterpret_cast<const float4*>(LF + (o + r) * kLDF + o + s4);
+#pragma unroll
+                        for (int s = s4; s < s4 + 4; ++s) {
+                            const float xs = acc[s] * inv[s];
+                            acc[s] = xs;
+#pragma unroll
+                            for (int r = s + 1; r < 16; ++r) {
+                                const float4 q = lq[r];
+                                const float l = (s & 3) == 0 ? q.x : (s & 3) == 1 ? q.y : (s & 3) == 2 ? q.z : q.w;
+                                acc[r] = fmaf(-l, xs, acc[r]);
+                            }
+                        }
+                    }
+                    __nv_bfloat16* tcol = reinterpret_cast<__nv_bfloat16*>(tt + ((o + c) & 7) * 2);
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) {
+                        TF[(o + r) * kLDF + o + c] = acc[r];
+                        *reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<unsigned char*>(tcol) +
+                                                           sw128_off(o + r, (o + c) >> 3)) = __float2bfloat16_rn(acc[r]);
+                    }
+                }
+            };
+            // M = diag(r) + lower_incl(K_bar K_til'^T) (KDN): its diagonal is the gain
+            // denominator z_t = r_t + sum_i p_hat_t,i k_t,i^2 (the decay factors cancel).
+            // Isotropic: M'' = diag(r / b_hat) + lower_incl(K_bar K_til''^T), its diagonal
+            // r_t / b_hat_t + ||k_t||^2.  PKDA and given gains: M = I + strict_lower(K_bar K_til^T).
+            auto set_diagonal = [&](int t) {   // z_t on the diagonal of row t, 1 / z_t, beta_eff
+                float* row = LF + t * kLDF;
+                if (PK || GK) {
+                    row[t] = 1.0f;
+                    sm[SM_INVD + t] = 1.0f;
+                } else {
+                    const float g = row[t];
+                    const float z = sm[SM_RZ + pb * 64 + t] + g;
+                    row[t] = z;
+                    sm[SM_INVD + t] = rcp_approx(z);
+                    // effective write strength k^T kappa = (z - r) / z: the Gram diagonal
+                    // over z (isotropic: both divided by b_hat)
+                    if (!SEG && P.beta_eff && t < nv)
+                        P.beta_eff[(static_cast<size_t>(b) * Tall + t0 + t) * H + h] = g / z;
+                }
+            };
+            if (ISO && lw == 3) iso_scan(n, nv);   // gain denominators of chunk n (r / b_hat)
+            if (DB) {
+                // The diagonal blocks of M straight from the operand tiles (warp-level bf16
+                // MMAs, warp lw -> block lw), inverted while the Gram MMA runs; the Gram's
+                // readout then only fills the blocks below them.
+                float x[2][4];
+                gram_block16(x, sb + OFF_KQ, 16384u, sb + OFF_KT, 8192u, 16 * lw, 16 * lw, lane);
+                store_tile_16x16(x, LF + (16 * lw) * kLDF + 16 * lw, kLDF, 1.0f, g8, q4);
+                if (ISO) named_bar(kBarWG2, 128);   // the scan's r / b_hat
+                else __syncwarp();
+                if (lane < 16) set_diagonal(16 * lw + lane);
+                named_bar(kBarWG2, 128);
+                invert_diagonal_blocks();
+            } else if (ISO) {
                 named_bar(kBarWG2, 128);
             }
+            // ---- Gram rows out of TMEM: M (fp32), query-write matrix A' (bf16)
             {
                 wait_or_abort(bar_mma, pb);
                 if (n > 0) wait_or_abort(bar_oj, pb ^ 1u);   // A' of chunk n-1 has been read
@@ -1012,41 +1147,20 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
                 uint32_t v0[32], v1[32];
                 tmem_ld64(TM_G, v0, v1);
                 if (lt < 64) {
-                    // KDN: M = diag(r) + lower_incl(K_bar K_til'^T): its diagonal is the gain
-                    // denominator z_t = r_t + sum_i p_hat_t,i k_t,i^2 (the decay factors cancel).
-                    // PKDA: M = I + strict_lower(K_bar K_til^T) (the write key is not normalised).
+                    // the whole row, or the blocks left of the diagonal block
                     float* row = LF + lt * kLDF;
+                    const int nc4 = DB ? 4 * (lt >> 4) : 16;
 #pragma unroll
                     for (int c4 = 0; c4 < 16; ++c4) {
                         const int s = 4 * c4;
-                        *reinterpret_cast<float4*>(row + s) =
-                            make_float4(__uint_as_float(s + 0 < 32 ? v0[s + 0] : v1[s + 0 - 32]),
-                                        __uint_as_float(s + 1 < 32 ? v0[s + 1] : v1[s + 1 - 32]),
-                                        __uint_as_float(s + 2 < 32 ? v0[s + 2] : v1[s + 2 - 32]),
-                                        __uint_as_float(s + 3 < 32 ? v0[s + 3] : v1[s + 3 - 32]));
+                        if (c4 < nc4)
+                            *reinterpret_cast<float4*>(row + s) =
+                                make_float4(__uint_as_float(s + 0 < 32 ? v0[s + 0] : v1[s + 0 - 32]),
+                                            __uint_as_float(s + 1 < 32 ? v0[s + 1] : v1[s + 1 - 32]),
+                                            __uint_as_float(s + 2 < 32 ? v0[s + 2] : v1[s + 2 - 32]),
+                                            __uint_as_float(s + 3 < 32 ? v0[s + 3] : v1[s + 3 - 32]));
                     }
-                    if (PK || GK) {
-                        row[lt] = 1.0f;
-                        sm[SM_INVD + lt] = 1.0f;
-                    } else {
-                        // column lt of row lt: a 5-level select tree on the lane bits
-                        uint32_t x[32];
-#pragma unroll
-                        for (int s = 0; s < 32; ++s) x[s] = lt < 32 ? v0[s] : v1[s];
-#pragma unroll
-                        for (int lv = 0; lv < 5; ++lv) {
-                            const bool hi = (lane >> lv) & 1;
-#pragma unroll
-                            for (int j = 0; j < (16 >> lv); ++j) x[j] = hi ? x[2 * j + 1] : x[2 * j];
-                        }
-                        const float z = sm[SM_RZ + pb * 64 + lt] + __uint_as_float(x[0]);
-                        row[lt] = z;
-                        sm[SM_INVD + lt] = 1.0f / z;
-                        // effective write strength k^T kappa = (z - r) / z: the Gram
-                        // diagonal over z (isotropic: both divided by b_hat)
-                        if (!SEG && P.beta_eff && lt < nv)
-                            P.beta_eff[(static_cast<size_t>(b) * Tall + t0 + lt) * H + h] = __uint_as_float(x[0]) / z;
-                    }
+                    if (!DB) set_diagonal(lt);   // (its own row, read back)
                 } else {
                     const int t = lt - 64;
 #pragma unroll
@@ -1065,51 +1179,10 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             }
             tc_fence_before();
             named_bar(kBarWG2, 128);
-            // ---- T = M^{-1}; each finished block also goes to the bf16 tile T [t][s]
-            //      (its blocks above the diagonal stay zero from the start)
-            unsigned char* tt = base + OFF_TT;
-            if (lt < 64) {  // 16x16 diagonal blocks: right-looking substitution, one column per thread
-                const int blk = lt >> 4, c = lt & 15, o = 16 * blk;
-                float acc[16], inv[16];
-#pragma unroll
-                for (int r4 = 0; r4 < 4; ++r4) {
-                    const float4 d4 = *reinterpret_cast<const float4*>(sm + SM_INVD + o + 4 * r4);
-                    inv[4 * r4 + 0] = d4.x;
-                    inv[4 * r4 + 1] = d4.y;
-                    inv[4 * r4 + 2] = d4.z;
-                    inv[4 * r4 + 3] = d4.w;
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) acc[r] = (r == c) ? 1.0f : 0.0f;
-#pragma unroll
-                for (int s4 = 0; s4 < 16; s4 += 4) {
-                    // columns s4..s4+3 of the rows below, one 16-byte load per row
-                    float4 lq[16];
-#pragma unroll
-                    for (int r = s4 + 1; r < 16; ++r)
-                        lq[r] = *reinterpret_cast<const float4*>(LF + (o + r) * kLDF + o + s4);
-#pragma unroll
-                    for (int s = s4; s < s4 + 4; ++s) {
-                        const float xs = acc[s] * inv[s];
-                        acc[s] = xs;
-#pragma unroll
-                        for (int r = s + 1; r < 16; ++r) {
-                            const float4 q = lq[r];
-                            const float l = (s & 3) == 0 ? q.x : (s & 3) == 1 ? q.y : (s & 3) == 2 ? q.z : q.w;
-                            acc[r] = fmaf(-l, xs, acc[r]);
-                        }
-                    }
-                }
-                __nv_bfloat16* tcol = reinterpret_cast<__nv_bfloat16*>(tt + ((o + c) & 7) * 2);
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    TF[(o + r) * kLDF + o + c] = acc[r];
-                    *reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<unsigned char*>(tcol) +
-                                                       sw128_off(o + r, (o + c) >> 3)) = __float2bfloat16_rn(acc[r]);
-                }
+            if (!DB) {
+                invert_diagonal_blocks();
+                named_bar(kBarWG2, 128);
             }
-            named_bar(kBarWG2, 128);
-            const int g8 = lane >> 2, q4 = lane & 3;
             if (lw < 2) {  // 16 -> 32 merges: T_ij = -T_ii (M_ij T_jj), (i, j) = (1, 0), (3, 2)
                 const int i = 2 * lw + 1, j = 2 * lw;
                 float x[2][4];
@@ -1162,6 +1235,9 @@ __global__ void __launch_bounds__(kNT, 1) kdn_fused_tc_kernel(const __grid_const
             }
             ph_v ^= 1u;
             fence_proxy_async();   // v has been read: the next chunk's copy may overwrite it
+            // (chunk n + 1's tiles landed before the gains pass; chunk n + 2's copies are
+            //  issued after chunk n + 1's operand pass)
+            if (PF && tid == 32 && n + 2 < nchunks) prefetch_inputs(n + 2);
             tc_fence_before();
             // ---- Delta'^T = Y^T T^T
             named_bar(kBarTReady, 256);
