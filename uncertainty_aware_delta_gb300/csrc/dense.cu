@@ -26,24 +26,35 @@
 //     z = w . y,   s = 1 / (r + z),   kappa = s G y,   Ptil <- Ptil_hat - s y y^T
 // (G y = P_hat k = u, so G (Ptil_hat - s y y^T) G = P_hat - kappa u^T): one
 // matrix-vector product and one rank-1 downdate, 2 d^2 multiply-adds.  When a
-// channel's running decay would fall below 2^-20 the token's G is folded into
-// Ptil (Ptil <- G Ptil G) and G restarts from 1, so omega / g^2 stays bounded.
+// channel's running decay would fall below 2^-20 the running G is folded into
+// Ptil (Ptil <- G Ptil G) and G restarts from 1, so omega / g^2 stays bounded
+// (for any one token's decay a above 2^-20).
 // The diagonal increments diag(omega / g^2) are kept in a per-row accumulator
 // beside the register block and folded in at the end and at each
 // renormalisation.
+//
+// Tokens go in pairs (t, t+1), so that one pass over the register block of Ptil
+// serves two matrix-vector products and one barrier serves two tokens.  With
+// y_t = (Ptil + diag(dacc_t)) w_t (Ptil before the pair) is the first token's y,
+// and the second token's y is the product with the downdated matrix,
+//     y_{t+1} = v - s_t (y_t . w_{t+1}) y_t,   v = (Ptil + diag(dacc_{t+1})) w_{t+1},
+//     z_{t+1} = w_{t+1} . v - s_t (y_t . w_{t+1})^2,
+// so the three dot products z_t, y_t . w_{t+1} and w_{t+1} . v are reduced together,
+// and then Ptil -= s_t y_t y_t^T + s_{t+1} y_{t+1} y_{t+1}^T.  A renormalisation that
+// the pair's second token needs happens at the pair's start (folding early is exact).
 //
 // CTA (b, h), 4 d threads: warp w owns rows 8w .. 8w+7 of Ptil, lane l the
 // columns C l .. C l + C - 1 (C = d / 32), in registers for the whole sequence;
 // the running decay of each channel is formed once, by the thread that stages
 // its inputs, and read from shared memory by the others.
-// Per token: the row products with w and their warp reduce-scatter (the four
-// lanes of a row end with its sum and keep its diagonal accumulator), z through
-// shared memory (the token's one barrier, which also carries the renormalisation
-// decision for the next token), the downdate and kappa.  Inputs are loaded from
-// global memory kPF tokens ahead into registers (the token loop is unrolled by
-// kPF so every register slot has a fixed name) and written to shared memory one
-// token ahead, so no global-memory latency sits on a token.  fp32 arithmetic
-// throughout.
+// Per pair: the row products with both w and their warp reduce-scatter (the four
+// lanes of a row end with its sums and keep its diagonal accumulator), the three
+// dot products through shared memory (the pair's one barrier, which also carries
+// the renormalisation decision for the next pair), the rank-2 downdate and the
+// two tokens' kappa.  Inputs are loaded from global memory kPP pairs ahead into
+// registers (the pair loop is unrolled by kPP so every register slot has a fixed
+// name) and written to shared memory one pair ahead, so no global-memory latency
+// sits on a pair.  fp32 arithmetic throughout.
 
 #include <cuda_bf16.h>
 
@@ -55,7 +66,7 @@ namespace {
 
 constexpr int kRowsPerWarp = 8;
 constexpr float kRenormFloor = 9.5367431640625e-07f;   // 2^-20
-constexpr int kPF = 4;   // tokens of inputs in flight (register slots)
+constexpr int kPP = 2;   // token pairs of inputs in flight (register slots)
 
 // This lane's C consecutive columns from shared memory in one vector load (lane l
 // reads words C l .. C l + C - 1: conflict-free, where C scalar loads of stride C
@@ -77,15 +88,18 @@ __device__ __forceinline__ void load_cols(const float* p, float (&x)[C]) {
 template <int D, typename TIO>
 __global__ void __launch_bounds__(4 * D) dense_cov_kernel(DenseArgs a, float* __restrict__ kappa) {
     constexpr int C = D / 32, W = D / kRowsPerWarp;
-    // per-token inputs in three buffers (token t in buffer t % 3): k, the running decay
-    // G_{t-1} a_t (before the token's renormalisation, if it has one), omega; y and the
-    // warps' partial sums of z in two (token parity).  A buffer is rewritten only after
-    // every thread has passed a later barrier than its last read, so one barrier per
-    // token suffices.
-    __shared__ __align__(16) float s_in[3][3][D];
-    __shared__ float s_r[3];
-    __shared__ __align__(16) float s_y[2][D];
-    __shared__ __align__(16) float s_zpart[2][W];
+    // per-pair inputs in three buffers (pair p in buffer p % 3): k and omega of its two
+    // tokens, the running decays G_{t-1} a_t and G_{t-1} a_t a_{t+1} (before the pair's
+    // renormalisation, if it has one) and a_{t+1}; y_t, the second token's unreduced
+    // product and the warps' partial sums of the three scalars in two (pair parity).  A
+    // buffer is rewritten only after every thread has passed a later barrier than its
+    // last read, so one barrier per pair suffices.
+    __shared__ __align__(16) float s_in[3][7][D];
+    __shared__ float s_r[3][2];
+    __shared__ __align__(16) float s_u[2][D];
+    __shared__ __align__(16) float s_v[2][D];
+    __shared__ __align__(16) float s_zpart[2][3][W];
+    enum { IK0 = 0, IK1, IW0, IW1, IG0, IG1, IA1 };
 
     const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -100,6 +114,7 @@ __global__ void __launch_bounds__(4 * D) dense_cov_kernel(DenseArgs a, float* __
     const size_t ts = static_cast<size_t>(a.H) * D;   // token stride of [B, T, H, d]
     const size_t row0 = static_cast<size_t>(b) * a.T * ts + static_cast<size_t>(h) * D;
     const size_t sb = static_cast<size_t>(bh) * D * D;
+    const int npairs = (a.T + 1) / 2;
 
     float P[kRowsPerWarp][C];   // Ptil without its diagonal increments
 #pragma unroll
@@ -109,152 +124,231 @@ __global__ void __launch_bounds__(4 * D) dense_cov_kernel(DenseArgs a, float* __
             const size_t e = sb + static_cast<size_t>(i0 + r) * D + j0 + c;
             P[r][c] = a.P0 ? a.P0[e] : (i0 + r == j0 + c ? 1.0f : 0.0f);
         }
-    float gs = 1.0f;     // stagers: running decay of channel ch after the current token
+    float gs = 1.0f;     // stagers: running decay of channel ch after the current pair
     float dacc = 0.0f;   // diagonal increment of row i0 + rho (the same on its four lanes)
-    bool folded = false; // the last token renormalised (its G is 1)
+    bool folded = false; // the last pair renormalised at its start
 
     // register slots of the prefetched inputs (stagers): k, log_alpha, omega of channel ch
-    // and r (channel 0) of one token each
-    float fk[kPF], fl[kPF], fw[kPF], fr[kPF];
-    auto fetch = [&](int t, float& k_, float& l_, float& w_, float& r_) {
-        if (stager && t < a.T) {
-            const size_t e = row0 + static_cast<size_t>(t) * ts + ch;
-            k_ = IO<TIO>::load(k, e);
-            l_ = a.log_alpha[e];
-            w_ = a.omega[e];
-            if (ch == 0) r_ = a.r[(static_cast<size_t>(b) * a.T + t) * a.H + h];
+    // and r (channel 0) of the two tokens of one pair each.  A token past T reads as
+    // k = 0, log_alpha = 0, omega = 0, r = 1: it changes nothing (zero gain, no decay,
+    // no noise), so an odd T ends on a pair with an empty second token.
+    float fk[kPP][2], fl[kPP][2], fw[kPP][2], fr[kPP][2];
+    auto fetch = [&](int pp, float (&k_)[2], float (&l_)[2], float (&w_)[2], float (&r_)[2]) {
+        if (stager) {
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int t = 2 * pp + e2;
+                k_[e2] = 0.0f;
+                l_[e2] = 0.0f;
+                w_[e2] = 0.0f;
+                r_[e2] = 1.0f;
+                if (t < a.T) {
+                    const size_t e = row0 + static_cast<size_t>(t) * ts + ch;
+                    k_[e2] = IO<TIO>::load(k, e);
+                    l_[e2] = a.log_alpha[e];
+                    w_[e2] = a.omega[e];
+                    if (ch == 0) r_[e2] = a.r[(static_cast<size_t>(b) * a.T + t) * a.H + h];
+                }
+            }
         }
     };
-    // a token's inputs into buffer t % 3, with the running decay G_{t-1} a_t of channel
-    // ch; returns whether it falls below the floor (the token then renormalises)
-    auto put = [&](int t, float k_, float l_, float w_, float r_) -> bool {
+    // a pair's inputs into buffer pp % 3 with the running decays of channel ch; returns
+    // whether the second token's falls below the floor (the pair then renormalises at
+    // its start: G_{t-1} a_t goes into Ptil and the second token's decay is a_{t+1})
+    auto put = [&](int pp, const float (&k_)[2], const float (&l_)[2], const float (&w_)[2],
+                   const float (&r_)[2]) -> bool {
         bool need = false;
         if (stager) {
-            const int bt = t % 3;
-            float* buf = &s_in[bt][0][0];
-            const float gn = gs * expf(l_);
-            buf[0 * D + ch] = k_;
-            buf[1 * D + ch] = gn;
-            buf[2 * D + ch] = w_;
-            if (ch == 0) s_r[bt] = r_;
-            need = !(gn >= kRenormFloor);
+            const int bt = pp % 3;
+            const float g0 = gs * expf(l_[0]), a1 = expf(l_[1]), g1 = g0 * a1;
+            s_in[bt][IK0][ch] = k_[0];
+            s_in[bt][IK1][ch] = k_[1];
+            s_in[bt][IW0][ch] = w_[0];
+            s_in[bt][IW1][ch] = w_[1];
+            s_in[bt][IG0][ch] = g0;
+            s_in[bt][IG1][ch] = g1;
+            s_in[bt][IA1][ch] = a1;
+            if (ch == 0) {
+                s_r[bt][0] = r_[0];
+                s_r[bt][1] = r_[1];
+            }
+            need = !(g1 >= kRenormFloor);
         }
         return need;
     };
 #pragma unroll
-    for (int u = 0; u < kPF; ++u) fetch(u, fk[u], fl[u], fw[u], fr[u]);
-    bool renorm = __syncthreads_or(a.T > 0 ? put(0, fk[0], fl[0], fw[0], fr[0]) : false);
-    fetch(kPF, fk[0], fl[0], fw[0], fr[0]);
+    for (int u = 0; u < kPP; ++u) fetch(u, fk[u], fl[u], fw[u], fr[u]);
+    bool renorm = __syncthreads_or(npairs > 0 ? put(0, fk[0], fl[0], fw[0], fr[0]) : false);
+    fetch(kPP, fk[0], fl[0], fw[0], fr[0]);
 
 #pragma unroll 1
-    for (int t0 = 0; t0 < a.T; t0 += kPF)
+    for (int p0 = 0; p0 < npairs; p0 += kPP)
 #pragma unroll
-    for (int u = 0; u < kPF; ++u) {
-        const int t = t0 + u;
-        if (t >= a.T) break;
-        const int bt = t % 3, pt = t & 1;
-        const float* kin = s_in[bt][0];
-        const float* gin = s_in[bt][1];
-        const float* win = s_in[bt][2];
-        // ---- decay: G_t = G_{t-1} diag(a_t); on renormalisation G_t goes into Ptil and
-        //      restarts from 1
-        float gc[C], g_rho;
-        load_cols<C>(gin + j0, gc);
+    for (int u = 0; u < kPP; ++u) {
+        const int pp = p0 + u;
+        if (pp >= npairs) break;
+        const int t = 2 * pp, bt = pp % 3, pt = pp & 1;
+        const float* in = &s_in[bt][0][0];
+        // ---- decays of the two tokens: G_t = G_{t-1} diag(a_t), G_{t+1} = G_t diag(a_{t+1});
+        //      on renormalisation G_t goes into Ptil, and G_t = 1, G_{t+1} = diag(a_{t+1})
+        float gc0[C], gc1[C], g0r, g1r;
+        load_cols<C>(in + IG0 * D + j0, gc0);
         if (renorm) {
 #pragma unroll
             for (int r = 0; r < kRowsPerWarp; ++r) {
-                const float gi = gin[i0 + r];
+                const float gi = in[IG0 * D + i0 + r];
 #pragma unroll
-                for (int c = 0; c < C; ++c) P[r][c] *= gi * gc[c];
+                for (int c = 0; c < C; ++c) P[r][c] *= gi * gc0[c];
             }
-            const float gd = gin[i0 + rho];
+            const float gd = in[IG0 * D + i0 + rho];
             dacc *= gd * gd;
 #pragma unroll
-            for (int c = 0; c < C; ++c) gc[c] = 1.0f;
-            g_rho = 1.0f;
-            gs = 1.0f;
+            for (int c = 0; c < C; ++c) gc0[c] = 1.0f;
+            load_cols<C>(in + IA1 * D + j0, gc1);
+            g0r = 1.0f;
+            g1r = in[IA1 * D + i0 + rho];
+            if (stager) gs = in[IA1 * D + ch];
         } else {
-            g_rho = gin[i0 + rho];
-            if (stager) gs = gin[ch];
+            load_cols<C>(in + IG1 * D + j0, gc1);
+            g0r = in[IG0 * D + i0 + rho];
+            g1r = in[IG1 * D + i0 + rho];
+            if (stager) gs = in[IG1 * D + ch];
         }
         folded = renorm;
-        // ---- Ptil_hat = Ptil + diag(omega / g^2); y = Ptil_hat w, w = G k
-        dacc += __fdividef(win[i0 + rho], g_rho * g_rho);
-        float wc[C];
-        load_cols<C>(kin + j0, wc);
+        // ---- diagonal increments omega / g^2 of the two tokens; w = G k
+        const float dacc0 = dacc + __fdividef(in[IW0 * D + i0 + rho], g0r * g0r);
+        const float dacc1 = dacc0 + __fdividef(in[IW1 * D + i0 + rho], g1r * g1r);
+        dacc = dacc1;
+        float wa[C], wb[C];
+        load_cols<C>(in + IK0 * D + j0, wa);
+        load_cols<C>(in + IK1 * D + j0, wb);
 #pragma unroll
-        for (int c = 0; c < C; ++c) wc[c] *= gc[c];
-        float rs[kRowsPerWarp];
+        for (int c = 0; c < C; ++c) {
+            wa[c] *= gc0[c];
+            wb[c] *= gc1[c];
+        }
+        // ---- both products with the same Ptil: Ptil w_t and Ptil w_{t+1}
+        float ru[kRowsPerWarp], rv[kRowsPerWarp];
 #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r) {
-            float acc = 0.0f;
+            float au = 0.0f, av = 0.0f;
 #pragma unroll
-            for (int c = 0; c < C; ++c) acc = fmaf(P[r][c], wc[c], acc);
-            rs[r] = acc;
+            for (int c = 0; c < C; ++c) {
+                au = fmaf(P[r][c], wa[c], au);
+                av = fmaf(P[r][c], wb[c], av);
+            }
+            ru[r] = au;
+            rv[r] = av;
         }
         // reduce-scatter over the lanes: lane bits 4, 3, 2 pick the row, then full sums
         // over the four lanes that share it
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const bool hi = lane & 16;
-            const float send = hi ? rs[j] : rs[j + 4], keep = hi ? rs[j + 4] : rs[j];
-            rs[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+            const float su = hi ? ru[j] : ru[j + 4], ku = hi ? ru[j + 4] : ru[j];
+            const float sv = hi ? rv[j] : rv[j + 4], kv = hi ? rv[j + 4] : rv[j];
+            ru[j] = ku + __shfl_xor_sync(0xffffffffu, su, 16);
+            rv[j] = kv + __shfl_xor_sync(0xffffffffu, sv, 16);
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const bool hi = lane & 8;
-            const float send = hi ? rs[j] : rs[j + 2], keep = hi ? rs[j + 2] : rs[j];
-            rs[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+            const float su = hi ? ru[j] : ru[j + 2], ku = hi ? ru[j + 2] : ru[j];
+            const float sv = hi ? rv[j] : rv[j + 2], kv = hi ? rv[j + 2] : rv[j];
+            ru[j] = ku + __shfl_xor_sync(0xffffffffu, su, 8);
+            rv[j] = kv + __shfl_xor_sync(0xffffffffu, sv, 8);
         }
         {
             const bool hi = lane & 4;
-            const float send = hi ? rs[0] : rs[1], keep = hi ? rs[1] : rs[0];
-            rs[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+            const float su = hi ? ru[0] : ru[1], ku = hi ? ru[1] : ru[0];
+            const float sv = hi ? rv[0] : rv[1], kv = hi ? rv[1] : rv[0];
+            ru[0] = ku + __shfl_xor_sync(0xffffffffu, su, 4);
+            rv[0] = kv + __shfl_xor_sync(0xffffffffu, sv, 4);
         }
-        rs[0] += __shfl_xor_sync(0xffffffffu, rs[0], 2);
-        rs[0] += __shfl_xor_sync(0xffffffffu, rs[0], 1);
-        const float w_rho = g_rho * kin[i0 + rho];
-        const float y = rs[0] + dacc * w_rho;   // row i0 + rho of Ptil_hat w
-        float zp = y * w_rho;                   // the same on the 4 lanes of a row
-        zp += __shfl_xor_sync(0xffffffffu, zp, 4);
-        zp += __shfl_xor_sync(0xffffffffu, zp, 8);
-        zp += __shfl_xor_sync(0xffffffffu, zp, 16);
-        if ((lane & 3) == 0) s_y[pt][i0 + rho] = y;
-        if (lane == 0) s_zpart[pt][warp] = zp;
-        // the next token's inputs (slot (u + 1) % kPF, fetched kPF - 1 tokens ago), whether it
-        // renormalises, and the fetch of token t + kPF + 1 into that slot once written
-        const int un = (u + 1) % kPF;   // (a constant once the loop over u is unrolled)
-        const bool need = t + 1 < a.T ? put(t + 1, fk[un], fl[un], fw[un], fr[un]) : false;
-        fetch(t + kPF + 1, fk[un], fl[un], fw[un], fr[un]);
+        ru[0] += __shfl_xor_sync(0xffffffffu, ru[0], 2);
+        rv[0] += __shfl_xor_sync(0xffffffffu, rv[0], 2);
+        ru[0] += __shfl_xor_sync(0xffffffffu, ru[0], 1);
+        rv[0] += __shfl_xor_sync(0xffffffffu, rv[0], 1);
+        // rows i0 + rho of y_t = (Ptil + diag(dacc_t)) w_t and of v = (Ptil + diag(dacc_{t+1}))
+        // w_{t+1}; the second token's y is v - s_t (y_t . w_{t+1}) y_t (Ptil after the first
+        // token's downdate, applied to w_{t+1}), known once s_t is
+        const float wa_r = g0r * in[IK0 * D + i0 + rho], wb_r = g1r * in[IK1 * D + i0 + rho];
+        const float yu = ru[0] + dacc0 * wa_r;
+        const float yv = rv[0] + dacc1 * wb_r;
+        // partial sums (the same on the 4 lanes of a row): z_t = w_t . y_t,
+        // y_t . w_{t+1}, w_{t+1} . v
+        float zq[3] = {yu * wa_r, yu * wb_r, yv * wb_r};
+#pragma unroll
+        for (int m = 4; m <= 16; m <<= 1)
+#pragma unroll
+            for (int e3 = 0; e3 < 3; ++e3) zq[e3] += __shfl_xor_sync(0xffffffffu, zq[e3], m);
+        if ((lane & 3) == 0) {
+            s_u[pt][i0 + rho] = yu;
+            s_v[pt][i0 + rho] = yv;
+        }
+        if (lane == 0) {
+            s_zpart[pt][0][warp] = zq[0];
+            s_zpart[pt][1][warp] = zq[1];
+            s_zpart[pt][2][warp] = zq[2];
+        }
+        // the next pair's inputs (slot (u + 1) % kPP, fetched kPP - 1 pairs ago), whether it
+        // renormalises, and the fetch of pair pp + kPP + 1 into that slot once written
+        const int un = (u + 1) % kPP;   // (a constant once the loop over u is unrolled)
+        const bool need = pp + 1 < npairs ? put(pp + 1, fk[un], fl[un], fw[un], fr[un]) : false;
+        fetch(pp + kPP + 1, fk[un], fl[un], fw[un], fr[un]);
         renorm = __syncthreads_or(need);   // 1
-        // ---- gain s = 1 / (r + z), kappa = s G y, downdate Ptil -= s y y^T
-        float z4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // ---- the three scalars, the two gains s = 1 / (r + z), y_{t+1}, and the rank-2
+        //      downdate Ptil -= s_t y_t y_t^T + s_{t+1} y_{t+1} y_{t+1}^T
+        float zs[3];
 #pragma unroll
-        for (int w4 = 0; w4 < W / 4; ++w4) {
-            const float4 zz = *reinterpret_cast<const float4*>(s_zpart[pt] + 4 * w4);
-            z4[0] += zz.x;
-            z4[1] += zz.y;
-            z4[2] += zz.z;
-            z4[3] += zz.w;
+        for (int e3 = 0; e3 < 3; ++e3) {
+            float z4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int w4 = 0; w4 < W / 4; ++w4) {
+                const float4 zz = *reinterpret_cast<const float4*>(s_zpart[pt][e3] + 4 * w4);
+                z4[0] += zz.x;
+                z4[1] += zz.y;
+                z4[2] += zz.z;
+                z4[3] += zz.w;
+            }
+            zs[e3] = (z4[0] + z4[1]) + (z4[2] + z4[3]);
         }
-        const float z = (z4[0] + z4[1]) + (z4[2] + z4[3]);
-        const float sg = __frcp_rn(s_r[bt] + z);
-        float yr[kRowsPerWarp], yc[C];
+        const float s0 = __frcp_rn(s_r[bt][0] + zs[0]);
+        const float cb = s0 * zs[1];                        // s_t (y_t . w_{t+1})
+        const float z1 = fmaf(-cb, zs[1], zs[2]);           // w_{t+1} . y_{t+1}
+        const float s1 = __frcp_rn(s_r[bt][1] + z1);
+        float yr0[kRowsPerWarp], yr1[kRowsPerWarp], yc0[C], yc1[C];
 #pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) yr[r] = sg * s_y[pt][i0 + r];
-        load_cols<C>(s_y[pt] + j0, yc);
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            const float y0 = s_u[pt][i0 + r];
+            yr0[r] = y0;
+            yr1[r] = fmaf(-cb, y0, s_v[pt][i0 + r]);
+        }
+        load_cols<C>(s_u[pt] + j0, yc0);
+        load_cols<C>(s_v[pt] + j0, yc1);
 #pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r)
+        for (int c = 0; c < C; ++c) yc1[c] = fmaf(-cb, yc0[c], yc1[c]);
 #pragma unroll
-            for (int c = 0; c < C; ++c) P[r][c] = fmaf(-yr[r], yc[c], P[r][c]);
-        if (stager) kappa[row0 + static_cast<size_t>(t) * ts + ch] = sg * gs * s_y[pt][ch];
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            const float f0 = s0 * yr0[r], f1 = s1 * yr1[r];
+#pragma unroll
+            for (int c = 0; c < C; ++c) P[r][c] = fmaf(-f0, yc0[c], fmaf(-f1, yc1[c], P[r][c]));
+        }
+        if (stager) {
+            // kappa = s G y for each token (G_t of channel ch: 1 after a renormalisation)
+            const float y0 = s_u[pt][ch], y1 = fmaf(-cb, y0, s_v[pt][ch]);
+            const float g0 = folded ? 1.0f : in[IG0 * D + ch];
+            kappa[row0 + static_cast<size_t>(t) * ts + ch] = s0 * g0 * y0;
+            if (t + 1 < a.T) kappa[row0 + static_cast<size_t>(t + 1) * ts + ch] = s1 * gs * y1;
+        }
     }
-    // final covariance P_T = G (Ptil + diag(dacc)) G with G of the last token (1 when it
-    // renormalised, or for T = 0): the register blocks first (each thread writes the
-    // block it read, so in-place resume is safe), then the diagonal increments, after
-    // a barrier
-    const float* gl = s_in[a.T > 0 ? (a.T - 1) % 3 : 0][1];   // the last token's buffer
-    const bool unit = a.T == 0 || folded;
+    // final covariance P_T = G (Ptil + diag(dacc)) G with G the running decay after the
+    // last pair (a_{t+1} when that pair renormalised; 1 for T = 0): the register blocks
+    // first (each thread writes the block it read, so in-place resume is safe), then the
+    // diagonal increments, after a barrier
+    const int lb = npairs > 0 ? (npairs - 1) % 3 : 0;
+    const float* gl = s_in[lb][folded ? IA1 : IG1];
+    const bool unit = a.T == 0;
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r)
 #pragma unroll
