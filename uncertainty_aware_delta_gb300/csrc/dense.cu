@@ -60,6 +60,7 @@
 
 #include "common.cuh"
 #include "kdn_internal.h"
+#include "mma_tf32x3.cuh"
 
 namespace kdn {
 namespace {
@@ -364,10 +365,281 @@ __global__ void __launch_bounds__(4 * D) dense_cov_kernel(DenseArgs a, float* __
     }
 }
 
+// ---------------------------------------------------------------- d = 128: token blocks
+// The same recurrence over blocks of up to 16 tokens, with the products on tensor
+// cores (3xTF32 warp-level MMAs, fp32-level accuracy) and Ptil in shared memory.
+// In a block of m tokens with decay factors G_j relative to a per-channel reference
+// (Ptil = e^{ref} P e^{ref} at the block start), w_j = G_j k_j and dacc_j = sum_{i<=j}
+// omega_i / G_i^2, every token's y is a combination of u_j = (Ptil + diag(dacc_j)) w_j:
+//     y_j = u_j - sum_{i<j} s_i (y_i . w_j) y_i,   s_j = 1 / (r_j + w_j . y_j).
+// With Gamma(l, j) = u_l . w_j, the elimination H(j, .) = Gamma(j, .) - sum_{i<j} s_i
+// H(i, j) H(i, .) gives s_j = 1 / (r_j + H(j, j)) and N(j, i) = s_i H(i, j), and
+// (I + N) Y = U.  So a block is: U += W Ptil (Ptil symmetric), Gamma = U W^T, the
+// 16 x 16 elimination on one warp, Y by forward substitution per channel, kappa_j =
+// s_j G_j y_j, and Ptil += diag(dacc) - Y^T diag(s) Y.  The reference is the middle
+// of the block's log decay, and a block ends early where some channel's log decay
+// would exceed kBlockLogDecay (one token at least; a single token beyond it takes its
+// own decay as the reference), so every factor stays within e^{+-20} and Ptil within
+// e^{-40} of P.
+constexpr int kTB = 16;                   // tokens per block
+constexpr int kLP = 132;                  // row stride (floats) of Ptil in shared memory
+constexpr int kLT = 132;                  // row stride of the [16][128] token tiles
+constexpr float kBlockLogDecay = 40.0f;
+constexpr int kBlockThreads = 512;
+constexpr size_t kBlockSmem = sizeof(float) * (128 * kLP + 5 * kTB * kLT + kTB * 17 + 2 * kTB + 128 + 4);
+
+template <typename TIO>
+__device__ __forceinline__ void load4(const TIO* p, float (&x)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&x)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xffff0000u);
+    x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+
+// C[16][8 w ..] (+)= A[16][128] B[128][8 w ..] for warp w (A rows of stride la, B rows of
+// stride lb): 3xTF32 m16n8k8 MMAs whose three products and two halves of the K steps
+// go to six accumulators, so the dependent chains are 8 MMAs long instead of 48.
+__device__ __forceinline__ void warp_row16_x_panel(const float* A, int la, const float* B, int lb, float* C, int lc,
+                                                   int c0) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    float acc[6][4];
+#pragma unroll
+    for (int u = 0; u < 6; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[u][e] = 0.0f;
+#pragma unroll 4
+    for (int ks = 0; ks < 16; ++ks) {
+        const int k0 = 8 * ks, hk = 3 * (ks & 1);
+        uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
+        split_tf32(A[g * la + k0 + q], ah[0], al[0]);
+        split_tf32(A[(g + 8) * la + k0 + q], ah[1], al[1]);
+        split_tf32(A[g * la + k0 + q + 4], ah[2], al[2]);
+        split_tf32(A[(g + 8) * la + k0 + q + 4], ah[3], al[3]);
+        split_tf32(B[(k0 + q) * lb + c0 + g], bh0, bl0);
+        split_tf32(B[(k0 + q + 4) * lb + c0 + g], bh1, bl1);
+        mma_m16n8k8_tf32(acc[hk + 0], al, bh0, bh1);
+        mma_m16n8k8_tf32(acc[hk + 1], ah, bl0, bl1);
+        mma_m16n8k8_tf32(acc[hk + 2], ah, bh0, bh1);
+    }
+    float* d0 = C + g * lc + c0 + 2 * q;
+    float* d1 = d0 + 8 * lc;
+    d0[0] += (acc[0][0] + acc[3][0]) + (acc[1][0] + acc[4][0]) + (acc[2][0] + acc[5][0]);
+    d0[1] += (acc[0][1] + acc[3][1]) + (acc[1][1] + acc[4][1]) + (acc[2][1] + acc[5][1]);
+    d1[0] += (acc[0][2] + acc[3][2]) + (acc[1][2] + acc[4][2]) + (acc[2][2] + acc[5][2]);
+    d1[1] += (acc[0][3] + acc[3][3]) + (acc[1][3] + acc[4][3]) + (acc[2][3] + acc[5][3]);
+}
+
+template <typename TIO>
+__global__ void __launch_bounds__(kBlockThreads, 1) dense_cov_block_kernel(DenseArgs a, float* __restrict__ kappa) {
+    constexpr int D = 128;
+    extern __shared__ float4 dyn_smem4[];
+    float* Pt = reinterpret_cast<float*>(dyn_smem4);   // [128][kLP]
+    float* sK = Pt + D * kLP;      // [16][kLT] k, then w = G k
+    float* sG = sK + kTB * kLT;    // [16][kLT] log_alpha, then G
+    float* sO = sG + kTB * kLT;    // [16][kLT] omega, then dacc
+    float* sU = sO + kTB * kLT;    // [16][kLT] u, then s y
+    float* sY = sU + kTB * kLT;    // [16][kLT] y
+    float* sH = sY + kTB * kLT;    // [16][17]  Gamma, then N below the diagonal
+    float* sR = sH + kTB * 17;     // [16]      r
+    float* sS = sR + kTB;          // [16]      s
+    float* sF = sS + kTB;          // [128]     scaling of Ptil at the block start
+    int* sM = reinterpret_cast<int*>(sF + D);   // tokens in the block
+
+    const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const TIO* kin = static_cast<const TIO*>(a.k);
+    const size_t ts = static_cast<size_t>(a.H) * D;
+    const size_t row0 = static_cast<size_t>(b) * a.T * ts + static_cast<size_t>(h) * D;
+    const size_t sb = static_cast<size_t>(bh) * D * D;
+
+    for (int e = tid; e < D * D / 4; e += kBlockThreads) {
+        const int r = e >> 5, c = (e & 31) * 4;
+        float4 v;
+        if (a.P0) v = *reinterpret_cast<const float4*>(a.P0 + sb + static_cast<size_t>(r) * D + c);
+        else v = make_float4(r == c ? 1.f : 0.f, r == c + 1 ? 1.f : 0.f, r == c + 2 ? 1.f : 0.f, r == c + 3 ? 1.f : 0.f);
+        *reinterpret_cast<float4*>(Pt + r * kLP + c) = v;
+    }
+    // staging: token j = warp of a tile, channels 4 lane .. 4 lane + 3; registers hold
+    // the next tile while a block runs
+    const int sj = warp, sc = 4 * lane;
+    float xk[4], xl[4], xw[4], xr = 1.0f;
+    auto load_tile = [&](int t0) {
+        const int t = t0 + sj;
+        if (t < a.T) {
+            const size_t e = row0 + static_cast<size_t>(t) * ts + sc;
+            load4<TIO>(kin + e, xk);
+            load4<float>(a.log_alpha + e, xl);
+            load4<float>(a.omega + e, xw);
+            xr = a.r[(static_cast<size_t>(b) * a.T + t) * a.H + h];
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) xk[c] = xl[c] = xw[c] = 0.0f;
+            xr = 1.0f;
+        }
+    };
+    float prev_end = 0.0f;   // channel tid: log decay at the end of the last block, relative to its reference
+    int t0 = 0;
+    if (a.T > 0) load_tile(0);
+    while (t0 < a.T) {
+        *reinterpret_cast<float4*>(sK + sj * kLT + sc) = make_float4(xk[0], xk[1], xk[2], xk[3]);
+        *reinterpret_cast<float4*>(sG + sj * kLT + sc) = make_float4(xl[0], xl[1], xl[2], xl[3]);
+        *reinterpret_cast<float4*>(sO + sj * kLT + sc) = make_float4(xw[0], xw[1], xw[2], xw[3]);
+        if (lane == 0) sR[sj] = xr;
+        if (tid == 0) *sM = min(kTB, a.T - t0);
+        __syncthreads();
+        // ---- block length: up to the first token whose log decay from the block start
+        //      leaves kBlockLogDecay on some channel (the first token always counts)
+        if (tid < D) {
+            float L = 0.0f;
+            int mi = kTB;
+#pragma unroll
+            for (int j = 0; j < kTB; ++j) {
+                L += sG[j * kLT + tid];
+                if (j > 0 && mi == kTB && !(fabsf(L) <= kBlockLogDecay)) mi = j;
+            }
+            mi = __reduce_min_sync(0xffffffffu, mi);
+            if (lane == 0) atomicMin(sM, mi);
+        }
+        __syncthreads();
+        const int m = *sM;
+        // ---- per channel: decay factors G_j about the reference, w = G k, dacc, u = dacc w,
+        //      and the scaling of Ptil into this block's frame
+        if (tid < D) {
+            const int i = tid;
+            float L = 0.0f;   // log decay of the block's m tokens (the same sums as above)
+#pragma unroll
+            for (int j = 0; j < kTB; ++j)
+                if (j < m) L += sG[j * kLT + i];
+            const float ref = fabsf(L) > kBlockLogDecay ? L : 0.5f * L;
+            sF[i] = expf(ref + prev_end);
+            prev_end = L - ref;
+            float dd = 0.0f, lj = 0.0f;
+#pragma unroll
+            for (int j = 0; j < kTB; ++j) {
+                float g = 1.0f, w = 0.0f;
+                if (j < m) {
+                    lj += sG[j * kLT + i];
+                    g = exp2f((lj - ref) * 1.4426950408889634f);
+                    w = g * sK[j * kLT + i];
+                    dd += __fdividef(sO[j * kLT + i], g * g);
+                }
+                sK[j * kLT + i] = w;
+                sG[j * kLT + i] = g;
+                sO[j * kLT + i] = dd;
+                sU[j * kLT + i] = dd * w;
+            }
+        }
+        if (tid < kTB && tid >= m) sR[tid] = 1.0f;   // (tokens of the tile not in this block)
+        __syncthreads();
+#pragma unroll 2
+        for (int e = tid; e < D * D / 4; e += kBlockThreads) {   // Ptil <- F Ptil F
+            const int r = e >> 5, c = (e & 31) * 4;
+            float4 x = *reinterpret_cast<float4*>(Pt + r * kLP + c);
+            const float4 f = *reinterpret_cast<const float4*>(sF + c);
+            const float fr = sF[r];
+            x.x *= fr * f.x; x.y *= fr * f.y; x.z *= fr * f.z; x.w *= fr * f.w;
+            *reinterpret_cast<float4*>(Pt + r * kLP + c) = x;
+        }
+        if (m == kTB && t0 + kTB < a.T) load_tile(t0 + kTB);
+        __syncthreads();
+        // ---- U += W Ptil (warp w: columns 8 w .. 8 w + 7)
+        warp_row16_x_panel(sK, kLT, Pt, kLP, sU, kLT, 8 * warp);
+        __syncthreads();
+        {   // ---- Gamma(l, j) = u_l . w_j: two threads per entry, each a half of the channels
+            //      (interleaved 4-channel groups, so the two halves sit in different banks)
+            const int o = tid >> 1, hh = tid & 1, l = o >> 4, j = o & 15;
+            const float* ur = sU + l * kLT + 4 * hh;
+            const float* wr = sK + j * kLT + 4 * hh;
+            float acc = 0.0f;
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {
+                const float4 x = *reinterpret_cast<const float4*>(ur + 8 * v);
+                const float4 y = *reinterpret_cast<const float4*>(wr + 8 * v);
+                acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            if (hh == 0) sH[l * 17 + j] = acc;
+        }
+        __syncthreads();
+        // ---- the elimination (warp 0)
+        if (warp == 0) {
+            float hc[kTB], rr[kTB];   // lane k: column k of H; r
+#pragma unroll
+            for (int j = 0; j < kTB; ++j) {
+                hc[j] = sH[j * 17 + (lane & 15)];
+                rr[j] = sR[j];
+            }
+            __syncwarp();
+            float sv = 0.0f;   // lane j: s_j
+#pragma unroll
+            for (int j = 0; j < kTB; ++j) {
+                const float sj_ = __fdividef(1.0f, rr[j] + __shfl_sync(0xffffffffu, hc[j], j));
+                if (lane == j) sv = sj_;
+                // lane jp > j: N(jp, j) = s_j H(j, jp), its own H(j, jp) (column jp)
+                if (lane > j && lane < kTB) sH[lane * 17 + j] = sj_ * hc[j];
+#pragma unroll
+                for (int jp = j + 1; jp < kTB; ++jp)
+                    hc[jp] = fmaf(-sj_ * __shfl_sync(0xffffffffu, hc[j], jp), hc[j], hc[jp]);
+            }
+            if (lane < kTB) sS[lane] = sv;
+        }
+        __syncthreads();
+        // ---- Y = (I + N)^{-1} U per channel, kappa, s y; diag(dacc) into Ptil
+        if (tid < D) {
+            const int c = tid;
+            float y[kTB];
+#pragma unroll
+            for (int j = 0; j < kTB; ++j) {
+                float acc = sU[j * kLT + c];
+#pragma unroll
+                for (int i = 0; i < j; ++i) acc = fmaf(-sH[j * 17 + i], y[i], acc);
+                y[j] = acc;
+            }
+#pragma unroll
+            for (int j = 0; j < kTB; ++j) {
+                const float s = sS[j];
+                sY[j * kLT + c] = y[j];
+                sU[j * kLT + c] = s * y[j];
+                if (j < m) kappa[row0 + static_cast<size_t>(t0 + j) * ts + c] = s * sG[j * kLT + c] * y[j];
+            }
+            Pt[c * kLP + c] += sO[(kTB - 1) * kLT + c];
+        }
+        __syncthreads();
+        // ---- Ptil -= (s Y)^T Y
+        smem_gemm<4>(D, D, kTB, sU, 1, kLT, sY, kLT, 1, Pt, kLP, -1.0f, true);
+        t0 += m;
+        if (m < kTB && t0 < a.T) load_tile(t0);   // (the prefetched tile started elsewhere)
+        __syncthreads();
+    }
+    // P_T = E Ptil E, E = e^{log decay at the end of the last block, relative to its reference}
+    if (tid < D) sF[tid] = expf(prev_end);
+    __syncthreads();
+    for (int e = tid; e < D * D / 4; e += kBlockThreads) {
+        const int r = e >> 5, c = (e & 31) * 4;
+        const float4 x = *reinterpret_cast<const float4*>(Pt + r * kLP + c);
+        const float fr = sF[r];
+        *reinterpret_cast<float4*>(a.P_T + sb + static_cast<size_t>(r) * D + c) =
+            make_float4(fr * sF[c] * x.x, fr * sF[c + 1] * x.y, fr * sF[c + 2] * x.z, fr * sF[c + 3] * x.w);
+    }
+}
+
 template <int D>
 cudaError_t launch_d(const DenseArgs& a, float* kappa, cudaStream_t s) {
     const int grid = a.B * a.H;
     if (grid == 0) return cudaSuccess;
+    if constexpr (D == 128) {
+        // token blocks on tensor cores
+        auto kern = a.io == 1 ? dense_cov_block_kernel<__nv_bfloat16> : dense_cov_block_kernel<float>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kBlockSmem));
+        kern<<<grid, kBlockThreads, kBlockSmem, s>>>(a, kappa);
+        return cudaGetLastError();
+    }
     if (a.io == 1)
         dense_cov_kernel<D, __nv_bfloat16><<<grid, 4 * D, 0, s>>>(a, kappa);
     else
