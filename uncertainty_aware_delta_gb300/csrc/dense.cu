@@ -386,7 +386,7 @@ constexpr int kLP = 132;                  // row stride (floats) of Ptil in shar
 constexpr int kLT = 132;                  // row stride of the [16][128] token tiles
 constexpr float kBlockLogDecay = 40.0f;
 constexpr int kBlockThreads = 512;
-constexpr size_t kBlockSmem = sizeof(float) * (128 * kLP + 5 * kTB * kLT + kTB * 17 + 2 * kTB + 128 + 4);
+constexpr size_t kBlockSmem = sizeof(float) * (128 * kLP + 7 * kTB * kLT + kTB * 17 + 2 * kTB + 128 + 4);
 
 template <typename TIO>
 __device__ __forceinline__ void load4(const TIO* p, float (&x)[4]);
@@ -402,11 +402,12 @@ __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, flo
     x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xffff0000u);
 }
 
-// C[16][8 w ..] (+)= A[16][128] B[128][8 w ..] for warp w (A rows of stride la, B rows of
-// stride lb): 3xTF32 m16n8k8 MMAs whose three products and two halves of the K steps
-// go to six accumulators, so the dependent chains are 8 MMAs long instead of 48.
-__device__ __forceinline__ void warp_row16_x_panel(const float* A, int la, const float* B, int lb, float* C, int lc,
-                                                   int c0) {
+// C[16][c0 + 8 columns] += f_c (A[16][128] B[128][c0 ..]) for one warp: A given as its
+// TF32 high and low parts (rows of stride la), B rows of stride lb split here.  3xTF32
+// m16n8k8 MMAs whose three products and two halves of the K steps go to six
+// accumulators, so the dependent chains are 8 MMAs long instead of 48.
+__device__ __forceinline__ void warp_row16_x_panel(const uint32_t* Ah, const uint32_t* Al, int la, const float* B,
+                                                   int lb, float* C, int lc, int c0, const float* f) {
     const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
     float acc[6][4];
 #pragma unroll
@@ -416,23 +417,71 @@ __device__ __forceinline__ void warp_row16_x_panel(const float* A, int la, const
 #pragma unroll 4
     for (int ks = 0; ks < 16; ++ks) {
         const int k0 = 8 * ks, hk = 3 * (ks & 1);
-        uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
-        split_tf32(A[g * la + k0 + q], ah[0], al[0]);
-        split_tf32(A[(g + 8) * la + k0 + q], ah[1], al[1]);
-        split_tf32(A[g * la + k0 + q + 4], ah[2], al[2]);
-        split_tf32(A[(g + 8) * la + k0 + q + 4], ah[3], al[3]);
+        const uint32_t ah[4] = {Ah[g * la + k0 + q], Ah[(g + 8) * la + k0 + q], Ah[g * la + k0 + q + 4],
+                                Ah[(g + 8) * la + k0 + q + 4]};
+        const uint32_t al[4] = {Al[g * la + k0 + q], Al[(g + 8) * la + k0 + q], Al[g * la + k0 + q + 4],
+                                Al[(g + 8) * la + k0 + q + 4]};
+        uint32_t bh0, bl0, bh1, bl1;
         split_tf32(B[(k0 + q) * lb + c0 + g], bh0, bl0);
         split_tf32(B[(k0 + q + 4) * lb + c0 + g], bh1, bl1);
         mma_m16n8k8_tf32(acc[hk + 0], al, bh0, bh1);
         mma_m16n8k8_tf32(acc[hk + 1], ah, bl0, bl1);
         mma_m16n8k8_tf32(acc[hk + 2], ah, bh0, bh1);
     }
+    const float f0 = f[c0 + 2 * q], f1 = f[c0 + 2 * q + 1];
     float* d0 = C + g * lc + c0 + 2 * q;
     float* d1 = d0 + 8 * lc;
-    d0[0] += (acc[0][0] + acc[3][0]) + (acc[1][0] + acc[4][0]) + (acc[2][0] + acc[5][0]);
-    d0[1] += (acc[0][1] + acc[3][1]) + (acc[1][1] + acc[4][1]) + (acc[2][1] + acc[5][1]);
-    d1[0] += (acc[0][2] + acc[3][2]) + (acc[1][2] + acc[4][2]) + (acc[2][2] + acc[5][2]);
-    d1[1] += (acc[0][3] + acc[3][3]) + (acc[1][3] + acc[4][3]) + (acc[2][3] + acc[5][3]);
+    d0[0] += f0 * ((acc[0][0] + acc[3][0]) + (acc[1][0] + acc[4][0]) + (acc[2][0] + acc[5][0]));
+    d0[1] += f1 * ((acc[0][1] + acc[3][1]) + (acc[1][1] + acc[4][1]) + (acc[2][1] + acc[5][1]));
+    d1[0] += f0 * ((acc[0][2] + acc[3][2]) + (acc[1][2] + acc[4][2]) + (acc[2][2] + acc[5][2]));
+    d1[1] += f1 * ((acc[0][3] + acc[3][3]) + (acc[1][3] + acc[4][3]) + (acc[2][3] + acc[5][3]));
+}
+
+// The block's update of Ptil for one warp (rows 16 (w >> 1) .., columns 64 (w & 1) ..):
+//     Ptil <- F Ptil F + diag(dacc) - (s Y)^T Y
+// (the frame change into this block, its diagonal increments and its rank-16 downdate
+// in one read-modify-write), the product on 3xTF32 m16n8k8 MMAs (K = 16 tokens).
+__device__ __forceinline__ void warp_block_update(const float* Ys, const float* Y, int lt, float* P, int lp,
+                                                  const float* f, const float* dacc, int warp) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const int r0 = 16 * (warp >> 1), cb = 64 * (warp & 1);
+    float acc[8][4];
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[n][e] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const int k0 = 8 * ks;
+        uint32_t ah[4], al[4];   // A(r, j) = (s y_j)[r]
+        split_tf32(Ys[(k0 + q) * lt + r0 + g], ah[0], al[0]);
+        split_tf32(Ys[(k0 + q) * lt + r0 + g + 8], ah[1], al[1]);
+        split_tf32(Ys[(k0 + q + 4) * lt + r0 + g], ah[2], al[2]);
+        split_tf32(Ys[(k0 + q + 4) * lt + r0 + g + 8], ah[3], al[3]);
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            const int c = cb + 8 * n + g;
+            uint32_t bh0, bl0, bh1, bl1;
+            split_tf32(Y[(k0 + q) * lt + c], bh0, bl0);
+            split_tf32(Y[(k0 + q + 4) * lt + c], bh1, bl1);
+            mma_m16n8k8_tf32(acc[n], al, bh0, bh1);
+            mma_m16n8k8_tf32(acc[n], ah, bl0, bl1);
+            mma_m16n8k8_tf32(acc[n], ah, bh0, bh1);
+        }
+    }
+    const int ra = r0 + g, rb = ra + 8;
+    const float fa = f[ra], fb = f[rb];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+        const int c = cb + 8 * n + 2 * q;
+        const float fc0 = f[c], fc1 = f[c + 1];
+        float* pa = P + ra * lp + c;
+        float* pb = P + rb * lp + c;
+        pa[0] = fmaf(fa * fc0, pa[0], (ra == c ? dacc[ra] : 0.0f) - acc[n][0]);
+        pa[1] = fmaf(fa * fc1, pa[1], (ra == c + 1 ? dacc[ra] : 0.0f) - acc[n][1]);
+        pb[0] = fmaf(fb * fc0, pb[0], (rb == c ? dacc[rb] : 0.0f) - acc[n][2]);
+        pb[1] = fmaf(fb * fc1, pb[1], (rb == c + 1 ? dacc[rb] : 0.0f) - acc[n][3]);
+    }
 }
 
 template <typename TIO>
@@ -445,7 +494,9 @@ __global__ void __launch_bounds__(kBlockThreads, 1) dense_cov_block_kernel(Dense
     float* sO = sG + kTB * kLT;    // [16][kLT] omega, then dacc
     float* sU = sO + kTB * kLT;    // [16][kLT] u, then s y
     float* sY = sU + kTB * kLT;    // [16][kLT] y
-    float* sH = sY + kTB * kLT;    // [16][17]  Gamma, then N below the diagonal
+    uint32_t* sWh = reinterpret_cast<uint32_t*>(sY + kTB * kLT);   // [16][kLT] w f, TF32 high part
+    uint32_t* sWl = sWh + kTB * kLT;                                 // [16][kLT] and low part
+    float* sH = reinterpret_cast<float*>(sWl + kTB * kLT);   // [16][17]  Gamma, then N below the diagonal
     float* sR = sH + kTB * 17;     // [16]      r
     float* sS = sR + kTB;          // [16]      s
     float* sF = sS + kTB;          // [128]     scaling of Ptil at the block start
@@ -483,7 +534,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) dense_cov_block_kernel(Dense
             xr = 1.0f;
         }
     };
-    float prev_end = 0.0f;   // channel tid: log decay at the end of the last block, relative to its reference
+    float prev_end = 0.0f;   // channel tid >> 2: log decay at the end of the last block, relative to its reference
     int t0 = 0;
     if (a.T > 0) load_tile(0);
     while (t0 < a.T) {
@@ -493,15 +544,32 @@ __global__ void __launch_bounds__(kBlockThreads, 1) dense_cov_block_kernel(Dense
         if (lane == 0) sR[sj] = xr;
         if (tid == 0) *sM = min(kTB, a.T - t0);
         __syncthreads();
+        // Per-channel work runs on four threads per channel (channel tid >> 2, tokens
+        // 4 p .. 4 p + 3 of the tile for p = tid & 3), the sums over tokens as scans over
+        // the four lanes.
+        const int ci = tid >> 2, cp = tid & 3;
+        auto scan4 = [&](float x) {   // inclusive scan over the four lanes of a channel
+            float y = __shfl_up_sync(0xffffffffu, x, 1, 4);
+            if (cp >= 1) x += y;
+            y = __shfl_up_sync(0xffffffffu, x, 2, 4);
+            if (cp >= 2) x += y;
+            return x;
+        };
         // ---- block length: up to the first token whose log decay from the block start
         //      leaves kBlockLogDecay on some channel (the first token always counts)
-        if (tid < D) {
-            float L = 0.0f;
+        {
+            float loc[4], acc = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc += sG[(4 * cp + e) * kLT + ci];
+                loc[e] = acc;
+            }
+            const float off = scan4(acc) - acc;
             int mi = kTB;
 #pragma unroll
-            for (int j = 0; j < kTB; ++j) {
-                L += sG[j * kLT + tid];
-                if (j > 0 && mi == kTB && !(fabsf(L) <= kBlockLogDecay)) mi = j;
+            for (int e = 3; e >= 0; --e) {
+                const int j = 4 * cp + e;
+                if (j > 0 && !(fabsf(off + loc[e]) <= kBlockLogDecay)) mi = j;
             }
             mi = __reduce_min_sync(0xffffffffu, mi);
             if (lane == 0) atomicMin(sM, mi);
@@ -510,46 +578,54 @@ __global__ void __launch_bounds__(kBlockThreads, 1) dense_cov_block_kernel(Dense
         const int m = *sM;
         // ---- per channel: decay factors G_j about the reference, w = G k, dacc, u = dacc w,
         //      and the scaling of Ptil into this block's frame
-        if (tid < D) {
-            const int i = tid;
-            float L = 0.0f;   // log decay of the block's m tokens (the same sums as above)
+        {
+            float loc[4], acc = 0.0f;
 #pragma unroll
-            for (int j = 0; j < kTB; ++j)
-                if (j < m) L += sG[j * kLT + i];
+            for (int e = 0; e < 4; ++e) {
+                if (4 * cp + e < m) acc += sG[(4 * cp + e) * kLT + ci];
+                loc[e] = acc;
+            }
+            const float incl = scan4(acc), off = incl - acc;
+            const float L = __shfl_sync(0xffffffffu, incl, 3, 4);   // log decay of the block's m tokens
             const float ref = fabsf(L) > kBlockLogDecay ? L : 0.5f * L;
-            sF[i] = expf(ref + prev_end);
+            const float fi = expf(ref + prev_end);
+            if (cp == 0) sF[ci] = fi;
             prev_end = L - ref;
-            float dd = 0.0f, lj = 0.0f;
+            float gq[4], wq[4], tq[4], dacc_loc = 0.0f;
 #pragma unroll
-            for (int j = 0; j < kTB; ++j) {
-                float g = 1.0f, w = 0.0f;
+            for (int e = 0; e < 4; ++e) {
+                const int j = 4 * cp + e;
+                gq[e] = 1.0f;
+                wq[e] = 0.0f;
+                tq[e] = 0.0f;
                 if (j < m) {
-                    lj += sG[j * kLT + i];
-                    g = exp2f((lj - ref) * 1.4426950408889634f);
-                    w = g * sK[j * kLT + i];
-                    dd += __fdividef(sO[j * kLT + i], g * g);
+                    gq[e] = exp2f((off + loc[e] - ref) * 1.4426950408889634f);
+                    wq[e] = gq[e] * sK[j * kLT + ci];
+                    dacc_loc += __fdividef(sO[j * kLT + ci], gq[e] * gq[e]);
                 }
-                sK[j * kLT + i] = w;
-                sG[j * kLT + i] = g;
-                sO[j * kLT + i] = dd;
-                sU[j * kLT + i] = dd * w;
+                tq[e] = dacc_loc;
+            }
+            const float doff = scan4(dacc_loc) - dacc_loc;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = 4 * cp + e;
+                const float dd = doff + tq[e];
+                sK[j * kLT + ci] = wq[e];
+                sG[j * kLT + ci] = gq[e];
+                sO[j * kLT + ci] = dd;
+                sU[j * kLT + ci] = dd * wq[e];
+                uint32_t wh, wl;   // (w f: the product below reads Ptil before its change of frame)
+                split_tf32(wq[e] * fi, wh, wl);
+                sWh[j * kLT + ci] = wh;
+                sWl[j * kLT + ci] = wl;
             }
         }
         if (tid < kTB && tid >= m) sR[tid] = 1.0f;   // (tokens of the tile not in this block)
-        __syncthreads();
-#pragma unroll 2
-        for (int e = tid; e < D * D / 4; e += kBlockThreads) {   // Ptil <- F Ptil F
-            const int r = e >> 5, c = (e & 31) * 4;
-            float4 x = *reinterpret_cast<float4*>(Pt + r * kLP + c);
-            const float4 f = *reinterpret_cast<const float4*>(sF + c);
-            const float fr = sF[r];
-            x.x *= fr * f.x; x.y *= fr * f.y; x.z *= fr * f.z; x.w *= fr * f.w;
-            *reinterpret_cast<float4*>(Pt + r * kLP + c) = x;
-        }
         if (m == kTB && t0 + kTB < a.T) load_tile(t0 + kTB);
         __syncthreads();
-        // ---- U += W Ptil (warp w: columns 8 w .. 8 w + 7)
-        warp_row16_x_panel(sK, kLT, Pt, kLP, sU, kLT, 8 * warp);
+        // ---- U += W (F Ptil F) (warp w: columns 8 w .. 8 w + 7; Ptil still in the last
+        //      block's frame)
+        warp_row16_x_panel(sWh, sWl, kLT, Pt, kLP, sU, kLT, 8 * warp, sF);
         __syncthreads();
         {   // ---- Gamma(l, j) = u_l . w_j: two threads per entry, each a half of the channels
             //      (interleaved 4-channel groups, so the two halves sit in different banks)
@@ -608,17 +684,16 @@ __global__ void __launch_bounds__(kBlockThreads, 1) dense_cov_block_kernel(Dense
                 sU[j * kLT + c] = s * y[j];
                 if (j < m) kappa[row0 + static_cast<size_t>(t0 + j) * ts + c] = s * sG[j * kLT + c] * y[j];
             }
-            Pt[c * kLP + c] += sO[(kTB - 1) * kLT + c];
         }
         __syncthreads();
-        // ---- Ptil -= (s Y)^T Y
-        smem_gemm<4>(D, D, kTB, sU, 1, kLT, sY, kLT, 1, Pt, kLP, -1.0f, true);
+        // ---- Ptil <- F Ptil F + diag(dacc) - (s Y)^T Y
+        warp_block_update(sU, sY, kLT, Pt, kLP, sF, sO + (kTB - 1) * kLT, warp);
         t0 += m;
         if (m < kTB && t0 < a.T) load_tile(t0);   // (the prefetched tile started elsewhere)
         __syncthreads();
     }
     // P_T = E Ptil E, E = e^{log decay at the end of the last block, relative to its reference}
-    if (tid < D) sF[tid] = expf(prev_end);
+    if ((tid & 3) == 0) sF[tid >> 2] = expf(prev_end);
     __syncthreads();
     for (int e = tid; e < D * D / 4; e += kBlockThreads) {
         const int r = e >> 5, c = (e & 31) * 4;
