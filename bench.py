@@ -718,12 +718,15 @@ def other_workloads(torch, kdn, WORKLOADS, device, barrier, peaks):
     flops = dense_algorithmic_flops(w.B, w.T, w.H, w.d)
     peak = dense_alu_peak_tflops(torch, device)
     out[w.name] = {"tokens_per_s": w.B * w.T / (ms / 1e3), "ms": ms,
-                   "kernels": "dense_cov_kernel + kdn_fused_tc_kernel (given gains)",
+                   "kernels": "dense_cov_block_kernel + kdn_fused_tc_kernel (given gains)",
+                   "traffic": {k: traffic_for(k, w.name) for k in ("dense_cov_block_kernel", "kdn_fused_tc_kernel")},
                    "outputs_finite": finite, "P_T_asymmetry": asym, "device_status": kdn.kdn_read_device_status(dws),
                    "bound": "alu", "algorithmic_flops": flops, "achieved_tflops": flops / (ms / 1e3) / 1e12,
                    "peak_tflops": peak, "alu_frac": flops / (ms / 1e3) / 1e12 / peak,
                    "note": "algorithmic flops are the plain filter's 13 d^2 per token-head; the covariance "
-                           "pass executes 4 d^2 (decay held outside P) and the mean runs chunkwise on tensor cores",
+                           "pass runs 16-token blocks (decay held outside P, the products on warp-level 3xTF32 "
+                           "tensor cores) and the mean runs chunkwise on tcgen05 tensor cores; the peak is the "
+                           "fp32 CUDA-core rate, so alu_frac is an effective fraction",
                    "peak_source": "SM count x 128 fp32 lanes x 2 flop x 2070 MHz (maximum SM clock)"}
     del x, dws
     # backward pass of the diagonal forward on the headline shape (fp32 CUDA cores)
