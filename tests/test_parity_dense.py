@@ -188,3 +188,28 @@ def test_dense_strong_decay_renormalises(io, d):
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(S_T)) and np.all(np.isfinite(P_T))
     e = _check(got, _reference(x), io, f"strong decay {io} d={d}")
     print(f"[parity] dense strong decay {io} d={d}: {e}")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_dense_blocks_end_early_on_concentrated_decay(io):
+    """For d = 128 the covariance pass runs blocks of up to 16 tokens, and a block
+    ends where some channel's log decay from the block start would exceed 40.
+    Eight tokens of log decay -6 on a few channels end blocks early, and one token of
+    log decay -45 on one channel is a block of its own, taken about its own decay.
+    The result must still be the fp64 filter's, through both mean paths."""
+    import torch
+
+    kdn = _kdn()
+    B, T, H, d = 1, 100, 2, 128
+    x = make_inputs("diag", B, T, H, d, d, io=io, seed=4242)
+    x["log_alpha"][:, 20:28, 0, :4] = -6.0
+    x["log_alpha"][:, 60, 1, 5] = -45.0
+    t = to_device(x)
+    ws = torch.empty(kdn.dense_workspace_size(B, T, H, d, kdn.KDN_BF16 if io == "bf16" else kdn.KDN_F32),
+                     dtype=torch.uint8, device="cuda")
+    got = kdn.kdn_dense_forward(t["q"], t["k"], t["v"], t["log_alpha"], t["omega"], t["r"], workspace=ws)
+    assert kdn.kdn_read_device_status(ws) == 0
+    o, S_T, P_T = (to_host(a) for a in got)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S_T)) and np.all(np.isfinite(P_T))
+    e = _check(got, _reference(x), io, f"blocks end early {io}")
+    print(f"[parity] dense blocks ending early {io}: {e}")
