@@ -438,11 +438,12 @@ __device__ __forceinline__ void warp_row16_x_panel(const uint32_t* Ah, const uin
 }
 
 // The block's update of Ptil for one warp (rows 16 (w >> 1) .., columns 64 (w & 1) ..):
-//     Ptil <- F Ptil F + diag(dacc) - (s Y)^T Y
-// (the frame change into this block, its diagonal increments and its rank-16 downdate
-// in one read-modify-write), the product on 3xTF32 m16n8k8 MMAs (K = 16 tokens).
+//     Ptil <- F Ptil F - (s Y)^T Y
+// (the frame change into this block and its rank-16 downdate in one read-modify-write;
+// the diagonal increments follow after a barrier), the product on 3xTF32 m16n8k8 MMAs
+// (K = 16 tokens).
 __device__ __forceinline__ void warp_block_update(const float* Ys, const float* Y, int lt, float* P, int lp,
-                                                  const float* f, const float* dacc, int warp) {
+                                                  const float* f, int warp) {
     const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
     const int r0 = 16 * (warp >> 1), cb = 64 * (warp & 1);
     float acc[8][4];
@@ -477,10 +478,10 @@ __device__ __forceinline__ void warp_block_update(const float* Ys, const float* 
         const float fc0 = f[c], fc1 = f[c + 1];
         float* pa = P + ra * lp + c;
         float* pb = P + rb * lp + c;
-        pa[0] = fmaf(fa * fc0, pa[0], (ra == c ? dacc[ra] : 0.0f) - acc[n][0]);
-        pa[1] = fmaf(fa * fc1, pa[1], (ra == c + 1 ? dacc[ra] : 0.0f) - acc[n][1]);
-        pb[0] = fmaf(fb * fc0, pb[0], (rb == c ? dacc[rb] : 0.0f) - acc[n][2]);
-        pb[1] = fmaf(fb * fc1, pb[1], (rb == c + 1 ? dacc[rb] : 0.0f) - acc[n][3]);
+        pa[0] = fmaf(fa * fc0, pa[0], -acc[n][0]);
+        pa[1] = fmaf(fa * fc1, pa[1], -acc[n][1]);
+        pb[0] = fmaf(fb * fc0, pb[0], -acc[n][2]);
+        pb[1] = fmaf(fb * fc1, pb[1], -acc[n][3]);
     }
 }
 
@@ -535,6 +536,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) dense_cov_block_kernel(Dense
         }
     };
     float prev_end = 0.0f;   // channel tid >> 2: log decay at the end of the last block, relative to its reference
+    float dfold = 0.0f;      // channel tid (< 128): the block's diagonal increment
     int t0 = 0;
     if (a.T > 0) load_tile(0);
     while (t0 < a.T) {
@@ -684,13 +686,15 @@ __global__ void __launch_bounds__(kBlockThreads, 1) dense_cov_block_kernel(Dense
                 sU[j * kLT + c] = s * y[j];
                 if (j < m) kappa[row0 + static_cast<size_t>(t0 + j) * ts + c] = s * sG[j * kLT + c] * y[j];
             }
+            dfold = sO[(kTB - 1) * kLT + c];
         }
         __syncthreads();
-        // ---- Ptil <- F Ptil F + diag(dacc) - (s Y)^T Y
-        warp_block_update(sU, sY, kLT, Pt, kLP, sF, sO + (kTB - 1) * kLT, warp);
+        // ---- Ptil <- F Ptil F - (s Y)^T Y, then + diag(dacc)
+        warp_block_update(sU, sY, kLT, Pt, kLP, sF, warp);
         t0 += m;
         if (m < kTB && t0 < a.T) load_tile(t0);   // (the prefetched tile started elsewhere)
         __syncthreads();
+        if (tid < D) Pt[tid * kLP + tid] += dfold;
     }
     // P_T = E Ptil E, E = e^{log decay at the end of the last block, relative to its reference}
     if ((tid & 3) == 0) sF[tid >> 2] = expf(prev_end);
