@@ -328,12 +328,17 @@ kdn_status kdn_pkda_step(int B, int H, int dk, int dv, float x, int io_dtype,
  * Outputs: o [B,T,H,d] io_dtype; S_T, P_T [B,H,d,d] fp32 (the state after token
  *          T-1; S_T == S0 and P_T == P0 are allowed).
  * Sizes  : d in {32, 64, 128} (d_k = d_v = d); any T >= 0; B, H >= 0.
- * Two passes.  The covariance recurrence runs token by token, one CTA per head
- * with P in registers, and writes the gains kappa_t [B,T,H,d] fp32 into the
- * workspace (with the decay held outside P: P_t = G_t Ptil_t G_t for the
- * running product G_t of the decays, so a token costs one matrix-vector product
- * and one rank-1 downdate, 2 d^2 multiply-adds; G is folded into Ptil whenever a
- * channel's running decay would fall below 2^-20).  Given the gains, the mean
+ * Two passes.  The covariance recurrence runs in token order, one CTA per head,
+ * and writes the gains kappa_t [B,T,H,d] fp32 into the workspace.  The decay is
+ * held outside P (P = G Ptil G for a diagonal G of decay factors), so a token
+ * costs one matrix-vector product and one rank-1 downdate, 2 d^2 multiply-adds.
+ * For d = 128 the tokens go in blocks of up to 16 with Ptil in shared memory:
+ * the block's products run on tensor cores (3xTF32, fp32-level accuracy) and a
+ * 16 x 16 elimination gives every token's gain from the block-start covariance.
+ * A block ends early where a channel's log decay within it would exceed 40.  For
+ * d = 32 and 64 the tokens go in pairs with Ptil in registers, and G is folded
+ * into Ptil whenever a channel's running decay would fall below 2^-20.  Given
+ * the gains, the mean
  * S = diag(a) S + kappa (v - (diag(a) S)^T k)^T is the delta rule with write
  * key kappa and runs chunkwise: on the fused tensor-core kernel (bf16 io,
  * d = 128, T > 32) or on the CUDA-core chunk path.
